@@ -1,0 +1,441 @@
+#!/usr/bin/env python
+"""Benchmark of batch-invariant selected-token log-probabilities on GB300.
+
+One step = one call of the fused LM-head projection + logprob path
+(lp_linear_logprob: the tensor-core kernel, then the fixed-order merge kernel)
+on the Qwen3-8B head shape: T=512 rows, d=4096, V=151936, bf16 H and W,
+int64 targets, fp32 logp and entropy out.  Inputs are seeded synthetic tensors
+(random-init weights of that shape), resident in HBM before timing; W (1.245
+GB) is larger than L2, so no flush is needed between steps.
+
+Printed: one JSON line with the step throughput in selected-token logprobs/s,
+the roofline of the dominant kernel (timed alone with CUDA events recorded by
+the library around it), the fp64 CPU oracle timed on a sample on this host,
+an end-to-end figure through the C ABI with host buffers, SM clocks sampled
+during the timed region, and a secondary line item for the logits-given path
+on the peaked 1024 x 151936 fp32 logits.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lp|reference]
+For N > 1 launch one process per GPU with torch.distributed.run; every rank
+runs its own batch of rows (weak scaling, no collective on the data path) and
+rank 0 prints the whole-job throughput over the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "selected-token logprobs/sec at T=512,d=4096,V=151936 bf16; % of roofline"
+WORKLOAD = "fused_qwen3_8b"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "lp_linear_kernel.fused_qwen3_8b.txt")
+LINEAR_SOURCE = os.path.join(ROOT, "invariant_token_logprobs_gb300", "csrc", "lp_linear.cu")
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["lp", "reference"], default="lp")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-logits", action="store_true", help="skip the logits-path line item")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target CPU time of the oracle baseline sample")
+    return p.parse_args(argv)
+
+
+# --------------------------------------------------------------------- helpers
+
+def load_peaks():
+    if os.path.exists(PEAKS_FILE):
+        with open(PEAKS_FILE) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def sha256_file(path: str) -> str:
+    h = hashlib.sha256()
+    with open(path, "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()
+
+
+def profile_traffic():
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
+    or None when absent or taken on a different kernel source."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    fields = {}
+    with open(PROFILE_SUMMARY) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+    if fields.get("source_sha256") != sha256_file(LINEAR_SOURCE):
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, period_ms: int = 20):
+        self.device_index = device_index
+        self.period_ms = period_ms
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="lp_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        t0 = time.time()
+        while time.time() - t0 < 5.0:  # wait for the first sample
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self, t_begin: float, t_end: float):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 10:
+                        continue
+                    try:
+                        ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                        rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+                    except ValueError:
+                        continue
+            os.unlink(self.path)
+        inside = [r for r in rows if t_begin - 0.05 <= r[0] <= t_end + 0.05]
+        use = inside if inside else rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i in range(4) if r[3][i].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(inside),
+                "window": "timed region" if inside else "nearest samples (timed region shorter than sampling)"}
+
+
+# ------------------------------------------------------------- CPU oracle legs
+
+def oracle_sample_seconds(h_host, w_host, y_host, rows):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.linear_selected_logprob(h_host[rows], w_host, y_host[rows])
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(x, budget_s: float):
+    """The fp64 oracle as it stands on a sample of rows of the same workload."""
+    import numpy as np
+    h = x.H.float().cpu().numpy()
+    w = x.W.float().cpu().numpy()
+    y = x.y.cpu().numpy()
+    T = h.shape[0]
+    t8 = oracle_sample_seconds(h, w, y, np.arange(8))
+    per_row = max(t8 / 8.0, 1e-4)
+    n = int(min(T, max(8, budget_s / per_row)))
+    rows = np.linspace(0, T - 1, n).astype(np.int64)
+    sec = oracle_sample_seconds(h, w, y, rows)
+    return {"value": n / sec, "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
+            "sample": f"{n} of {T} rows of {WORKLOAD} (d=4096, full V=151936), fp64 numpy oracle, "
+                      f"{sec:.1f} s"}
+
+
+def run_reference(args):
+    """--impl reference: the fp64 CPU oracle, timed per step on a bounded row sample."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import torch
+    from invariant_token_logprobs_gb300 import synth
+    import oracle
+
+    torch.set_num_threads(host_cores())
+    x = synth.fused_inputs(WORKLOAD, device="cpu")
+    h = x.H.float().numpy()
+    w64 = x.W.double().numpy()  # the oracle's own dtype, converted once outside the steps
+    y = x.y.numpy()
+    T = h.shape[0]
+    # size each step so the whole run stays within about two minutes
+    t0 = time.perf_counter()
+    oracle.linear_selected_logprob(h[:4], w64, y[:4])
+    per4 = time.perf_counter() - t0
+    per_step_budget = max(0.05, 120.0 / max(1, args.steps + args.warmup))
+    rows_per_step = int(max(1, min(T, 4 * per_step_budget / max(per4, 1e-6))))
+    rng = np.random.default_rng(0)
+    for _ in range(args.warmup):
+        r = rng.integers(0, T, rows_per_step)
+        oracle.linear_selected_logprob(h[r], w64, y[r])
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        r = rng.integers(0, T, rows_per_step)
+        oracle.linear_selected_logprob(h[r], w64, y[r])
+    sec = time.perf_counter() - t0
+    value = rows_per_step * args.steps / sec
+    sample = (f"{rows_per_step} random rows of {WORKLOAD} per step (d=4096, full V=151936), "
+              f"fp64 numpy oracle, W pre-converted to fp64")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sec / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "T": T, "d": 4096, "V": 151936, "seed": 2,
+                   "rows_per_step": rows_per_step},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": host_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# -------------------------------------------------------------------- GPU arm
+
+def run_lp(args):
+    import torch
+    import torch.distributed as dist
+    from invariant_token_logprobs_gb300 import lp, synth
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = lp.load()
+    peaks, peaks_kind = load_peaks()
+
+    spec = synth.WORKLOADS[WORKLOAD]
+    x = synth.fused_inputs(WORKLOAD, device=dev, seed=spec.seed + 1000 * rank)
+    T, d = x.H.shape
+    V = x.W.shape[0]
+    ws = torch.empty(lp.lp_linear_logprob_workspace_size(T, d, V), dtype=torch.uint8, device=dev)
+    logp = torch.empty(T, device=dev)
+    ent = torch.empty(T, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v: float) -> float:
+        if world == 1:
+            return v
+        t = torch.tensor([v], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(max(3, args.warmup)):
+        lp.lp_linear_logprob(x.H, x.W, x.y, logp, ent, ws)
+    K = args.steps
+    k_start = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    k_stop = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    for ev in k_start + k_stop:  # torch creates an event on its first record
+        ev.record(stream)
+    barrier()
+    torch.cuda.synchronize()
+    t_begin = time.time()
+    ev0.record(stream)
+    for i in range(K):
+        lp.lp_set_kernel_timing_events(k_start[i], k_stop[i])
+        lp.lp_linear_logprob(x.H, x.W, x.y, logp, ent, ws)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_end = time.time()
+    barrier()
+    lp.lp_set_kernel_timing_events(None, None)
+    sampler.stop()
+    clocks = sampler.summary(t_begin, t_end)
+    err_word = lp.lp_get_device_error(ws)
+    if err_word != 0:
+        raise RuntimeError(f"device-side wait gave up (error word {err_word})")
+
+    total_ms = max_over_ranks(ev0.elapsed_time(ev1))
+    kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(k_start, k_stop))
+    kernel_ms = max_over_ranks(kernel_ms)
+    ms_per_step = total_ms / K
+    value = world * T * K / (total_ms / 1e3)
+
+    flops = 2.0 * T * d * V
+    w_bytes = 2.0 * V * d + 2.0 * T * d + 8.0 * T + 8.0 * T
+    peak_tf = peaks["bf16_tflops"]
+    achieved_tf = flops / (kernel_ms / 1e3) / 1e12
+    roofline_us = max(flops / (peak_tf * 1e12), w_bytes / (peaks["hbm_gbs"] * 1e9)) * 1e6
+    roofline = {
+        "bound": "tensor", "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s",
+        "frac": achieved_tf / peak_tf, "traffic": profile_traffic(),
+        "kernel": "lp_linear_kernel", "kernel_us": kernel_ms * 1e3,
+        "algorithmic_flops_per_launch": flops, "roofline_us": roofline_us,
+        "peak_source": f"{peaks_kind} bf16 burst ({'MEASURED_PEAKS.json' if peaks_kind == 'measured' else 'fallback'})",
+    }
+
+    # end to end through the C ABI with host buffers: H and targets copied in
+    # from pinned memory, logp and entropy copied out, every step
+    h_host = x.H.cpu().pin_memory()
+    y_host = x.y.cpu().pin_memory()
+    lp_host = torch.empty(T, pin_memory=True)
+    ent_host = torch.empty(T, pin_memory=True)
+    h_dev = torch.empty_like(x.H)
+    y_dev = torch.empty_like(x.y)
+    K2 = max(1, min(K, 100))
+    for _ in range(3):
+        h_dev.copy_(h_host, non_blocking=True)
+        y_dev.copy_(y_host, non_blocking=True)
+        lp.lp_linear_logprob(h_dev, x.W, y_dev, logp, ent, ws)
+        lp_host.copy_(logp, non_blocking=True)
+        ent_host.copy_(ent, non_blocking=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K2):
+        h_dev.copy_(h_host, non_blocking=True)
+        y_dev.copy_(y_host, non_blocking=True)
+        lp.lp_linear_logprob(h_dev, x.W, y_dev, logp, ent, ws)
+        lp_host.copy_(logp, non_blocking=True)
+        ent_host.copy_(ent, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
+    e2e = {"value": world * T * K2 / (e2e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": h_host.numel() * h_host.element_size() + y_host.numel() * 8,
+           "d2h_bytes_per_step": 8 * T, "steps": K2,
+           "note": "W (the LM-head weight) is resident model state; per step H and targets go in and logp/entropy come out"}
+
+    logits_item = None
+    if not args.no_logits:
+        del h_host
+        logits_item = bench_logits(lp, synth, torch, dev, stream, peaks, peaks_kind, max_over_ranks,
+                                   world, rank)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(x, args.cpu_seconds)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded bf16 H (RMS-normalised N(0,1)) and W ~ N(0, 0.02^2), uniform targets",
+        "config": {"workload": WORKLOAD, "T": T, "d": d, "V": V, "seed": spec.seed,
+                   "rows_per_gpu": T, "l2": "inputs larger than L2 (W = 1.245 GB), no flush",
+                   "parallelism": f"replicas x{world} (rows partitioned, no collective)"},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+        "backend": lp.lp_backend_id(),
+        "logits_path": logits_item,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def bench_logits(lp, synth, torch, dev, stream, peaks, peaks_kind, max_over_ranks, world, rank):
+    """Secondary line item: the logits-given path on the peaked workload."""
+    z = synth.logits_inputs("logits_peaked", device=dev, seed=1 + 1000 * rank)
+    T, V = z.z.shape
+    logp = torch.empty(T, device=dev)
+    ent = torch.empty(T, device=dev)
+    for _ in range(5):
+        lp.lp_logprob_from_logits(z.z, z.y, logp, ent)
+    K = 50
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(K):
+        lp.lp_logprob_from_logits(z.z, z.y, logp, ent)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1)) / K
+    nbytes = 4.0 * T * V + 8.0 * T + 8.0 * T
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"workload": "logits_peaked", "T": T, "V": V, "value": world * T / (ms / 1e3),
+            "unit": "rows/s", "us_per_call": ms * 1e3, "gpu_launches_per_call": 1,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                         "kernel": "lp_logits_final_kernel",
+                         "algorithmic_bytes_per_launch": nbytes,
+                         "peak_source": f"{peaks_kind} copy bandwidth"}}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_lp(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,251 @@
+/*
+ * lp.h: C ABI of liblp, batch-invariant selected-token log-probabilities on
+ * GB300 (sm_103a).
+ *
+ * For every row t of a logits matrix z[T, V] and its selected token y_t the
+ * library computes
+ *
+ *     logp[t]    = z[t, y_t] - log sum_v exp z[t, v]
+ *     entropy[t] = -sum_v p[t, v] log p[t, v],   p[t, :] = softmax(z[t, :])
+ *
+ * in float32 output.  This is the selected-token log-probability that every
+ * candidate of the RL-Kernel logprob prior-art report (report.json, kind
+ * qwen3_next_logprob_prior_art, field "candidates") computes from shared
+ * logits, and the "linear_logp" operator (rlkernel.linear_logp.bitwise.v1 in
+ * the backend readbacks of the RL-Kernel H100 PCP evidence record,
+ * h100-pcp.json, section "validation") when the logits are the LM-head
+ * projection z = H W^T.  The entropy is the per-row quantity the trainer logs
+ * as train/entropy_loss (h100-pcp.json, section "comparison").
+ *
+ * Results are bitwise identical for a given row whatever batch it sits in, at
+ * whatever offset, whatever number of vocabulary shards (1, 2 or 4) it is split
+ * into, and however often the call is repeated: the properties batch_bitwise,
+ * tp4_equals_tp1 and distinct_results_in_repeats == 1 of the prior-art report.
+ * The reduction over the vocabulary is cut into four fixed "quarters"
+ * [floor(q V / 4), floor((q+1) V / 4)), q = 0..3; each quarter is reduced in a
+ * fixed order and the quarters are merged as (Q0 + Q1) + (Q2 + Q3).
+ *
+ * Conventions for every entry point:
+ *  - Memory: every pointer argument is DEVICE memory owned by the caller,
+ *    except the array of shard pointers of lp_merge_partials, which lives on
+ *    the host (its elements are device pointers).  The library never
+ *    allocates or frees memory; the fused path takes a caller-provided
+ *    workspace sized by its query function.
+ *  - Streams: all work is enqueued on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream).  Calls do not synchronise with the host.
+ *  - Errors: argument errors are detected on the host and returned before
+ *    anything is enqueued; outputs are then untouched.  A failed launch
+ *    returns LP_ERR_CUDA.  Errors found on the device never fault: a target
+ *    outside [0, V) gives logp = NaN for that row (its entropy is still
+ *    valid); a pipeline wait that exceeds its time bound sets the workspace
+ *    error word (read it with lp_get_device_error) and that call's outputs
+ *    are NaN.
+ *  - Device: the current CUDA device must have compute capability 10.3
+ *    (sm_103a).  Any other device gives LP_ERR_UNSUPPORTED_DEVICE; there is no
+ *    fallback.
+ *  - Types: logits and outputs are float32; H and W are bfloat16 (raw 16-bit
+ *    storage, passed as void*); targets are int64.  Strides are in elements.
+ */
+#ifndef LP_H_
+#define LP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LP_API __attribute__((visibility("default")))
+#else
+#define LP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum lp_status {
+  LP_OK = 0,
+  LP_ERR_INVALID_ARGUMENT = 1,   /* null pointer, bad size or stride, bad shard */
+  LP_ERR_MISALIGNED = 2,         /* a pointer or stride breaks an alignment rule */
+  LP_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3 */
+  LP_ERR_WORKSPACE_TOO_SMALL = 4,
+  LP_ERR_CUDA = 5,               /* a CUDA runtime or driver call failed */
+  LP_ERR_TIMEOUT = 6             /* a device-side wait gave up (see lp_get_device_error) */
+} lp_status;
+
+/* ------------------------------------------------------------------------
+ * Logits given: a bandwidth-bound streaming reduction of fp32 logits.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * lp_logprob_from_logits: logp and (optionally) entropy of every row of
+ * fp32 logits, as the prior-art report's candidates compute them from shared
+ * logits (report.json, "candidates", "reference": "shared_logits_fp64").
+ *
+ *   logits      [T, V] float32, row r at logits + r * ld_logits; 4-byte aligned.
+ *               Rows whose start is 16-byte aligned are read with 128-bit loads;
+ *               others with scalar loads (same arithmetic, same result).
+ *   ld_logits   row stride in elements, >= V.
+ *   targets     [T] int64 selected token per row (8-byte aligned).
+ *   T           rows, >= 0 (T == 0 returns LP_OK and enqueues nothing).
+ *   V           vocabulary size, 1 <= V < 2^31.
+ *   logp_out    [T] float32.
+ *   entropy_out [T] float32, or NULL to skip the entropy output.
+ *   stream      cudaStream_t.
+ */
+LP_API lp_status lp_logprob_from_logits(const float* logits, int64_t ld_logits,
+                                 const int64_t* targets, int64_t T, int64_t V,
+                                 float* logp_out, float* entropy_out,
+                                 void* stream);
+
+/*
+ * lp_vocab_shard_range: the global vocabulary columns [*begin, *end) that
+ * shard `shard_index` of `n_shards` (1, 2 or 4) contiguous shards covers:
+ * begin = floor(shard_index * V / n_shards).  A shard is a whole number of
+ * quarters, so its per-row partial states merge bitwise-identically to the
+ * unsharded result (the single-GPU form of the prior-art report's
+ * tp4_equals_tp1 property).  Pure host function.
+ */
+LP_API lp_status lp_vocab_shard_range(int64_t vocab_total, int shard_index, int n_shards,
+                               int64_t* begin, int64_t* end);
+
+/*
+ * lp_logprob_partials_from_logits: per-row quarter states of one vocabulary
+ * shard of fp32 logits.
+ *
+ *   logits_shard [T, end - begin] float32: the shard's columns only (column 0
+ *                is global column `begin`, see lp_vocab_shard_range).  May be
+ *                NULL for an empty shard (possible only when vocab_total < 4).
+ *   ld_logits    row stride in elements, >= end - begin.
+ *   targets      [T] int64 GLOBAL token ids.
+ *   vocab_total  V of the unsharded vocabulary.
+ *   shard_index, n_shards: which shard (n_shards in {1, 2, 4}).
+ *   partials_out [T][4 / n_shards][4] float32 (16-byte aligned): for each row
+ *                and quarter of the shard, the state (m, s, u, t): the
+ *                quarter's maximum logit m, s = sum exp(z - m),
+ *                u = sum exp(z - m) (z - m), and the target logit t (-inf when
+ *                the target is not in this quarter, NaN when the target is
+ *                outside [0, vocab_total)).
+ */
+LP_API lp_status lp_logprob_partials_from_logits(const float* logits_shard, int64_t ld_logits,
+                                          const int64_t* targets, int64_t T,
+                                          int64_t vocab_total, int shard_index,
+                                          int n_shards, float* partials_out,
+                                          void* stream);
+
+/*
+ * lp_merge_partials: merge the quarter states of 1, 2 or 4 shards in the fixed
+ * order (Q0 + Q1) + (Q2 + Q3) and finalise logp and entropy.
+ *
+ *   shard_partials  HOST array of n_shards DEVICE pointers, in shard order;
+ *                   element i is shard i's partials_out ([T][4 / n_shards][4]
+ *                   float32, 16-byte aligned) from either partials entry point.
+ *   n_shards        1, 2 or 4.
+ *   logp_out        [T] float32; entropy_out [T] float32 or NULL.
+ */
+LP_API lp_status lp_merge_partials(const float* const* shard_partials, int n_shards,
+                            int64_t T, float* logp_out, float* entropy_out,
+                            void* stream);
+
+/* ------------------------------------------------------------------------
+ * Fused LM-head projection + logprob ("linear_logp"): z = H W^T is formed
+ * tile by tile in tensor memory (tcgen05, bf16 inputs, fp32 accumulation) and
+ * reduced on the fly; the T x V logits never reach global memory.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * lp_linear_logprob_workspace_size: bytes of workspace lp_linear_logprob needs
+ * for T rows and vocabulary V (d does not change it).  The workspace holds a
+ * 256-byte header (the device error word) and one 16-byte state per row and
+ * 256-column vocabulary tile.
+ */
+LP_API size_t lp_linear_logprob_workspace_size(int64_t T, int64_t d, int64_t V);
+
+/*
+ * lp_linear_logprob: logp and entropy of softmax(H W^T) per row.
+ *
+ *   H           [T, d] bfloat16, row r at H + r * ld_h (elements); 16-byte
+ *               aligned; ld_h % 8 == 0 and ld_h >= d.
+ *   W           [V, d] bfloat16 LM-head weight, row v at W + v * ld_w; 16-byte
+ *               aligned; ld_w % 8 == 0 and ld_w >= d.
+ *   targets     [T] int64.
+ *   T >= 0, 1 <= d < 2^31, 1 <= V < 2^31.
+ *   logp_out    [T] float32; entropy_out [T] float32 or NULL.
+ *   workspace   device memory, 256-byte aligned, at least
+ *               lp_linear_logprob_workspace_size(T, d, V) bytes; its contents
+ *               on entry do not matter.  Do not share one workspace between
+ *               calls that may run concurrently.
+ */
+LP_API lp_status lp_linear_logprob(const void* H, int64_t ld_h, const void* W, int64_t ld_w,
+                            const int64_t* targets, int64_t T, int64_t d, int64_t V,
+                            float* logp_out, float* entropy_out,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * lp_linear_logprob_partials_workspace_size: workspace bytes for one shard.
+ */
+LP_API size_t lp_linear_logprob_partials_workspace_size(int64_t T, int64_t d,
+                                                 int64_t vocab_total, int n_shards);
+
+/*
+ * lp_linear_logprob_partials: the quarter states of one vocabulary shard of the
+ * fused path, to be merged by lp_merge_partials.
+ *
+ *   W_shard     [end - begin, d] bfloat16: rows [begin, end) of the full W,
+ *               (see lp_vocab_shard_range), row 0 = global row `begin`.  A
+ *               shard that is empty (possible only when vocab_total < 4) must
+ *               still point to one readable row; it contributes nothing.
+ *   targets     [T] int64 GLOBAL token ids.
+ *   partials_out [T][4 / n_shards][4] float32, layout as in
+ *               lp_logprob_partials_from_logits.
+ *   Other arguments as in lp_linear_logprob.
+ */
+LP_API lp_status lp_linear_logprob_partials(const void* H, int64_t ld_h, const void* W_shard,
+                                     int64_t ld_w, const int64_t* targets, int64_t T,
+                                     int64_t d, int64_t vocab_total, int shard_index,
+                                     int n_shards, float* partials_out,
+                                     void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics and tuning.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * lp_get_device_error: read the error word of a fused-path workspace after the
+ * call that used it (synchronises `stream`).  Returns LP_OK when no
+ * device-side wait gave up, LP_ERR_TIMEOUT when one did (then *word_out, if
+ * not NULL, holds which pipeline role gave up: bit 0 loader, bit 1 MMA issuer,
+ * bit 2 epilogue), LP_ERR_CUDA if the read failed.
+ */
+LP_API lp_status lp_get_device_error(const void* workspace, size_t workspace_bytes,
+                              uint32_t* word_out, void* stream);
+
+/*
+ * lp_set_persistent_grid_limit: cap the number of persistent CTAs of the fused
+ * kernel (0 = one per SM, the default).  Results do not depend on it: the work
+ * is cut into fixed tiles whatever the grid (the single-GPU analogue of the
+ * report's nccl_setting_invariant property).  Process-wide setting.
+ */
+LP_API lp_status lp_set_persistent_grid_limit(int max_ctas);
+
+/*
+ * lp_set_kernel_timing_events: diagnostics.  When both are non-NULL, every
+ * later fused-path call records `start_event` on its stream immediately before
+ * its tensor-core kernel (the dominant kernel) and `stop_event` immediately
+ * after it, so a caller can time that kernel alone with cudaEventElapsedTime.
+ * Arguments are cudaEvent_t handles owned by the caller; pass NULL, NULL to
+ * stop recording.  Process-wide setting; not for concurrent callers.
+ */
+LP_API lp_status lp_set_kernel_timing_events(void* start_event, void* stop_event);
+
+/* Human-readable name of a status code (static storage). */
+LP_API const char* lp_status_string(lp_status status);
+
+/* Fixed identifier of this backend, "lp.sm103a.bitwise.v1". */
+LP_API const char* lp_backend_id(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LP_H_ */

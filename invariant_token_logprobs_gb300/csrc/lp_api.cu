@@ -1,0 +1,269 @@
+// lp_api.cu: the C-ABI front end of liblp (declared in include/lp.h).
+//
+// Every entry point validates its arguments on the host, in this order:
+// sizes and null pointers (LP_ERR_INVALID_ARGUMENT), alignment
+// (LP_ERR_MISALIGNED), workspace size (LP_ERR_WORKSPACE_TOO_SMALL), and only
+// then the current device (LP_ERR_UNSUPPORTED_DEVICE unless compute capability
+// 10.3).  Nothing is enqueued before all checks pass.  There is no fallback
+// path of any kind: on another device, or without a device, calls fail.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "lp_device.cuh"
+#include "lp_internal.h"
+
+namespace lp {
+
+namespace {
+std::atomic<int> g_grid_limit{0};
+std::atomic<cudaEvent_t> g_ev_start{nullptr};
+std::atomic<cudaEvent_t> g_ev_stop{nullptr};
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_dev_state[kMaxDevices];  // 0 unknown, 1 supported, 2 unsupported
+std::atomic<int> g_dev_sms[kMaxDevices];
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+}  // namespace
+
+int persistent_grid_limit() { return g_grid_limit.load(std::memory_order_relaxed); }
+
+void timing_events(cudaEvent_t* start, cudaEvent_t* stop) {
+  *start = g_ev_start.load(std::memory_order_acquire);
+  *stop = g_ev_stop.load(std::memory_order_acquire);
+}
+
+lp_status current_device(Device* dev) {
+  int ordinal = 0;
+  if (cudaGetDevice(&ordinal) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of a missing device
+    return LP_ERR_UNSUPPORTED_DEVICE;
+  }
+  if (ordinal < 0 || ordinal >= kMaxDevices) return LP_ERR_UNSUPPORTED_DEVICE;
+  int state = g_dev_state[ordinal].load(std::memory_order_acquire);
+  if (state == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, ordinal) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, ordinal) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, ordinal) != cudaSuccess) {
+      cudaGetLastError();
+      return LP_ERR_CUDA;
+    }
+    g_dev_sms[ordinal].store(sms, std::memory_order_relaxed);
+    state = (major == 10 && minor == 3) ? 1 : 2;
+    g_dev_state[ordinal].store(state, std::memory_order_release);
+  }
+  if (state != 1) return LP_ERR_UNSUPPORTED_DEVICE;
+  dev->ordinal = ordinal;
+  dev->sm_count = g_dev_sms[ordinal].load(std::memory_order_relaxed);
+  return LP_OK;
+}
+
+namespace {
+
+lp_status check_shard(int shard_index, int n_shards) {
+  if (!(n_shards == 1 || n_shards == 2 || n_shards == 4)) return LP_ERR_INVALID_ARGUMENT;
+  if (shard_index < 0 || shard_index >= n_shards) return LP_ERR_INVALID_ARGUMENT;
+  return LP_OK;
+}
+
+lp_status check_fused_args(const void* H, int64_t ld_h, const void* W, int64_t ld_w,
+                           const int64_t* targets, int64_t T, int64_t d, int64_t V) {
+  if (T < 0 || T > kMaxDim || d < 1 || d > kMaxDim || V < 1 || V > kMaxDim)
+    return LP_ERR_INVALID_ARGUMENT;
+  if (ld_h < d || ld_w < d) return LP_ERR_INVALID_ARGUMENT;
+  if (T == 0) return LP_OK;
+  if (H == nullptr || W == nullptr || targets == nullptr) return LP_ERR_INVALID_ARGUMENT;
+  if (!aligned(H, 16) || !aligned(W, 16) || (ld_h % 8) != 0 || (ld_w % 8) != 0 ||
+      !aligned(targets, 8))
+    return LP_ERR_MISALIGNED;
+  return LP_OK;
+}
+
+}  // namespace
+}  // namespace lp
+
+
+extern "C" {
+
+const char* lp_status_string(lp_status status) {
+  switch (status) {
+    case LP_OK: return "LP_OK";
+    case LP_ERR_INVALID_ARGUMENT: return "LP_ERR_INVALID_ARGUMENT";
+    case LP_ERR_MISALIGNED: return "LP_ERR_MISALIGNED";
+    case LP_ERR_UNSUPPORTED_DEVICE: return "LP_ERR_UNSUPPORTED_DEVICE";
+    case LP_ERR_WORKSPACE_TOO_SMALL: return "LP_ERR_WORKSPACE_TOO_SMALL";
+    case LP_ERR_CUDA: return "LP_ERR_CUDA";
+    case LP_ERR_TIMEOUT: return "LP_ERR_TIMEOUT";
+  }
+  return "LP_ERR_UNKNOWN";
+}
+
+const char* lp_backend_id(void) { return "lp.sm103a.bitwise.v1"; }
+
+lp_status lp_set_persistent_grid_limit(int max_ctas) {
+  if (max_ctas < 0) return LP_ERR_INVALID_ARGUMENT;
+  lp::g_grid_limit.store(max_ctas, std::memory_order_relaxed);
+  return LP_OK;
+}
+
+lp_status lp_set_kernel_timing_events(void* start_event, void* stop_event) {
+  if ((start_event == nullptr) != (stop_event == nullptr)) return LP_ERR_INVALID_ARGUMENT;
+  lp::g_ev_start.store(static_cast<cudaEvent_t>(start_event), std::memory_order_release);
+  lp::g_ev_stop.store(static_cast<cudaEvent_t>(stop_event), std::memory_order_release);
+  return LP_OK;
+}
+
+lp_status lp_vocab_shard_range(int64_t vocab_total, int shard_index, int n_shards,
+                               int64_t* begin, int64_t* end) {
+  if (vocab_total < 1 || vocab_total > lp::kMaxDim || begin == nullptr || end == nullptr)
+    return LP_ERR_INVALID_ARGUMENT;
+  const lp_status st = lp::check_shard(shard_index, n_shards);
+  if (st != LP_OK) return st;
+  int q_first, n_q;
+  lp::shard_quarters(shard_index, n_shards, q_first, n_q);
+  *begin = lp::quarter_begin(vocab_total, q_first);
+  *end = lp::quarter_begin(vocab_total, q_first + n_q);
+  return LP_OK;
+}
+
+lp_status lp_logprob_from_logits(const float* logits, int64_t ld_logits, const int64_t* targets,
+                                 int64_t T, int64_t V, float* logp_out, float* entropy_out,
+                                 void* stream) {
+  if (T < 0 || T > lp::kMaxDim / 4 || V < 1 || V > lp::kMaxDim || ld_logits < V)
+    return LP_ERR_INVALID_ARGUMENT;
+  if (T == 0) return LP_OK;
+  if (logits == nullptr || targets == nullptr || logp_out == nullptr)
+    return LP_ERR_INVALID_ARGUMENT;
+  if (!lp::aligned(logits, 4) || !lp::aligned(targets, 8) || !lp::aligned(logp_out, 4) ||
+      !lp::aligned(entropy_out, 4))
+    return LP_ERR_MISALIGNED;
+  lp::Device dev;
+  const lp_status st = lp::current_device(&dev);
+  if (st != LP_OK) return st;
+  return lp::launch_logits_final(logits, ld_logits, targets, T, V, logp_out, entropy_out,
+                                 static_cast<cudaStream_t>(stream));
+}
+
+lp_status lp_logprob_partials_from_logits(const float* logits_shard, int64_t ld_logits,
+                                          const int64_t* targets, int64_t T,
+                                          int64_t vocab_total, int shard_index, int n_shards,
+                                          float* partials_out, void* stream) {
+  lp_status st = lp::check_shard(shard_index, n_shards);
+  if (st != LP_OK) return st;
+  if (T < 0 || T > lp::kMaxDim / 4 || vocab_total < 1 || vocab_total > lp::kMaxDim)
+    return LP_ERR_INVALID_ARGUMENT;
+  int64_t b, e;
+  lp_vocab_shard_range(vocab_total, shard_index, n_shards, &b, &e);
+  if (ld_logits < e - b || ld_logits < 1) return LP_ERR_INVALID_ARGUMENT;
+  if (T == 0) return LP_OK;
+  // an empty shard (vocab_total < 4 only) reads no logits and may pass NULL
+  if ((logits_shard == nullptr && e > b) || targets == nullptr || partials_out == nullptr)
+    return LP_ERR_INVALID_ARGUMENT;
+  if (!lp::aligned(logits_shard, 4) || !lp::aligned(targets, 8) ||
+      !lp::aligned(partials_out, 16))
+    return LP_ERR_MISALIGNED;
+  lp::Device dev;
+  st = lp::current_device(&dev);
+  if (st != LP_OK) return st;
+  int q_first, n_q;
+  lp::shard_quarters(shard_index, n_shards, q_first, n_q);
+  return lp::launch_logits_partials(logits_shard, ld_logits, targets, T, vocab_total, q_first,
+                                    n_q, partials_out, static_cast<cudaStream_t>(stream));
+}
+
+lp_status lp_merge_partials(const float* const* shard_partials, int n_shards, int64_t T,
+                            float* logp_out, float* entropy_out, void* stream) {
+  if (!(n_shards == 1 || n_shards == 2 || n_shards == 4)) return LP_ERR_INVALID_ARGUMENT;
+  if (T < 0 || T > lp::kMaxDim) return LP_ERR_INVALID_ARGUMENT;
+  if (T == 0) return LP_OK;
+  if (shard_partials == nullptr || logp_out == nullptr) return LP_ERR_INVALID_ARGUMENT;
+  for (int i = 0; i < n_shards; ++i) {
+    if (shard_partials[i] == nullptr) return LP_ERR_INVALID_ARGUMENT;
+    if (!lp::aligned(shard_partials[i], 16)) return LP_ERR_MISALIGNED;
+  }
+  if (!lp::aligned(logp_out, 4) || !lp::aligned(entropy_out, 4)) return LP_ERR_MISALIGNED;
+  lp::Device dev;
+  const lp_status st = lp::current_device(&dev);
+  if (st != LP_OK) return st;
+  return lp::launch_merge_partials(shard_partials, n_shards, T, logp_out, entropy_out,
+                                   static_cast<cudaStream_t>(stream));
+}
+
+size_t lp_linear_logprob_workspace_size(int64_t T, int64_t d, int64_t V) {
+  (void)d;
+  if (T < 0 || V < 1 || V > lp::kMaxDim) return 0;
+  return lp::linear_workspace_bytes(T, V, 4);
+}
+
+size_t lp_linear_logprob_partials_workspace_size(int64_t T, int64_t d, int64_t vocab_total,
+                                                 int n_shards) {
+  (void)d;
+  if (T < 0 || vocab_total < 1 || vocab_total > lp::kMaxDim) return 0;
+  if (!(n_shards == 1 || n_shards == 2 || n_shards == 4)) return 0;
+  return lp::linear_workspace_bytes(T, vocab_total, 4 / n_shards);
+}
+
+lp_status lp_linear_logprob(const void* H, int64_t ld_h, const void* W, int64_t ld_w,
+                            const int64_t* targets, int64_t T, int64_t d, int64_t V,
+                            float* logp_out, float* entropy_out, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  lp_status st = lp::check_fused_args(H, ld_h, W, ld_w, targets, T, d, V);
+  if (st != LP_OK || T == 0) return st;
+  if (logp_out == nullptr || workspace == nullptr) return LP_ERR_INVALID_ARGUMENT;
+  if (!lp::aligned(logp_out, 4) || !lp::aligned(entropy_out, 4) || !lp::aligned(workspace, 256))
+    return LP_ERR_MISALIGNED;
+  if (workspace_bytes < lp::linear_workspace_bytes(T, V, 4)) return LP_ERR_WORKSPACE_TOO_SMALL;
+  lp::Device dev;
+  st = lp::current_device(&dev);
+  if (st != LP_OK) return st;
+  return lp::launch_linear(dev, H, ld_h, W, ld_w, targets, T, d, V, 0, 4, logp_out, entropy_out,
+                           nullptr, workspace, static_cast<cudaStream_t>(stream));
+}
+
+lp_status lp_linear_logprob_partials(const void* H, int64_t ld_h, const void* W_shard,
+                                     int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
+                                     int64_t vocab_total, int shard_index, int n_shards,
+                                     float* partials_out, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  lp_status st = lp::check_shard(shard_index, n_shards);
+  if (st != LP_OK) return st;
+  st = lp::check_fused_args(H, ld_h, W_shard, ld_w, targets, T, d, vocab_total);
+  if (st != LP_OK || T == 0) return st;
+  if (partials_out == nullptr || workspace == nullptr) return LP_ERR_INVALID_ARGUMENT;
+  if (!lp::aligned(partials_out, 16) || !lp::aligned(workspace, 256)) return LP_ERR_MISALIGNED;
+  int q_first, n_q;
+  lp::shard_quarters(shard_index, n_shards, q_first, n_q);
+  if (workspace_bytes < lp::linear_workspace_bytes(T, vocab_total, n_q))
+    return LP_ERR_WORKSPACE_TOO_SMALL;
+  lp::Device dev;
+  st = lp::current_device(&dev);
+  if (st != LP_OK) return st;
+  return lp::launch_linear(dev, H, ld_h, W_shard, ld_w, targets, T, d, vocab_total, q_first, n_q,
+                           nullptr, nullptr, partials_out, workspace,
+                           static_cast<cudaStream_t>(stream));
+}
+
+lp_status lp_get_device_error(const void* workspace, size_t workspace_bytes, uint32_t* word_out,
+                              void* stream) {
+  if (workspace == nullptr || workspace_bytes < lp::kWorkspaceHeader)
+    return LP_ERR_INVALID_ARGUMENT;
+  if (!lp::aligned(workspace, 256)) return LP_ERR_MISALIGNED;
+  lp::Device dev;
+  const lp_status st = lp::current_device(&dev);
+  if (st != LP_OK) return st;
+  uint32_t word = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return LP_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LP_ERR_CUDA;
+  if (word_out != nullptr) *word_out = word;
+  return word == 0 ? LP_OK : LP_ERR_TIMEOUT;
+}
+
+}  // extern "C"

@@ -1,0 +1,133 @@
+// lp_device.cuh: arithmetic shared by every kernel of liblp.
+//
+// The per-row state of a slice of the vocabulary is (m, s, u, t):
+//   m  the slice's maximum logit,
+//   s  sum over the slice of exp(z - m),
+//   u  sum over the slice of exp(z - m) * (z - m),
+//   t  the target logit z[y] when y lies in the slice, -inf when it does not,
+//      NaN when y is outside [0, V).
+// From the states of the four vocabulary quarters the row's results follow:
+//   logp    = (t - M) - log S
+//   entropy = log S - U / S
+// with M the largest m and S, U the quarter sums rebased to M.  This is
+// log-sum-exp of the selected-token log-probability of the RL-Kernel logprob
+// prior-art report (report.json, "candidates") split into slices; entropy uses
+// -sum p log p = log Z - sum p z.
+//
+// Every kernel that forms or merges states goes through the functions below,
+// so a slice's state has one bit pattern whichever kernel or call produced it.
+// The library is compiled with --fmad=false and the arithmetic here uses
+// explicit rounding intrinsics: no multiply-add is contracted differently in
+// different kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace lp {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kQuarters = 4;
+
+__host__ __device__ __forceinline__ int64_t quarter_begin(int64_t V, int q) {
+  return (static_cast<int64_t>(q) * V) / kQuarters;
+}
+
+// exp(x) as exp2(x * log2 e) with CUDA's exp2f.
+__device__ __forceinline__ float exp_f(float x) { return exp2f(__fmul_rn(x, kLog2e)); }
+
+// max that returns NaN when either operand is NaN.
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000u); }
+__device__ __forceinline__ float quiet_nan() { return __int_as_float(0x7fffffffu); }
+
+// Online state of one thread over a sequence of logits.
+struct Online {
+  float m, s, u;
+  __device__ __forceinline__ void reset() {
+    m = neg_inf();
+    s = 0.f;
+    u = 0.f;
+  }
+  // Raise the running maximum to bm (a maximum over the next values, computed
+  // with fmax_nan).  NaN in bm makes the state NaN from here on.
+  __device__ __forceinline__ void raise_to(float bm) {
+    if (!(bm <= m)) {
+      if (m == neg_inf()) {
+        s = 0.f;
+        u = 0.f;
+      } else {
+        const float delta = __fsub_rn(m, bm);  // < 0
+        const float a = exp_f(delta);
+        u = __fmul_rn(a, __fmaf_rn(delta, s, u));
+        s = __fmul_rn(a, s);
+      }
+      m = bm;
+    }
+  }
+  __device__ __forceinline__ bool active() const { return m != neg_inf(); }
+};
+
+// One logit's terms relative to the running maximum m: e = exp(x - m) and the
+// clamped difference d = x - m, so that e * d is 0 for a -inf logit (never
+// 0 * inf) while NaN stays NaN.
+__device__ __forceinline__ void term(float x, float m, float& e, float& d) {
+  d = fmax_nan(__fsub_rn(x, m), -3.402823466e38f);
+  e = exp_f(d);
+}
+
+// Rebase (m, s, u) to a common maximum M >= m: returns (s', u') with
+// s' = e^(m-M) s and u' = e^(m-M) (u + (m - M) s).  An empty state (m = -inf)
+// contributes nothing.
+__device__ __forceinline__ void rebase(float m, float s, float u, float M, float& s_out,
+                                       float& u_out) {
+  if (m == neg_inf()) {
+    s_out = 0.f;
+    u_out = 0.f;
+    return;
+  }
+  const float delta = __fsub_rn(m, M);
+  const float a = exp_f(delta);
+  s_out = __fmul_rn(a, s);
+  u_out = __fmul_rn(a, __fmaf_rn(delta, s, u));
+}
+
+// Final merge of the four quarter states, fixed order (Q0 + Q1) + (Q2 + Q3),
+// in float64, and the row's results.
+__device__ __forceinline__ void finalise(const float4 (&q)[kQuarters], float& logp,
+                                         float& entropy) {
+  const float M = fmaxf(fmaxf(q[0].x, q[1].x), fmaxf(q[2].x, q[3].x));
+  double S_q[kQuarters], U_q[kQuarters];
+#pragma unroll
+  for (int i = 0; i < kQuarters; ++i) {
+    if (q[i].x == neg_inf()) {
+      S_q[i] = 0.0;
+      U_q[i] = 0.0;
+    } else {
+      const double delta = __dsub_rn(static_cast<double>(q[i].x), static_cast<double>(M));
+      const double a = exp(delta);
+      S_q[i] = __dmul_rn(a, static_cast<double>(q[i].y));
+      U_q[i] = __dmul_rn(a, __fma_rn(delta, static_cast<double>(q[i].y),
+                                     static_cast<double>(q[i].z)));
+    }
+  }
+  const double S = __dadd_rn(__dadd_rn(S_q[0], S_q[1]), __dadd_rn(S_q[2], S_q[3]));
+  const double U = __dadd_rn(__dadd_rn(U_q[0], U_q[1]), __dadd_rn(U_q[2], U_q[3]));
+  const float t = fmax_nan(fmax_nan(q[0].w, q[1].w), fmax_nan(q[2].w, q[3].w));
+  if (!(M > neg_inf()) || !(S > 0.0)) {  // no distribution, or NaN somewhere
+    logp = quiet_nan();
+    entropy = quiet_nan();
+    return;
+  }
+  const double log_s = log(S);
+  logp = __double2float_rn(
+      __dsub_rn(__dsub_rn(static_cast<double>(t), static_cast<double>(M)), log_s));
+  entropy = __double2float_rn(__dsub_rn(log_s, __ddiv_rn(U, S)));
+}
+
+}  // namespace lp

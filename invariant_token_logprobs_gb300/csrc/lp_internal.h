@@ -1,0 +1,63 @@
+// lp_internal.h: launchers shared between the C-ABI front end (lp_api.cu) and
+// the kernel translation units.  Arguments reaching these functions have
+// already been validated by the front end.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/lp.h"
+
+namespace lp {
+
+// Header at the start of every fused-path workspace.
+constexpr size_t kWorkspaceHeader = 256;
+// Vocabulary tile width of the fused path (columns of z per tensor-memory tile).
+constexpr int kTileN = 256;
+
+// Error bits of the workspace error word.
+constexpr uint32_t kErrLoader = 1u;
+constexpr uint32_t kErrMma = 2u;
+constexpr uint32_t kErrEpilogue = 4u;
+
+// Quarter range [q_first, q_first + n_q) of shard `shard_index` of `n_shards`.
+inline void shard_quarters(int shard_index, int n_shards, int& q_first, int& n_q) {
+  n_q = 4 / n_shards;
+  q_first = shard_index * n_q;
+}
+
+// Tiles of kTileN columns per quarter; the same for every quarter (a quarter
+// one column narrower than the widest gets a masked tail).
+inline int64_t tiles_per_quarter(int64_t V) {
+  const int64_t wmax = (V + 3) / 4;
+  return (wmax + kTileN - 1) / kTileN;
+}
+
+struct Device {
+  int ordinal;
+  int sm_count;
+};
+lp_status current_device(Device* dev);  // checks compute capability 10.3
+
+// logits path
+lp_status launch_logits_final(const float* logits, int64_t ld, const int64_t* targets,
+                              int64_t T, int64_t V, float* logp, float* entropy,
+                              cudaStream_t stream);
+lp_status launch_logits_partials(const float* logits_shard, int64_t ld,
+                                 const int64_t* targets, int64_t T, int64_t V_total,
+                                 int q_first, int n_q, float* partials, cudaStream_t stream);
+lp_status launch_merge_partials(const float* const* shard_partials, int n_shards, int64_t T,
+                                float* logp, float* entropy, cudaStream_t stream);
+
+// fused path
+size_t linear_workspace_bytes(int64_t T, int64_t V_total, int n_q);
+lp_status launch_linear(const Device& dev, const void* H, int64_t ld_h, const void* W,
+                        int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
+                        int64_t V_total, int q_first, int n_q, float* logp, float* entropy,
+                        float* partials_out, void* workspace, cudaStream_t stream);
+
+int persistent_grid_limit();
+void timing_events(cudaEvent_t* start, cudaEvent_t* stop);
+
+}  // namespace lp

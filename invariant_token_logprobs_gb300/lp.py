@@ -1,0 +1,293 @@
+"""ctypes binding of liblp (the C ABI in include/lp.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of liblp.  PyTorch is used for device memory and the current stream.
+There is no fallback: if the library cannot be loaded, or the current device is
+not a GB300 (compute capability 10.3), calls raise :class:`LpError`.
+
+The ``lp_*`` functions mirror the C entry points one to one and take tensors
+instead of raw pointers; the short names below them (``logprob_from_logits``,
+``linear_logprob``, ...) allocate the outputs and workspace with torch.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional, Sequence
+
+import torch
+
+from . import _build_lib
+
+__all__ = [
+    "LpError",
+    "STATUS",
+    "load",
+    "declared_symbols",
+    "lp_logprob_from_logits",
+    "lp_logprob_partials_from_logits",
+    "lp_merge_partials",
+    "lp_vocab_shard_range",
+    "lp_linear_logprob_workspace_size",
+    "lp_linear_logprob",
+    "lp_linear_logprob_partials_workspace_size",
+    "lp_linear_logprob_partials",
+    "lp_get_device_error",
+    "lp_set_persistent_grid_limit",
+    "lp_set_kernel_timing_events",
+    "lp_status_string",
+    "lp_backend_id",
+    "logprob_from_logits",
+    "logprob_partials_from_logits",
+    "merge_partials",
+    "linear_logprob",
+    "linear_logprob_partials",
+    "vocab_shard_range",
+]
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "lp.h")
+
+STATUS = {
+    0: "LP_OK",
+    1: "LP_ERR_INVALID_ARGUMENT",
+    2: "LP_ERR_MISALIGNED",
+    3: "LP_ERR_UNSUPPORTED_DEVICE",
+    4: "LP_ERR_WORKSPACE_TOO_SMALL",
+    5: "LP_ERR_CUDA",
+    6: "LP_ERR_TIMEOUT",
+}
+
+
+class LpError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+_i64 = ctypes.c_int64
+_int = ctypes.c_int
+_vp = ctypes.c_void_p
+_sz = ctypes.c_size_t
+
+_SIGNATURES = {
+    "lp_logprob_from_logits": (_int, [_vp, _i64, _vp, _i64, _i64, _vp, _vp, _vp]),
+    "lp_vocab_shard_range": (_int, [_i64, _int, _int, ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
+    "lp_logprob_partials_from_logits": (_int, [_vp, _i64, _vp, _i64, _i64, _int, _int, _vp, _vp]),
+    "lp_merge_partials": (_int, [ctypes.POINTER(_vp), _int, _i64, _vp, _vp, _vp]),
+    "lp_linear_logprob_workspace_size": (_sz, [_i64, _i64, _i64]),
+    "lp_linear_logprob": (_int, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _sz, _vp]),
+    "lp_linear_logprob_partials_workspace_size": (_sz, [_i64, _i64, _i64, _int]),
+    "lp_linear_logprob_partials": (
+        _int, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _int, _int, _vp, _vp, _sz, _vp]),
+    "lp_get_device_error": (_int, [_vp, _sz, ctypes.POINTER(ctypes.c_uint32), _vp]),
+    "lp_set_persistent_grid_limit": (_int, [_int]),
+    "lp_set_kernel_timing_events": (_int, [_vp, _vp]),
+    "lp_status_string": (ctypes.c_char_p, [_int]),
+    "lp_backend_id": (ctypes.c_char_p, []),
+}
+
+
+def declared_symbols() -> list[str]:
+    """Names of the entry points include/lp.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    return re.findall(r"^LP_API\s+[\w\s\*]+?\b(lp_\w+)\s*\(", text, flags=re.M)
+
+
+def load(build_if_needed: bool = True) -> ctypes.CDLL:
+    """Load liblp.so (building it first when it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build_lib.LIB
+    if build_if_needed and _build_lib._stale():
+        _build_lib.build()
+    if not os.path.exists(path):
+        raise LpError("load", 5)
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise LpError(fn, status)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _row_stride(t: torch.Tensor) -> int:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError("expected a 2-D tensor with contiguous rows")
+    return t.stride(0)
+
+
+# ----------------------------------------------------------------- C entry points
+
+def lp_logprob_from_logits(logits, targets, logp, entropy=None, stream=None) -> None:
+    if logits.dtype != torch.float32 or targets.dtype != torch.int64:
+        raise TypeError("logits must be float32 and targets int64")
+    T, V = logits.shape
+    _check("lp_logprob_from_logits", load().lp_logprob_from_logits(
+        _ptr(logits), _row_stride(logits), _ptr(targets), T, V, _ptr(logp), _ptr(entropy),
+        _stream(stream)))
+
+
+def lp_vocab_shard_range(vocab_total: int, shard_index: int, n_shards: int) -> tuple[int, int]:
+    b, e = _i64(), _i64()
+    _check("lp_vocab_shard_range",
+           load().lp_vocab_shard_range(vocab_total, shard_index, n_shards, ctypes.byref(b), ctypes.byref(e)))
+    return b.value, e.value
+
+
+def lp_logprob_partials_from_logits(logits_shard, targets, vocab_total, shard_index, n_shards,
+                                    partials, stream=None) -> None:
+    if logits_shard.dtype != torch.float32 or targets.dtype != torch.int64:
+        raise TypeError("logits must be float32 and targets int64")
+    T = logits_shard.shape[0]
+    _check("lp_logprob_partials_from_logits", load().lp_logprob_partials_from_logits(
+        _ptr(logits_shard), _row_stride(logits_shard), _ptr(targets), T, vocab_total,
+        shard_index, n_shards, _ptr(partials), _stream(stream)))
+
+
+def lp_merge_partials(shard_partials: Sequence[torch.Tensor], T: int, logp, entropy=None,
+                      stream=None) -> None:
+    arr = (_vp * len(shard_partials))(*[p.data_ptr() for p in shard_partials])
+    _check("lp_merge_partials", load().lp_merge_partials(
+        arr, len(shard_partials), T, _ptr(logp), _ptr(entropy), _stream(stream)))
+
+
+def lp_linear_logprob_workspace_size(T: int, d: int, V: int) -> int:
+    return int(load().lp_linear_logprob_workspace_size(T, d, V))
+
+
+def lp_linear_logprob_partials_workspace_size(T: int, d: int, vocab_total: int, n_shards: int) -> int:
+    return int(load().lp_linear_logprob_partials_workspace_size(T, d, vocab_total, n_shards))
+
+
+def _check_bf16(H, W, targets):
+    if H.dtype != torch.bfloat16 or W.dtype != torch.bfloat16 or targets.dtype != torch.int64:
+        raise TypeError("H and W must be bfloat16 and targets int64")
+
+
+def lp_linear_logprob(H, W, targets, logp, entropy, workspace, stream=None) -> None:
+    _check_bf16(H, W, targets)
+    T, d = H.shape
+    V = W.shape[0]
+    _check("lp_linear_logprob", load().lp_linear_logprob(
+        _ptr(H), _row_stride(H), _ptr(W), _row_stride(W), _ptr(targets), T, d, V,
+        _ptr(logp), _ptr(entropy), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def lp_linear_logprob_partials(H, W_shard, targets, vocab_total, shard_index, n_shards,
+                               partials, workspace, stream=None) -> None:
+    _check_bf16(H, W_shard, targets)
+    T, d = H.shape
+    _check("lp_linear_logprob_partials", load().lp_linear_logprob_partials(
+        _ptr(H), _row_stride(H), _ptr(W_shard), _row_stride(W_shard), _ptr(targets), T, d,
+        vocab_total, shard_index, n_shards, _ptr(partials), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def lp_get_device_error(workspace, stream=None) -> int:
+    """The workspace error word (0: no device-side wait gave up)."""
+    word = ctypes.c_uint32(0)
+    st = load().lp_get_device_error(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    ctypes.byref(word), _stream(stream))
+    if st not in (0, 6):
+        raise LpError("lp_get_device_error", st)
+    return int(word.value)
+
+
+def lp_set_persistent_grid_limit(max_ctas: int) -> None:
+    _check("lp_set_persistent_grid_limit", load().lp_set_persistent_grid_limit(max_ctas))
+
+
+def lp_set_kernel_timing_events(start_event=None, stop_event=None) -> None:
+    """Record torch.cuda.Event pairs around the fused path's tensor-core kernel."""
+    a = None if start_event is None else start_event.cuda_event
+    b = None if stop_event is None else stop_event.cuda_event
+    _check("lp_set_kernel_timing_events", load().lp_set_kernel_timing_events(a, b))
+
+
+def lp_status_string(status: int) -> str:
+    return load().lp_status_string(status).decode()
+
+
+def lp_backend_id() -> str:
+    return load().lp_backend_id().decode()
+
+
+# ------------------------------------------------------------ allocating helpers
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    # torch's caching allocator returns blocks aligned to at least 512 bytes
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def logprob_from_logits(z: torch.Tensor, y: torch.Tensor, with_entropy: bool = True, stream=None):
+    T = z.shape[0]
+    logp = torch.empty(T, dtype=torch.float32, device=z.device)
+    ent = torch.empty(T, dtype=torch.float32, device=z.device) if with_entropy else None
+    lp_logprob_from_logits(z, y, logp, ent, stream)
+    return logp, ent
+
+
+def vocab_shard_range(vocab_total: int, shard_index: int, n_shards: int) -> tuple[int, int]:
+    return lp_vocab_shard_range(vocab_total, shard_index, n_shards)
+
+
+def logprob_partials_from_logits(z_shard, y, vocab_total, shard_index, n_shards, stream=None):
+    T = z_shard.shape[0]
+    partials = torch.empty((T, 4 // n_shards, 4), dtype=torch.float32, device=z_shard.device)
+    lp_logprob_partials_from_logits(z_shard, y, vocab_total, shard_index, n_shards, partials, stream)
+    return partials
+
+
+def merge_partials(shard_partials: Sequence[torch.Tensor], with_entropy: bool = True, stream=None):
+    T = shard_partials[0].shape[0]
+    dev = shard_partials[0].device
+    logp = torch.empty(T, dtype=torch.float32, device=dev)
+    ent = torch.empty(T, dtype=torch.float32, device=dev) if with_entropy else None
+    lp_merge_partials(shard_partials, T, logp, ent, stream)
+    return logp, ent
+
+
+def linear_logprob(H, W, y, with_entropy: bool = True, workspace=None, stream=None):
+    T, d = H.shape
+    V = W.shape[0]
+    if workspace is None:
+        workspace = _workspace(lp_linear_logprob_workspace_size(T, d, V), H.device)
+    logp = torch.empty(T, dtype=torch.float32, device=H.device)
+    ent = torch.empty(T, dtype=torch.float32, device=H.device) if with_entropy else None
+    lp_linear_logprob(H, W, y, logp, ent, workspace, stream)
+    return logp, ent
+
+
+def linear_logprob_partials(H, W_shard, y, vocab_total, shard_index, n_shards, workspace=None,
+                            stream=None):
+    T, d = H.shape
+    if workspace is None:
+        workspace = _workspace(
+            lp_linear_logprob_partials_workspace_size(T, d, vocab_total, n_shards), H.device)
+    partials = torch.empty((T, 4 // n_shards, 4), dtype=torch.float32, device=H.device)
+    lp_linear_logprob_partials(H, W_shard, y, vocab_total, shard_index, n_shards, partials,
+                               workspace, stream)
+    return partials

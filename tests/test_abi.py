@@ -1,0 +1,126 @@
+"""The C ABI without a GPU: the library loads, exports every entry point the
+header declares, and rejects bad arguments on the host before touching the
+device.  Valid calls on a machine without a GB300 fail with
+LP_ERR_UNSUPPORTED_DEVICE: there is no fallback path.
+"""
+
+import ctypes
+
+import pytest
+import torch
+
+from invariant_token_logprobs_gb300 import lp
+
+OK, INVALID, MISALIGNED, UNSUPPORTED, WS_SMALL = 0, 1, 2, 3, 4
+A = 1 << 20  # a fake, well-aligned device address; never dereferenced by these calls
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return lp.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = lp.declared_symbols()
+    assert len(names) == 13
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(lp._SIGNATURES)
+
+
+def test_status_strings_and_backend(lib):
+    for code, name in lp.STATUS.items():
+        assert lp.lp_status_string(code) == name
+    assert lp.lp_status_string(99) == "LP_ERR_UNKNOWN"
+    assert lp.lp_backend_id() == "lp.sm103a.bitwise.v1"
+
+
+def test_vocab_shard_range():
+    V = 151936
+    assert lp.vocab_shard_range(V, 0, 1) == (0, V)
+    assert lp.vocab_shard_range(V, 1, 2) == (75968, V)
+    assert [lp.vocab_shard_range(V, i, 4) for i in range(4)] == [
+        (0, 37984), (37984, 75968), (75968, 113952), (113952, 151936)]
+    # quarters of a vocabulary not divisible by 4: floor(q V / 4)
+    assert [lp.vocab_shard_range(10, i, 4) for i in range(4)] == [(0, 2), (2, 5), (5, 7), (7, 10)]
+    assert lp.vocab_shard_range(10, 1, 2) == (5, 10)
+    for bad in [(V, 0, 3), (V, 2, 2), (V, -1, 4), (0, 0, 1)]:
+        with pytest.raises(lp.LpError):
+            lp.vocab_shard_range(*bad)
+
+
+def test_workspace_sizes(lib):
+    # header + one 16-byte state per row and 256-column tile of each quarter
+    tiles = -(-(151936 // 4) // 256)
+    assert tiles == 149
+    assert lp.lp_linear_logprob_workspace_size(512, 4096, 151936) == 256 + 4 * tiles * 512 * 16
+    assert lp.lp_linear_logprob_partials_workspace_size(512, 4096, 151936, 2) == 256 + 2 * tiles * 512 * 16
+    assert lp.lp_linear_logprob_workspace_size(0, 8, 10) == 256
+    assert lp.lp_linear_logprob_workspace_size(-1, 8, 10) == 0
+
+
+def test_logits_argument_errors(lib):
+    f = lib.lp_logprob_from_logits
+    assert f(A, 100, A, 0, 100, A, A, None) == OK          # T == 0: nothing to do
+    assert f(A, 100, A, -1, 100, A, A, None) == INVALID
+    assert f(A, 100, A, 4, 0, A, A, None) == INVALID       # V == 0
+    assert f(A, 99, A, 4, 100, A, A, None) == INVALID      # ld < V
+    assert f(None, 100, A, 4, 100, A, A, None) == INVALID
+    assert f(A, 100, None, 4, 100, A, A, None) == INVALID
+    assert f(A, 100, A, 4, 100, None, A, None) == INVALID
+    assert f(A + 2, 100, A, 4, 100, A, A, None) == MISALIGNED
+    assert f(A, 100, A + 4, 4, 100, A, A, None) == MISALIGNED
+    assert f(A, 100, A, 4, 100, A + 1, A, None) == MISALIGNED
+
+
+def test_fused_argument_errors(lib):
+    f = lib.lp_linear_logprob
+    ws = lp.lp_linear_logprob_workspace_size(64, 256, 8192)
+    args = [A, 256, A, 256, A, 64, 256, 8192, A, A, A, ws, None]
+
+    def call(**kw):
+        a = list(args)
+        for k, v in kw.items():
+            a[["H", "ld_h", "W", "ld_w", "y", "T", "d", "V", "logp", "ent", "ws", "wsb", "s"].index(k)] = v
+        return f(*a)
+
+    assert call(T=0) == OK
+    assert call(d=0) == INVALID
+    assert call(V=0) == INVALID
+    assert call(ld_h=255) == INVALID
+    assert call(H=None) == INVALID
+    assert call(logp=None) == INVALID
+    assert call(ws=None) == INVALID
+    assert call(H=A + 8) == MISALIGNED
+    assert call(W=A + 2) == MISALIGNED
+    assert call(ld_h=260) == MISALIGNED      # row pitch not a multiple of 16 bytes
+    assert call(ws=A + 128) == MISALIGNED
+    assert call(wsb=ws - 1) == WS_SMALL
+    g = lib.lp_linear_logprob_partials
+    wsp = lp.lp_linear_logprob_partials_workspace_size(64, 256, 8192, 4)
+    assert g(A, 256, A, 256, A, 64, 256, 8192, 4, 4, A, A, wsp, None) == INVALID  # shard index
+    assert g(A, 256, A, 256, A, 64, 256, 8192, 0, 3, A, A, wsp, None) == INVALID  # 3 shards
+    assert g(A, 256, A, 256, A, 64, 256, 8192, 1, 4, A + 4, A, wsp, None) == MISALIGNED
+    assert g(A, 256, A, 256, A, 64, 256, 8192, 1, 4, A, A, wsp - 16, None) == WS_SMALL
+
+
+def test_merge_argument_errors(lib):
+    f = lib.lp_merge_partials
+    arr = (ctypes.c_void_p * 4)(A, A, A, A)
+    assert f(arr, 3, 8, A, A, None) == INVALID
+    assert f(arr, 4, 0, A, A, None) == OK
+    bad = (ctypes.c_void_p * 2)(A, A + 8)
+    assert f(bad, 2, 8, A, A, None) == MISALIGNED
+    none = (ctypes.c_void_p * 2)(A, None)
+    assert f(none, 2, 8, A, A, None) == INVALID
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")
+def test_valid_call_without_gb300_fails_loudly(lib):
+    assert lib.lp_logprob_from_logits(A, 100, A, 4, 100, A, A, None) == UNSUPPORTED
+    ws = lp.lp_linear_logprob_workspace_size(64, 256, 8192)
+    assert lib.lp_linear_logprob(A, 256, A, 256, A, 64, 256, 8192, A, A, A, ws, None) == UNSUPPORTED
+    arr = (ctypes.c_void_p * 1)(A)
+    assert lib.lp_merge_partials(arr, 1, 8, A, A, None) == UNSUPPORTED
+    assert lib.lp_set_persistent_grid_limit(-1) == INVALID
+    assert lib.lp_set_persistent_grid_limit(0) == OK

@@ -1,0 +1,147 @@
+"""Parity and invariance of the logits-given path on a GB300, through the C ABI.
+
+Oracle: fp64 CPU definition on host copies of the same fp32 logits.  Tolerance
+2e-6 absolute on logp (the prior-art report measures about 8e-7 for 1024
+tokens against fp64) and 1e-5 on entropy.  Bitwise checks: batch position and
+row offset, unaligned row stride, 1/2/4 vocabulary shards, 10 repeats.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from invariant_token_logprobs_gb300 import lp, synth
+from _gpu_helpers import (LOGITS_ENT_TOL, LOGITS_LOGP_TOL, bits, max_err, oracle_logits)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    lp.load()
+
+
+def _check(z, y, rows=None, logp_tol=LOGITS_LOGP_TOL, ent_tol=LOGITS_ENT_TOL):
+    logp, ent = lp.logprob_from_logits(z, y)
+    torch.cuda.synchronize()
+    sel = slice(None) if rows is None else rows
+    ref_lp, ref_ent = oracle_logits(z, y, rows)
+    e_lp = max_err(logp[sel], ref_lp)
+    e_ent = max_err(ent[sel], ref_ent)
+    assert e_lp <= logp_tol, f"logp max abs err {e_lp}"
+    assert e_ent <= ent_tol, f"entropy max abs err {e_ent}"
+    return logp, ent, e_lp, e_ent
+
+
+@pytest.mark.parametrize("T,V", [(64, 8192), (37, 1001), (5, 7), (3, 1), (4, 3), (9, 4096 + 13),
+                                 (2, 37984 * 4 + 2)])
+def test_small_all_rows(T, V):
+    x = synth.logits_inputs("logits_peaked", device=DEV, T=T, V=V, seed=100 + V)
+    _check(x.z, x.y)
+
+
+def test_peaked_workload_full_size_sampled_rows():
+    x = synth.logits_inputs("logits_peaked", device=DEV)
+    assert x.z.shape == (1024, 151936)
+    rows = torch.arange(0, 1024, 8)
+    logp, ent, e_lp, e_ent = _check(x.z, x.y, rows)
+    print(f"peaked 1024x151936: logp err {e_lp:.3e}, entropy err {e_ent:.3e}")
+
+
+def test_near_uniform_rows_within_report_scale():
+    """Near-uniform rows over the 151936 vocabulary: |logp| ~ ln V = 11.93.
+    The report's fp32 candidates land 7.8e-7 .. 8.1e-7 from fp64 at 1024
+    tokens; ours must stay below one fp32 ulp there (2^-20)."""
+    g = torch.Generator(device=DEV)
+    g.manual_seed(21)
+    z = torch.randn((1024, 151936), generator=g, device=DEV) * 0.01
+    y = torch.randint(0, 151936, (1024,), generator=g, device=DEV)
+    logp, ent = lp.logprob_from_logits(z, y)
+    rows = torch.arange(0, 1024, 4)
+    ref_lp, ref_ent = oracle_logits(z, y, rows)
+    e = max_err(logp[rows], ref_lp)
+    assert e <= 2.0 ** -20, e
+    assert max_err(ent[rows], ref_ent) <= LOGITS_ENT_TOL
+
+
+def test_batch_offset_and_stride_bitwise():
+    x = synth.logits_inputs("logits_peaked", device=DEV, T=96, V=20000, seed=7)
+    lp_all, ent_all = lp.logprob_from_logits(x.z, x.y)
+    # the same rows alone, reversed, and inside a bigger batch at an offset
+    idx = torch.tensor([5, 17, 90, 0, 63], device=DEV)
+    lp_sub, ent_sub = lp.logprob_from_logits(x.z[idx].contiguous(), x.y[idx])
+    assert torch.equal(bits(lp_sub), bits(lp_all[idx])) and torch.equal(bits(ent_sub), bits(ent_all[idx]))
+    big = torch.randn((300, 20000), device=DEV)
+    yb = torch.randint(0, 20000, (300,), device=DEV)
+    big[123:123 + 96] = x.z
+    yb[123:123 + 96] = x.y
+    lp_big, ent_big = lp.logprob_from_logits(big, yb)
+    assert torch.equal(bits(lp_big[123:219]), bits(lp_all)) and torch.equal(bits(ent_big[123:219]), bits(ent_all))
+    # unaligned rows (row stride V + 1): scalar loads, same arithmetic
+    wide = torch.empty((96, 20001), device=DEV)
+    wide[:, :20000] = x.z
+    lp_w, ent_w = lp.logprob_from_logits(wide[:, :20000], x.y)
+    assert torch.equal(bits(lp_w), bits(lp_all)) and torch.equal(bits(ent_w), bits(ent_all))
+    # entropy output is optional and does not change logp
+    lp_only, none = lp.logprob_from_logits(x.z, x.y, with_entropy=False)
+    assert none is None and torch.equal(bits(lp_only), bits(lp_all))
+
+
+@pytest.mark.parametrize("V", [151936, 8192 + 6, 3])
+def test_shards_bitwise_equal_unsharded(V):
+    x = synth.logits_inputs("logits_peaked", device=DEV, T=64, V=V, seed=3)
+    ref_lp, ref_ent = lp.logprob_from_logits(x.z, x.y)
+    for n in (1, 2, 4):
+        parts = []
+        for i in range(n):
+            b, e = lp.vocab_shard_range(V, i, n)
+            parts.append(lp.logprob_partials_from_logits(x.z[:, b:e], x.y, V, i, n))
+        m_lp, m_ent = lp.merge_partials(parts)
+        assert torch.equal(bits(m_lp), bits(ref_lp)), f"{n} shards logp"
+        assert torch.equal(bits(m_ent), bits(ref_ent)), f"{n} shards entropy"
+
+
+def test_ten_repeats_one_distinct_result():
+    x = synth.logits_inputs("logits_peaked", device=DEV, T=256)
+    outs = set()
+    for _ in range(10):
+        logp, ent = lp.logprob_from_logits(x.z, x.y)
+        outs.add((bits(logp).numpy().tobytes(), bits(ent).numpy().tobytes()))
+    assert len(outs) == 1
+
+
+def test_special_values():
+    V = 5000
+    z = torch.randn((6, V), device=DEV)
+    y = torch.tensor([1, 2, -1, V, 4, 10], device=DEV)
+    z[1, 2] = float("-inf")        # target logit -inf
+    z[3, :] = float("-inf")        # no distribution
+    z[4, 100] = float("nan")       # NaN logit
+    z[5, ::2] = float("-inf")      # half the columns removed
+    logp, ent = lp.logprob_from_logits(z, y)
+    ref_lp, ref_ent = oracle_logits(z, y)
+    assert max_err(logp, ref_lp) <= LOGITS_LOGP_TOL
+    assert max_err(ent, ref_ent) <= LOGITS_ENT_TOL
+    assert math.isinf(float(logp[1])) and float(logp[1]) < 0
+    assert math.isnan(float(logp[2])) and math.isfinite(float(ent[2]))  # bad target
+    assert math.isnan(float(logp[3])) and math.isnan(float(ent[3]))
+    assert math.isnan(float(logp[4])) and math.isnan(float(ent[4]))
+
+
+def test_uniform_closed_form():
+    V = 151936
+    z = torch.full((8, V), 2.5, device=DEV)
+    y = torch.arange(8, device=DEV) * 1000
+    logp, ent = lp.logprob_from_logits(z, y)
+    assert float((logp.double() + math.log(V)).abs().max()) <= 1e-6
+    assert float((ent.double() - math.log(V)).abs().max()) <= 1e-5
+
+
+def test_empty_batch():
+    z = torch.empty((0, 100), device=DEV)
+    y = torch.empty((0,), dtype=torch.int64, device=DEV)
+    logp, ent = lp.logprob_from_logits(z, y)
+    assert logp.numel() == 0
