@@ -61,6 +61,12 @@ constexpr uint32_t kTmemCols = 2 * kBN;
 constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;
 constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kNumBars * 8 + 16;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
+#ifndef LP_PREFETCH_KBLOCKS
+#define LP_PREFETCH_KBLOCKS 12
+#endif
+// W boxes are prefetched into L2 this many K blocks ahead of their load, so the
+// HBM latency of the first touch of a W tile is hidden behind the ring.
+constexpr int kPrefetchKBlocks = LP_PREFETCH_KBLOCKS;
 
 // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B bf16
 // (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 in
@@ -70,7 +76,7 @@ constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
 
 struct LinearArgs {
   const int64_t* targets;
-  float4* chunks;  // [n_q * n_tiles_q][T]
+  float4* chunks;  // [T][n_q][n_tiles_q]
   uint32_t* err;
   int64_t V;       // full vocabulary size
   int64_t w_row0;  // global vocabulary index of W row 0
@@ -78,6 +84,7 @@ struct LinearArgs {
   int n_mb;
   int n_kb;
   int q_first;
+  int n_q;
   int n_tiles_q;
   int total_tiles;
 };
@@ -151,6 +158,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
+}
+
+// Pull a box of the tensor into L2 ahead of its load (no shared memory, no
+// barrier).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -277,12 +293,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t pending = 0;        // stages with a load in flight (bit mask)
       uint32_t pending_parity = 0; // parity of that load's phase
       bool ok = true;
+      auto w_row_of = [&](int u) {
+        int mb, ql, j;
+        decode_tile(a, u, mb, ql, j);
+        return static_cast<int>(quarter_begin(a.V, a.q_first + ql) - a.w_row0) + j * kBN;
+      };
+      int pf_u = blockIdx.x, pf_kb = 0;  // prefetch cursor, kPrefetchKBlocks ahead
+      auto prefetch_next = [&]() {
+        if (pf_u < a.total_tiles) tma_prefetch_2d(&tmB, pf_kb * kBK, w_row_of(pf_u));
+        if (++pf_kb == a.n_kb) {
+          pf_kb = 0;
+          pf_u += gridDim.x;
+        }
+      };
+      for (int i = 0; i < kPrefetchKBlocks; ++i) prefetch_next();
       for (int u = blockIdx.x; ok && u < a.total_tiles; u += gridDim.x) {
         int mb, ql, j;
         decode_tile(a, u, mb, ql, j);
         const int a_row = mb * kBM;
-        const int b_row =
-            static_cast<int>(quarter_begin(a.V, a.q_first + ql) - a.w_row0) + j * kBN;
+        const int b_row = w_row_of(u);
         for (int kb = 0; kb < a.n_kb; ++kb) {
           if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, a.err, kErrLoader)) {
             ok = false;
@@ -294,6 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sa + kABytes, &tmB, kb * kBK, b_row, full_bar(stage));
           pending |= 1u << stage;
           pending_parity = (pending_parity & ~(1u << stage)) | (phase << stage);
+          prefetch_next();
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -417,8 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
       if (row < a.T) {
-        const int64_t chunk = static_cast<int64_t>(ql) * a.n_tiles_q + j;
-        a.chunks[chunk * a.T + row] = make_float4(st.m, st.s, st.u, t);
+        a.chunks[(row * a.n_q + ql) * a.n_tiles_q + j] = make_float4(st.m, st.s, st.u, t);
       }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
@@ -436,47 +465,58 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Merge the tile states of each quarter (left to right, rebased to the
-// quarter maximum, float64 sums) and then either finalise the row from its four
-// quarters or store the quarter states of a shard.
-// Block: 32 rows x 4 quarter slots.
+// Merge the tile states of each quarter and then either finalise the row from
+// its four quarters or store the quarter states of a shard.  One block per
+// row, one warp per quarter: the quarter's maximum is exact (order-free); lane
+// l rebases tiles l, l+32, l+64, ... to it and sums them in float64, and the
+// 32 lane sums are combined by a fixed shuffle tree.  The result depends only
+// on the quarter's tile states.
 __global__ void __launch_bounds__(128)
     lp_tile_merge_kernel(const float4* __restrict__ chunks, const int64_t* __restrict__ targets,
-                         const uint32_t* __restrict__ err, int64_t T, int n_q, int n_tiles_q,
-                         int64_t V, float* __restrict__ logp, float* __restrict__ entropy,
+                         const uint32_t* __restrict__ err, int n_q, int n_tiles_q, int64_t V,
+                         float* __restrict__ logp, float* __restrict__ entropy,
                          float4* __restrict__ partials_out) {
-  __shared__ float4 qs[kQuarters][32];
+  __shared__ float4 qs[kQuarters];
   const int ql = threadIdx.x >> 5;
-  const int r = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * 32 + r;
-  float4 st = make_float4(neg_inf(), 0.f, 0.f, neg_inf());
-  if (ql < n_q && row < T) {
-    const float4* c = chunks + static_cast<int64_t>(ql) * n_tiles_q * T + row;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = blockIdx.x;
+  if (ql < n_q) {
+    const float4* c = chunks + (row * n_q + ql) * n_tiles_q;
     float M = neg_inf();
-    for (int j = 0; j < n_tiles_q; ++j) M = fmaxf(M, c[static_cast<int64_t>(j) * T].x);
+    for (int j = lane; j < n_tiles_q; j += 32) M = fmaxf(M, c[j].x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     double S = 0.0, U = 0.0;
     float t = neg_inf();
-    for (int j = 0; j < n_tiles_q; ++j) {
-      const float4 x = c[static_cast<int64_t>(j) * T];
+    for (int j = lane; j < n_tiles_q; j += 32) {
+      const float4 x = c[j];
       float s, u;
       rebase(x.x, x.y, x.z, M, s, u);
       S = __dadd_rn(S, static_cast<double>(s));
       U = __dadd_rn(U, static_cast<double>(u));
       t = fmax_nan(t, x.w);
     }
-    const int64_t y = targets[row];
-    if (y < 0 || y >= V) t = quiet_nan();
-    st = make_float4(M, __double2float_rn(S), __double2float_rn(U), t);
-    if (*err != 0u) st.y = quiet_nan();  // a pipeline wait gave up: no result
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      S = __dadd_rn(S, __shfl_down_sync(0xffffffffu, S, off));
+      U = __dadd_rn(U, __shfl_down_sync(0xffffffffu, U, off));
+      t = fmax_nan(t, __shfl_down_sync(0xffffffffu, t, off));
+    }
+    if (lane == 0) {
+      const int64_t y = targets[row];
+      if (y < 0 || y >= V) t = quiet_nan();
+      float4 st = make_float4(M, __double2float_rn(S), __double2float_rn(U), t);
+      if (*err != 0u) st.y = quiet_nan();  // a pipeline wait gave up: no result
+      if (partials_out != nullptr)
+        partials_out[row * n_q + ql] = st;
+      else
+        qs[ql] = st;
+    }
   }
-  if (partials_out != nullptr) {
-    if (ql < n_q && row < T) partials_out[row * n_q + ql] = st;
-    return;
-  }
-  qs[ql][r] = st;
+  if (partials_out != nullptr) return;
   __syncthreads();
-  if (ql == 0 && row < T) {
-    const float4 q4[kQuarters] = {qs[0][r], qs[1][r], qs[2][r], qs[3][r]};
+  if (threadIdx.x == 0) {
+    const float4 q4[kQuarters] = {qs[0], qs[1], qs[2], qs[3]};
     float lp, ent;
     finalise(q4, lp, ent);
     logp[row] = lp;
@@ -559,6 +599,7 @@ lp_status launch_linear(const Device& dev, const void* H, int64_t ld_h, const vo
   a.n_mb = static_cast<int>((T + kBM - 1) / kBM);
   a.n_kb = static_cast<int>((d + kBK - 1) / kBK);
   a.q_first = q_first;
+  a.n_q = n_q;
   a.n_tiles_q = static_cast<int>(tiles_per_quarter(V_total));
   const int64_t total = int64_t(a.n_mb) * n_q * a.n_tiles_q;
   if (total >= (int64_t(1) << 31)) return LP_ERR_INVALID_ARGUMENT;
@@ -576,9 +617,8 @@ lp_status launch_linear(const Device& dev, const void* H, int64_t ld_h, const vo
   lp_linear_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, a);
   if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
   if (ev_stop != nullptr && cudaEventRecord(ev_stop, stream) != cudaSuccess) return LP_ERR_CUDA;
-  const int64_t mblocks = (T + 31) / 32;
-  lp_tile_merge_kernel<<<static_cast<unsigned>(mblocks), 128, 0, stream>>>(
-      a.chunks, targets, a.err, T, n_q, a.n_tiles_q, V_total, logp, entropy,
+  lp_tile_merge_kernel<<<static_cast<unsigned>(T), 128, 0, stream>>>(
+      a.chunks, targets, a.err, n_q, a.n_tiles_q, V_total, logp, entropy,
       reinterpret_cast<float4*>(partials_out));
   return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }

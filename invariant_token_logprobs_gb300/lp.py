@@ -99,12 +99,16 @@ def declared_symbols() -> list[str]:
 
 
 def load(build_if_needed: bool = True) -> ctypes.CDLL:
-    """Load liblp.so (building it first when it is missing or stale)."""
+    """Load liblp.so (building it first when it is missing or stale).
+
+    The environment variable LP_LIBRARY names another build of the same
+    library to load instead (for comparing builds); it is never a fallback.
+    """
     global _lib
     if _lib is not None:
         return _lib
-    path = _build_lib.LIB
-    if build_if_needed and _build_lib._stale():
+    path = os.environ.get("LP_LIBRARY", _build_lib.LIB)
+    if build_if_needed and path == _build_lib.LIB and _build_lib._stale():
         _build_lib.build()
     if not os.path.exists(path):
         raise LpError("load", 5)
