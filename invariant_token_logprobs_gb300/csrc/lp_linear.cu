@@ -2,7 +2,7 @@
 // ("linear_logp", rlkernel.linear_logp.bitwise.v1 in the backend readbacks of
 // the RL-Kernel H100 PCP evidence record, h100-pcp.json, section "validation").
 //
-// z = H W^T (bf16 inputs, fp32 accumulation) is formed one 128 x 256 tile at a
+// z = H W^T (bf16 inputs, fp32 accumulation) is formed one 256 x 256 tile at a
 // time in tensor memory and reduced on the spot to a per-row state
 // (max, sum-exp, sum-exp*(z-max), target logit); the T x V logits never reach
 // global memory.
@@ -10,30 +10,40 @@
 // Tiling.  The vocabulary is cut into four quarters [floor(qV/4),
 // floor((q+1)V/4)); each quarter into 256-column tiles counted from the
 // quarter's first column (the last tile of a quarter is masked past the
-// quarter's end).  Rows are cut into 128-row blocks.  A work unit is one
+// quarter's end).  Rows are cut into 256-row blocks.  A work unit is one
 // (row block, quarter, tile); its per-row state goes to the workspace, and a
-// second kernel merges the tiles of each quarter left to right (rebased to
-// the quarter's maximum, summed in float64) and then the quarters as
-// (Q0 + Q1) + (Q2 + Q3).  Every value depends only on the row and on the
-// fixed tile grid of its quarter: not on T, the row's offset, the shard, the
-// grid size or the order in which CTAs pick up tiles.
+// second kernel merges the tiles of each quarter (rebased to the quarter's
+// maximum, float64 sums in a fixed tree) and then the quarters as
+// (Q0 + Q1) + (Q2 + Q3).  Every value depends only on the row and on the fixed
+// tile grid of its quarter: not on T, the row's offset, the shard, the grid
+// size or the order in which CTAs pick up tiles.
 //
-// Kernel structure (one CTA per SM, persistent, 6 warps):
-//   warp 0     TMA loader: bf16 tiles H[128 x 64] and W[256 x 64] with
-//              128-byte swizzle into a 4-stage shared-memory ring;
-//   warp 1     allocates 512 tensor-memory columns (two 128 x 256 fp32
-//              accumulators) and one lane issues tcgen05.mma (M=128, N=256,
-//              K=16; kind::f16, bf16 x bf16 -> f32) for every 64-wide K block;
-//   warps 2-5  epilogue: tcgen05.ld of the finished accumulator, one row per
-//              thread, online reduction in column order, state store.
-// While the epilogue drains one accumulator the MMAs fill the other.
-// Units are taken round-robin in (tile, row block) order so that the CTAs that
+// Kernel structure: persistent CTA pairs (thread-block clusters of 2, one CTA
+// per SM), each CTA with 6 warps.  The pair computes a 256 x 256 tile with
+// tcgen05.mma.cta_group::2 (M=256, N=256, K=16, kind::f16 bf16 x bf16 -> f32):
+// CTA r holds rows 128r..128r+127 of the H tile and rows 128r..128r+127 of the
+// W tile in its own shared memory, and receives rows 128r.. of the result in
+// its own tensor memory.  Each SM so stages 32 KB per 64-wide K block instead
+// of the 48 KB a single-CTA 128 x 256 tile needs: with the tensor core reading
+// what TMA writes, shared-memory bandwidth is what bounds a single-CTA tile.
+//   warp 0     TMA loader (both CTAs): its CTA's halves of the H and W boxes
+//              (64 x 128 each, 128-byte swizzle) into a 6-stage ring; the
+//              bytes of both CTAs complete one barrier in the leader CTA;
+//   warp 1     tensor memory: 512 columns (two 128 x 256 fp32 accumulators)
+//              allocated by both CTAs; one lane of the leader CTA issues the
+//              MMAs and commits them to barriers in both CTAs (multicast);
+//   warps 2-5  epilogue (both CTAs): tcgen05.ld of the finished accumulator,
+//              one row per thread, online reduction in column order, state
+//              store, then an arrive on the leader's accumulator-empty barrier.
+// While the epilogues drain one accumulator the MMAs fill the other.  Units
+// are taken round-robin in (tile, row block) order so that the pairs that
 // share a W tile run at the same time and W is read from HBM about once.
 //
 // Every wait on an mbarrier is bounded by %globaltimer: a wait that gives up
 // sets the workspace error word and an abort flag in shared memory, the other
-// roles stop at their next wait, in-flight copies and MMAs are drained with
-// bounded waits, tensor memory is freed and the CTA returns.  The merge kernel
+// roles of that CTA stop at their next wait (the roles of the other CTA give up
+// on their own bounded waits), in-flight copies and MMAs are drained with
+// bounded waits, tensor memory is freed and the CTAs return.  The merge kernel
 // then writes NaN for every row.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -47,13 +57,14 @@
 namespace lp {
 namespace {
 
-constexpr int kBM = 128;  // rows of H per tile (tensor-memory lanes)
-constexpr int kBN = kTileN;  // vocabulary columns per tile
-constexpr int kBK = 64;   // K per pipeline stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kBM = 128;       // rows of H per CTA (tensor-memory lanes); 256 per pair
+constexpr int kBN = kTileN;    // vocabulary columns per tile (pair); 128 W rows per CTA
+constexpr int kBNHalf = kBN / 2;
+constexpr int kBK = 64;        // K per pipeline stage: 64 bf16 = one 128-byte swizzle row
 constexpr int kUmmaK = 16;
-constexpr int kStages = 4;
-constexpr int kABytes = kBM * kBK * 2;
-constexpr int kBBytes = kBN * kBK * 2;
+constexpr int kStages = 6;
+constexpr int kABytes = kBM * kBK * 2;       // 16 KB
+constexpr int kBBytes = kBNHalf * kBK * 2;   // 16 KB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 192;
 constexpr int kEpilogueThreads = 128;
@@ -61,18 +72,12 @@ constexpr uint32_t kTmemCols = 2 * kBN;
 constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;
 constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kNumBars * 8 + 16;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
-#ifndef LP_PREFETCH_KBLOCKS
-#define LP_PREFETCH_KBLOCKS 12
-#endif
-// W boxes are prefetched into L2 this many K blocks ahead of their load, so the
-// HBM latency of the first touch of a W tile is hidden behind the ring.
-constexpr int kPrefetchKBlocks = LP_PREFETCH_KBLOCKS;
 
 // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B bf16
 // (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 in
-// bits 17-22, M >> 4 in bits 24-28.
+// bits 17-22, M >> 4 in bits 24-28; M = 256 for the CTA pair.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                            (uint32_t(kBN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+                            (uint32_t(kBN >> 3) << 17) | (uint32_t((2 * kBM) >> 4) << 24);
 
 struct LinearArgs {
   const int64_t* targets;
@@ -81,7 +86,7 @@ struct LinearArgs {
   int64_t V;       // full vocabulary size
   int64_t w_row0;  // global vocabulary index of W row 0
   int T;
-  int n_mb;
+  int n_mb;        // 256-row blocks
   int n_kb;
   int q_first;
   int n_q;
@@ -102,10 +107,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -151,22 +152,38 @@ __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// TMA load of a box into this CTA's shared memory; the transferred bytes are
+// counted on `bar`, a shared::cluster address that may lie in the peer CTA.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                             uint32_t bar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
       "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
 
-// Pull a box of the tensor into L2 ahead of its load (no shared memory, no
-// barrier).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1)
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -176,10 +193,15 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   bar)
-               : "memory");
+// Arrive on `bar` (same offset) in both CTAs of the pair once every MMA issued
+// so far by this thread has completed.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  const uint16_t both = 3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(bar),
+      "h"(both)
+      : "memory");
 }
 
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
@@ -187,7 +209,7 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
       : "memory");
 }
@@ -237,8 +259,9 @@ __device__ __forceinline__ void decode_tile(const LinearArgs& a, int u, int& mb,
 }
 
 // ------------------------------------------------------------------- kernel
+// ------------------------------------------------------------------- kernel
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     lp_linear_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const LinearArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -257,6 +280,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();  // 0: leader (issues the MMAs), 1: peer
+  const int pair = blockIdx.x >> 1;
+  const int n_pairs = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -265,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), kEpilogueThreads);
+      mbar_init(tempty_bar(b), 2 * kEpilogueThreads);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -274,14 +300,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
+  __syncwarp();
+  cluster_sync();  // both CTAs' barriers initialised and tensor memory allocated
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -290,47 +318,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t pending = 0;        // stages with a load in flight (bit mask)
-      uint32_t pending_parity = 0; // parity of that load's phase
+      uint32_t pending = 0;         // stages with a load in flight (leader: bit mask)
+      uint32_t pending_parity = 0;  // parity of that load's phase
       bool ok = true;
-      auto w_row_of = [&](int u) {
+      for (int u = pair; ok && u < a.total_tiles; u += n_pairs) {
         int mb, ql, j;
         decode_tile(a, u, mb, ql, j);
-        return static_cast<int>(quarter_begin(a.V, a.q_first + ql) - a.w_row0) + j * kBN;
-      };
-      int pf_u = blockIdx.x, pf_kb = 0;  // prefetch cursor, kPrefetchKBlocks ahead
-      auto prefetch_next = [&]() {
-        if (pf_u < a.total_tiles) tma_prefetch_2d(&tmB, pf_kb * kBK, w_row_of(pf_u));
-        if (++pf_kb == a.n_kb) {
-          pf_kb = 0;
-          pf_u += gridDim.x;
-        }
-      };
-      for (int i = 0; i < kPrefetchKBlocks; ++i) prefetch_next();
-      for (int u = blockIdx.x; ok && u < a.total_tiles; u += gridDim.x) {
-        int mb, ql, j;
-        decode_tile(a, u, mb, ql, j);
-        const int a_row = mb * kBM;
-        const int b_row = w_row_of(u);
+        const int a_row = mb * (2 * kBM) + static_cast<int>(rank) * kBM;
+        const int b_row = static_cast<int>(quarter_begin(a.V, a.q_first + ql) - a.w_row0) +
+                          j * kBN + static_cast<int>(rank) * kBNHalf;
         for (int kb = 0; kb < a.n_kb; ++kb) {
           if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, a.err, kErrLoader)) {
             ok = false;
             break;
           }
           const uint32_t sa = smem_u32(smem + stage * kStageBytes);
-          mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
-          tma_load_2d(sa, &tmA, kb * kBK, a_row, full_bar(stage));
-          tma_load_2d(sa + kABytes, &tmB, kb * kBK, b_row, full_bar(stage));
-          pending |= 1u << stage;
-          pending_parity = (pending_parity & ~(1u << stage)) | (phase << stage);
-          prefetch_next();
+          const uint32_t leader_full = cluster_addr(full_bar(stage), 0);
+          if (rank == 0) {
+            mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytes);
+            pending |= 1u << stage;
+            pending_parity = (pending_parity & ~(1u << stage)) | (phase << stage);
+          }
+          tma_load_2d(sa, &tmA, kb * kBK, a_row, leader_full);
+          tma_load_2d(sa + kABytes, &tmB, kb * kBK, b_row, leader_full);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      if (!ok) {  // let every issued copy land before the CTA can exit
+      if (!ok && rank == 0) {  // let every issued copy land before the pair can exit
         for (int s = 0; s < kStages; ++s)
           if (pending & (1u << s)) drain_wait(full_bar(s), (pending_parity >> s) & 1u);
       }
@@ -338,59 +355,59 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < a.total_tiles; u += gridDim.x) {
-        if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, abort_flag, a.err, kErrMma)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-        for (int kb = 0; kb < a.n_kb; ++kb) {
-          if (!wait_bar(full_bar(stage), phase, abort_flag, a.err, kErrMma)) {
+      if (rank == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int u = pair; ok && u < a.total_tiles; u += n_pairs) {
+          if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, abort_flag, a.err, kErrMma)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + stage * kStageBytes);
-          const uint32_t sb = sa + kABytes;
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+          for (int kb = 0; kb < a.n_kb; ++kb) {
+            if (!wait_bar(full_bar(stage), phase, abort_flag, a.err, kErrMma)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+            const uint32_t sb = sa + kABytes;
 #pragma unroll
-          for (int k = 0; k < kBK / kUmmaK; ++k) {
-            tc_mma(d_tmem, sw128_desc(sa + k * kUmmaK * 2), sw128_desc(sb + k * kUmmaK * 2),
-                   (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < kBK / kUmmaK; ++k) {
+              tc_mma(d_tmem, sw128_desc(sa + k * kUmmaK * 2), sw128_desc(sb + k * kUmmaK * 2),
+                     (kb | k) != 0 ? 1u : 0u);
+            }
+            tc_commit_pair(empty_bar(stage));  // frees the stage in both CTAs
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          tc_commit(empty_bar(stage));  // frees the stage once these MMAs are done
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          if (!ok) break;
+          tc_commit_pair(tfull_bar(acc));  // accumulator ready in both CTAs
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
         }
-        if (!ok) break;
-        tc_commit(tfull_bar(acc));  // accumulator ready once all its MMAs are done
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
+        tc_commit_pair(drain_bar);  // arrives once every MMA issued here is done
       }
-      if (!ok) {
-        tc_commit(drain_bar);
-        drain_wait(drain_bar, 0);
-      }
+      drain_wait(drain_bar, 0);
     }
   } else {
     // -------------------------------------------------------------- epilogue
     const int lane_grp = warp & 3;  // tensor-memory lanes 32*lane_grp .. +31
-    const int row_in_tile = lane_grp * 32 + lane;
+    const int row_in_tile = static_cast<int>(rank) * kBM + lane_grp * 32 + lane;
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(lane_grp * 32) << 16);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = blockIdx.x; u < a.total_tiles; u += gridDim.x) {
+    for (int u = pair; u < a.total_tiles; u += n_pairs) {
       int mb, ql, j;
       decode_tile(a, u, mb, ql, j);
       const int q = a.q_first + ql;
-      const int64_t row = static_cast<int64_t>(mb) * kBM + row_in_tile;
+      const int64_t row = static_cast<int64_t>(mb) * (2 * kBM) + row_in_tile;
       const int64_t y = row < a.T ? a.targets[row] : -1;
       const int64_t qc0 = quarter_begin(a.V, q);
       const int64_t qw = quarter_begin(a.V, q + 1) - qc0;
@@ -445,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(tempty_bar(acc));
+      mbar_arrive_cluster(cluster_addr(tempty_bar(acc), 0));
       if (row < a.T) {
         a.chunks[(row * a.n_q + ql) * a.n_tiles_q + j] = make_float4(st.m, st.s, st.u, t);
       }
@@ -456,14 +473,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  __syncwarp();
+  cluster_sync();  // no remote arrive or copy into either CTA is still pending
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"(kTmemCols)
                  : "memory");
   }
 }
+
 
 // Merge the tile states of each quarter and then either finalise the row from
 // its four quarters or store the quarter states of a shard.  One block per
@@ -587,7 +607,7 @@ lp_status launch_linear(const Device& dev, const void* H, int64_t ld_h, const vo
   const int64_t w_rows = max(quarter_begin(V_total, q_first + n_q) - w_row0, int64_t(1));
   CUtensorMap tmA, tmB;
   if (!encode_bf16_2d(&tmA, H, T, d, ld_h, kBM)) return LP_ERR_CUDA;
-  if (!encode_bf16_2d(&tmB, W, w_rows, d, ld_w, kBN)) return LP_ERR_CUDA;
+  if (!encode_bf16_2d(&tmB, W, w_rows, d, ld_w, kBNHalf)) return LP_ERR_CUDA;
 
   LinearArgs a;
   a.targets = targets;
@@ -596,7 +616,7 @@ lp_status launch_linear(const Device& dev, const void* H, int64_t ld_h, const vo
   a.V = V_total;
   a.w_row0 = w_row0;
   a.T = static_cast<int>(T);
-  a.n_mb = static_cast<int>((T + kBM - 1) / kBM);
+  a.n_mb = static_cast<int>((T + 2 * kBM - 1) / (2 * kBM));
   a.n_kb = static_cast<int>((d + kBK - 1) / kBK);
   a.q_first = q_first;
   a.n_q = n_q;
@@ -605,10 +625,13 @@ lp_status launch_linear(const Device& dev, const void* H, int64_t ld_h, const vo
   if (total >= (int64_t(1) << 31)) return LP_ERR_INVALID_ARGUMENT;
   a.total_tiles = static_cast<int>(total);
 
-  int grid = dev.sm_count;
+  // one CTA pair per two SMs (clusters of 2), never more pairs than units
+  int pairs = dev.sm_count / 2;
   const int limit = persistent_grid_limit();
-  if (limit > 0 && limit < grid) grid = limit;
-  if (total < grid) grid = static_cast<int>(total);
+  if (limit > 0 && (limit + 1) / 2 < pairs) pairs = (limit + 1) / 2;
+  if (total < pairs) pairs = static_cast<int>(total);
+  if (pairs < 1) pairs = 1;
+  const int grid = 2 * pairs;
 
   if (cudaMemsetAsync(workspace, 0, kWorkspaceHeader, stream) != cudaSuccess) return LP_ERR_CUDA;
   cudaEvent_t ev_start, ev_stop;
