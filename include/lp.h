@@ -181,6 +181,35 @@ LP_API lp_status lp_linear_logprob(const void* H, int64_t ld_h, const void* W, i
                             void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * lp_linear_logprob_noalloc: lp_linear_logprob without a caller-provided
+ * workspace, for callers that cannot allocate device memory: code hosted by a
+ * runtime that owns every byte of device memory through its own pool and does
+ * not let plug-ins call cudaMalloc, or code on a latency-critical path where a
+ * cudaMalloc (which can synchronise the device) is not acceptable.  The pages
+ * this library follows have no counterpart of this call.
+ *
+ * It allocates nothing: its scratch is a fixed 32 MiB array in device memory
+ * that every GPU loading the library holds until the process exits.  Inputs
+ * and outputs are as in lp_linear_logprob and are still the caller's.  The
+ * results are those of lp_linear_logprob on the same inputs.
+ *
+ *   Limit: the call needs lp_linear_logprob_workspace_size(T, d, V) <= 32 MiB
+ *   (at V = 151936 that is T <= 3518 rows); larger calls return
+ *   LP_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *   Set-up: the first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ *   Sharing: all calls on a device share the array, which keeps the last
+ *   call's contents (each call clears what must start at zero).  Calls whose
+ *   work can overlap on the GPU, e.g. on two unsynchronised streams, race on
+ *   the array: order them on one stream.
+ */
+LP_API lp_status lp_linear_logprob_noalloc(const void* H, int64_t ld_h, const void* W,
+                                           int64_t ld_w, const int64_t* targets, int64_t T,
+                                           int64_t d, int64_t V, float* logp_out,
+                                           float* entropy_out, void* stream);
+
+/*
  * lp_linear_logprob_partials_workspace_size: workspace bytes for one shard.
  */
 LP_API size_t lp_linear_logprob_partials_workspace_size(int64_t T, int64_t d,

@@ -226,6 +226,25 @@ lp_status lp_linear_logprob(const void* H, int64_t ld_h, const void* W, int64_t 
                            nullptr, workspace, static_cast<cudaStream_t>(stream));
 }
 
+lp_status lp_linear_logprob_noalloc(const void* H, int64_t ld_h, const void* W, int64_t ld_w,
+                                    const int64_t* targets, int64_t T, int64_t d, int64_t V,
+                                    float* logp_out, float* entropy_out, void* stream) {
+  lp_status st = lp::check_fused_args(H, ld_h, W, ld_w, targets, T, d, V);
+  if (st != LP_OK || T == 0) return st;
+  if (logp_out == nullptr) return LP_ERR_INVALID_ARGUMENT;
+  if (!lp::aligned(logp_out, 4) || !lp::aligned(entropy_out, 4)) return LP_ERR_MISALIGNED;
+  if (lp::linear_workspace_bytes(T, V, 4) > lp::static_scratch_bytes())
+    return LP_ERR_WORKSPACE_TOO_SMALL;
+  lp::Device dev;
+  st = lp::current_device(&dev);
+  if (st != LP_OK) return st;
+  void* scratch = nullptr;
+  st = lp::static_scratch(dev.ordinal, &scratch);
+  if (st != LP_OK) return st;
+  return lp::launch_linear(dev, H, ld_h, W, ld_w, targets, T, d, V, 0, 4, logp_out, entropy_out,
+                           nullptr, scratch, static_cast<cudaStream_t>(stream));
+}
+
 lp_status lp_linear_logprob_partials(const void* H, int64_t ld_h, const void* W_shard,
                                      int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
                                      int64_t vocab_total, int shard_index, int n_shards,

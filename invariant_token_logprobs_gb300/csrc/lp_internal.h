@@ -57,6 +57,10 @@ lp_status launch_linear(const Device& dev, const void* H, int64_t ld_h, const vo
                         int64_t V_total, int q_first, int n_q, float* logp, float* entropy,
                         float* partials_out, void* workspace, cudaStream_t stream);
 
+// fixed device scratch of the no-alloc fused call
+size_t static_scratch_bytes();
+lp_status static_scratch(int ordinal, void** out);
+
 int persistent_grid_limit();
 void timing_events(cudaEvent_t* start, cudaEvent_t* stop);
 

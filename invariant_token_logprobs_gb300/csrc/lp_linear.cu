@@ -646,4 +646,43 @@ lp_status launch_linear(const Device& dev, const void* H, int64_t ld_h, const vo
   return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }
 
+// --------------------------------------------- fixed scratch for the no-alloc call
+//
+// lp_linear_logprob_noalloc runs the same two kernels as lp_linear_logprob, but
+// with its workspace in this file-scope device array instead of memory the
+// caller allocates.  Every device that loads the library holds the array until
+// the process exits.  All calls on a device share it and it keeps the last
+// call's contents; the only part that must start at zero (the error word in
+// its header) is cleared by each call on its stream.  Two calls whose work
+// overlaps on the GPU (different streams, no ordering between them) race on
+// the array and may return wrong results.
+
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;  // 32 MiB
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+size_t static_scratch_bytes() { return kStaticScratchBytes; }
+
+// Device address of g_static_scratch on the current device.  In host code the
+// array's name is only a host-side stand-in; the device address comes from
+// cudaGetSymbolAddress, called once per device with that device current (the
+// first no-alloc call on each device does it).
+lp_status static_scratch(int ordinal, void** out) {
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDev] = {};
+  if (ordinal < 0 || ordinal >= kMaxDev) return LP_ERR_UNSUPPORTED_DEVICE;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[ordinal] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return LP_ERR_CUDA;
+    }
+    addr[ordinal] = p;
+  }
+  *out = addr[ordinal];
+  return LP_OK;
+}
+
 }  // namespace lp

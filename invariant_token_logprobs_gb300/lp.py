@@ -32,6 +32,7 @@ __all__ = [
     "lp_vocab_shard_range",
     "lp_linear_logprob_workspace_size",
     "lp_linear_logprob",
+    "lp_linear_logprob_noalloc",
     "lp_linear_logprob_partials_workspace_size",
     "lp_linear_logprob_partials",
     "lp_get_device_error",
@@ -80,6 +81,7 @@ _SIGNATURES = {
     "lp_merge_partials": (_int, [ctypes.POINTER(_vp), _int, _i64, _vp, _vp, _vp]),
     "lp_linear_logprob_workspace_size": (_sz, [_i64, _i64, _i64]),
     "lp_linear_logprob": (_int, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _vp, _vp, _vp, _sz, _vp]),
+    "lp_linear_logprob_noalloc": (_int, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _vp, _vp, _vp]),
     "lp_linear_logprob_partials_workspace_size": (_sz, [_i64, _i64, _i64, _int]),
     "lp_linear_logprob_partials": (
         _int, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _int, _int, _vp, _vp, _sz, _vp]),
@@ -198,6 +200,17 @@ def lp_linear_logprob(H, W, targets, logp, entropy, workspace, stream=None) -> N
         _ptr(H), _row_stride(H), _ptr(W), _row_stride(W), _ptr(targets), T, d, V,
         _ptr(logp), _ptr(entropy), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+def lp_linear_logprob_noalloc(H, W, targets, logp, entropy=None, stream=None) -> None:
+    """lp_linear_logprob with the library's fixed device scratch instead of a
+    workspace: for callers that cannot allocate device memory (see lp.h)."""
+    _check_bf16(H, W, targets)
+    T, d = H.shape
+    V = W.shape[0]
+    _check("lp_linear_logprob_noalloc", load().lp_linear_logprob_noalloc(
+        _ptr(H), _row_stride(H), _ptr(W), _row_stride(W), _ptr(targets), T, d, V,
+        _ptr(logp), _ptr(entropy), _stream(stream)))
 
 
 def lp_linear_logprob_partials(H, W_shard, targets, vocab_total, shard_index, n_shards,

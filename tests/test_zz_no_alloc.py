@@ -1,0 +1,51 @@
+"""lp_linear_logprob_noalloc: the fused call for callers that cannot allocate
+device memory (a host runtime that owns all device memory and forbids
+cudaMalloc in plug-ins, or a latency-critical path that must not risk a
+synchronising allocation).  It uses the library's fixed device scratch instead
+of a workspace.
+
+Checked through the C ABI against lp_linear_logprob on the same inputs, on two
+calls in a row (different shapes, so the second call reuses scratch the first
+one left behind), within the fused-path tolerance (and, since both run the same
+kernels, bit for bit).  The file is named so that pytest collects it last.
+"""
+
+import pytest
+import torch
+
+from invariant_token_logprobs_gb300 import lp, synth
+from _gpu_helpers import FUSED_TOL, bits
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _compare(x):
+    T = x.H.shape[0]
+    ref_lp, ref_ent = lp.linear_logprob(x.H, x.W, x.y)
+    logp = torch.full((T,), float("nan"), device=DEV)
+    ent = torch.full((T,), float("nan"), device=DEV)
+    lp.lp_linear_logprob_noalloc(x.H, x.W, x.y, logp, ent)
+    torch.cuda.synchronize()
+    assert float((logp - ref_lp).abs().max()) <= FUSED_TOL
+    assert float((ent - ref_ent).abs().max()) <= FUSED_TOL
+    assert torch.equal(bits(logp), bits(ref_lp)) and torch.equal(bits(ent), bits(ref_ent))
+
+
+def test_noalloc_matches_workspace_call_twice_in_a_row():
+    lp.load()
+    a = synth.fused_inputs("fused_tiny", device=DEV)
+    b = synth.fused_inputs("fused_tiny", device=DEV, T=300, d=512, V=20000 + 3, seed=11)
+    _compare(a)
+    _compare(b)
+    _compare(a)
+
+
+def test_noalloc_rejects_calls_beyond_its_scratch():
+    lib = lp.load()
+    A = 1 << 20  # never dereferenced: the size check comes first
+    V, d = 151936, 4096
+    assert lp.lp_linear_logprob_workspace_size(3518, d, V) <= 32 << 20
+    assert lp.lp_linear_logprob_workspace_size(3519, d, V) > 32 << 20
+    st = lib.lp_linear_logprob_noalloc(A, d, A, d, A, 3519, d, V, A, A, None)
+    assert st == 4  # LP_ERR_WORKSPACE_TOO_SMALL
