@@ -76,6 +76,24 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(v: float, world: int, device) -> float:
+    """The largest of one float per rank (every rank gets it); identity when
+    world == 1.  `device` is where the collective's tensor lives (the GPU for
+    NCCL, the CPU for gloo)."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_throughput(rows_per_rank: int, steps: int, world: int, max_ms: float) -> float:
+    """Rows of all ranks per second of the slowest rank (weak scaling)."""
+    return world * rows_per_rank * steps / (max_ms / 1e3)
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -280,12 +298,8 @@ def run_lp(args):
         if world > 1:
             dist.barrier()
 
-    def max_over_ranks(v: float) -> float:
-        if world == 1:
-            return v
-        t = torch.tensor([v], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    def max_over(v: float) -> float:
+        return max_over_ranks(v, world, dev)
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -316,11 +330,11 @@ def run_lp(args):
     if err_word != 0:
         raise RuntimeError(f"device-side wait gave up (error word {err_word})")
 
-    total_ms = max_over_ranks(ev0.elapsed_time(ev1))
+    total_ms = max_over(ev0.elapsed_time(ev1))
     kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(k_start, k_stop))
-    kernel_ms = max_over_ranks(kernel_ms)
+    kernel_ms = max_over(kernel_ms)
     ms_per_step = total_ms / K
-    value = world * T * K / (total_ms / 1e3)
+    value = whole_job_throughput(T, K, world, total_ms)
 
     flops = 2.0 * T * d * V
     w_bytes = 2.0 * V * d + 2.0 * T * d + 8.0 * T + 8.0 * T
@@ -363,8 +377,8 @@ def run_lp(args):
         ent_host.copy_(ent, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1))
-    e2e = {"value": world * T * K2 / (e2e_ms / 1e3), "unit": "tokens/s",
+    e2e_ms = max_over(e0.elapsed_time(e1))
+    e2e = {"value": whole_job_throughput(T, K2, world, e2e_ms), "unit": "tokens/s",
            "h2d_bytes_per_step": h_host.numel() * h_host.element_size() + y_host.numel() * 8,
            "d2h_bytes_per_step": 8 * T, "steps": K2,
            "note": "W (the LM-head weight) is resident model state; per step H and targets go in and logp/entropy come out"}
@@ -372,7 +386,7 @@ def run_lp(args):
     logits_item = None
     if not args.no_logits:
         del h_host
-        logits_item = bench_logits(lp, synth, torch, dev, stream, peaks, peaks_kind, max_over_ranks,
+        logits_item = bench_logits(lp, synth, torch, dev, stream, peaks, peaks_kind, max_over,
                                    world, rank)
 
     cpu = None
@@ -402,7 +416,7 @@ def run_lp(args):
     return 0
 
 
-def bench_logits(lp, synth, torch, dev, stream, peaks, peaks_kind, max_over_ranks, world, rank):
+def bench_logits(lp, synth, torch, dev, stream, peaks, peaks_kind, max_over, world, rank):
     """Secondary line item: the logits-given path on the peaked workload."""
     z = synth.logits_inputs("logits_peaked", device=dev, seed=1 + 1000 * rank)
     T, V = z.z.shape
@@ -419,10 +433,10 @@ def bench_logits(lp, synth, torch, dev, stream, peaks, peaks_kind, max_over_rank
         lp.lp_logprob_from_logits(z.z, z.y, logp, ent)
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = max_over_ranks(e0.elapsed_time(e1)) / K
+    ms = max_over(e0.elapsed_time(e1)) / K
     nbytes = 4.0 * T * V + 8.0 * T + 8.0 * T
     gbs = nbytes / (ms / 1e3) / 1e9
-    return {"workload": "logits_peaked", "T": T, "V": V, "value": world * T / (ms / 1e3),
+    return {"workload": "logits_peaked", "T": T, "V": V, "value": whole_job_throughput(T, 1, world, ms),
             "unit": "rows/s", "us_per_call": ms * 1e3, "gpu_launches_per_call": 1,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm_gbs"], "traffic": None,
