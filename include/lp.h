@@ -174,6 +174,10 @@ LP_API size_t lp_linear_logprob_workspace_size(int64_t T, int64_t d, int64_t V);
  *               lp_linear_logprob_workspace_size(T, d, V) bytes; its contents
  *               on entry do not matter.  Do not share one workspace between
  *               calls that may run concurrently.
+ *
+ * H and W are expected to hold finite values.  Non-finite inputs never fault;
+ * a row whose logits include NaN or +inf gives NaN, and a row whose logits
+ * include -inf may give NaN instead of treating that column as absent.
  */
 LP_API lp_status lp_linear_logprob(const void* H, int64_t ld_h, const void* W, int64_t ld_w,
                             const int64_t* targets, int64_t T, int64_t d, int64_t V,

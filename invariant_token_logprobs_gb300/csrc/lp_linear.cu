@@ -251,6 +251,43 @@ __device__ __forceinline__ void tmem_load64(uint32_t taddr, float (&v)[64]) {
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Add the 64 logits of a fully valid piece to the online state (whose maximum
+// already covers them): e = 2^(x log2e - m log2e) (one fma, one ex2.approx.ftz),
+// s += e, u += e (x - m), in packed f32x2 arithmetic with four lane sums.  Used
+// only when every logit of the piece is finite, which a product of finite bf16
+// inputs always is.
+__device__ __forceinline__ void accumulate_piece_packed(const float (&v)[64], Online& st) {
+  const float mL = __fmul_rn(st.m, kLog2e);
+  uint64_t mm, ll, nml, zero;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(mm) : "f"(st.m));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(ll) : "f"(kLog2e));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(nml) : "f"(-mL));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(zero) : "f"(0.f));
+  uint64_t s2[2] = {zero, zero}, u2[2] = {zero, zero};
+#pragma unroll
+  for (int i = 0; i < 64; i += 2) {
+    uint64_t x2, d2, a2, e2;
+    float a0, a1, e0, e1;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x2) : "f"(v[i]), "f"(v[i + 1]));
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d2) : "l"(x2), "l"(mm));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(a2) : "l"(x2), "l"(ll), "l"(nml));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a2));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(a0));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(e2) : "f"(e0), "f"(e1));
+    const int k = (i >> 1) & 1;
+    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(s2[k]) : "l"(e2));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(u2[k]) : "l"(e2), "l"(d2));
+  }
+  float sa[4], ua[4];
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(sa[0]), "=f"(sa[1]) : "l"(s2[0]));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(sa[2]), "=f"(sa[3]) : "l"(s2[1]));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(ua[0]), "=f"(ua[1]) : "l"(u2[0]));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(ua[2]), "=f"(ua[3]) : "l"(u2[1]));
+  st.s = __fadd_rn(st.s, __fadd_rn(__fadd_rn(sa[0], sa[1]), __fadd_rn(sa[2], sa[3])));
+  st.u = __fadd_rn(st.u, __fadd_rn(__fadd_rn(ua[0], ua[1]), __fadd_rn(ua[2], ua[3])));
+}
+
 __device__ __forceinline__ void decode_tile(const LinearArgs& a, int u, int& mb, int& ql, int& j) {
   mb = u % a.n_mb;
   const int g = u / a.n_mb;
@@ -284,6 +321,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int pair = blockIdx.x >> 1;
   const int n_pairs = gridDim.x >> 1;
 
+  // The error word of this call starts at zero; a wait can only give up (and
+  // set it) a full time bound after every CTA of the grid has started.
+  if (blockIdx.x == 0 && threadIdx.x == 0) *a.err = 0u;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_bar(s), 1);
@@ -447,7 +487,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 1; i < 64; ++i) bm = fmax_nan(bm, v[i]);
         st.raise_to(bm);
-        if (st.active()) {
+        if (p * 64 + 64 <= valid) {
+          accumulate_piece_packed(v, st);
+        } else if (st.active()) {
           float sa[4] = {0.f, 0.f, 0.f, 0.f};
           float ua[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -488,8 +530,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // Merge the tile states of each quarter and then either finalise the row from
 // its four quarters or store the quarter states of a shard.  One block per
 // row, one warp per quarter: the quarter's maximum is exact (order-free); lane
-// l rebases tiles l, l+32, l+64, ... to it and sums them in float64, and the
-// 32 lane sums are combined by a fixed shuffle tree.  The result depends only
+// l rebases tiles l, l+32, l+64, ... to it and sums them, and the 32 lane sums
+// are combined by a fixed shuffle tree.  The result depends only
 // on the quarter's tile states.
 __global__ void __launch_bounds__(128)
     lp_tile_merge_kernel(const float4* __restrict__ chunks, const int64_t* __restrict__ targets,
@@ -506,26 +548,26 @@ __global__ void __launch_bounds__(128)
     for (int j = lane; j < n_tiles_q; j += 32) M = fmaxf(M, c[j].x);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    double S = 0.0, U = 0.0;
+    float S = 0.f, U = 0.f;
     float t = neg_inf();
     for (int j = lane; j < n_tiles_q; j += 32) {
       const float4 x = c[j];
       float s, u;
       rebase(x.x, x.y, x.z, M, s, u);
-      S = __dadd_rn(S, static_cast<double>(s));
-      U = __dadd_rn(U, static_cast<double>(u));
+      S = __fadd_rn(S, s);
+      U = __fadd_rn(U, u);
       t = fmax_nan(t, x.w);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      S = __dadd_rn(S, __shfl_down_sync(0xffffffffu, S, off));
-      U = __dadd_rn(U, __shfl_down_sync(0xffffffffu, U, off));
+      S = __fadd_rn(S, __shfl_down_sync(0xffffffffu, S, off));
+      U = __fadd_rn(U, __shfl_down_sync(0xffffffffu, U, off));
       t = fmax_nan(t, __shfl_down_sync(0xffffffffu, t, off));
     }
     if (lane == 0) {
       const int64_t y = targets[row];
       if (y < 0 || y >= V) t = quiet_nan();
-      float4 st = make_float4(M, __double2float_rn(S), __double2float_rn(U), t);
+      float4 st = make_float4(M, S, U, t);
       if (*err != 0u) st.y = quiet_nan();  // a pipeline wait gave up: no result
       if (partials_out != nullptr)
         partials_out[row * n_q + ql] = st;
@@ -633,7 +675,6 @@ lp_status launch_linear(const Device& dev, const void* H, int64_t ld_h, const vo
   if (pairs < 1) pairs = 1;
   const int grid = 2 * pairs;
 
-  if (cudaMemsetAsync(workspace, 0, kWorkspaceHeader, stream) != cudaSuccess) return LP_ERR_CUDA;
   cudaEvent_t ev_start, ev_stop;
   timing_events(&ev_start, &ev_stop);
   if (ev_start != nullptr && cudaEventRecord(ev_start, stream) != cudaSuccess) return LP_ERR_CUDA;
@@ -653,7 +694,7 @@ lp_status launch_linear(const Device& dev, const void* H, int64_t ld_h, const vo
 // caller allocates.  Every device that loads the library holds the array until
 // the process exits.  All calls on a device share it and it keeps the last
 // call's contents; the only part that must start at zero (the error word in
-// its header) is cleared by each call on its stream.  Two calls whose work
+// its header) is cleared by each call's kernel.  Two calls whose work
 // overlaps on the GPU (different streams, no ordering between them) race on
 // the array and may return wrong results.
 
