@@ -26,7 +26,10 @@ Readings where the sources are silent (each is listed with its reason in the
 design notes of this repository):
 
 * entropy is the Shannon entropy of softmax(z[t, :]) in nats;
-* no temperature is applied (tau = 1);
+* by default no temperature is applied (tau = 1); with a temperature tau > 0
+  every logit is divided by tau first (the rollout engine samples at
+  temperature 0.7: RL-Kernel H100 PCP evidence record, h100-pcp.json, section
+  ``scope``), i.e. the definition above applied to z / tau;
 * a target outside [0, V) has no defined log-probability: logp is NaN, the
   entropy is still reported;
 * a logit of -inf contributes nothing; a row whose logits are all -inf has no
@@ -71,7 +74,15 @@ def logsumexp_rows(z: np.ndarray) -> np.ndarray:
             return m[:, 0] + np.log(s)
 
 
-def selected_logprob(z: np.ndarray, y: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+def _scaled(z: np.ndarray, temperature: float) -> np.ndarray:
+    t = float(temperature)
+    if not (np.isfinite(t) and t > 0.0):
+        raise ValueError("temperature must be finite and > 0")
+    return z if t == 1.0 else z / t
+
+
+def selected_logprob(z: np.ndarray, y: np.ndarray,
+                     temperature: float = 1.0) -> tuple[np.ndarray, np.ndarray]:
     """(logp[T], entropy[T]) in float64 for logits z [T, V] and targets y [T].
 
     logp[t] = z[t, y_t] - logZ[t]: the selected-token log-probability every
@@ -81,9 +92,11 @@ def selected_logprob(z: np.ndarray, y: np.ndarray) -> tuple[np.ndarray, np.ndarr
     ``train/entropy_loss`` (H100 PCP evidence record, h100-pcp.json, section
     ``comparison``).
 
-    A target outside [0, V) gives logp = NaN.
+    A target outside [0, V) gives logp = NaN.  With ``temperature`` tau the
+    logits are z / tau (the rollout's sampling temperature, h100-pcp.json,
+    section ``scope``).
     """
-    z = np.asarray(z, dtype=np.float64)
+    z = _scaled(np.asarray(z, dtype=np.float64), temperature)
     y = np.asarray(y, dtype=np.int64)
     if z.ndim != 2 or y.shape != (z.shape[0],):
         raise ValueError("expected z [T, V] and y [T]")
@@ -123,7 +136,8 @@ def linear_logits(h: np.ndarray, w: np.ndarray) -> np.ndarray:
 
 
 def linear_selected_logprob(
-    h: np.ndarray, w: np.ndarray, y: np.ndarray, vocab_block: int = 8192
+    h: np.ndarray, w: np.ndarray, y: np.ndarray, vocab_block: int = 8192,
+    temperature: float = 1.0,
 ) -> tuple[np.ndarray, np.ndarray]:
     """(logp[T], entropy[T]) of softmax(H W^T) in float64.
 
@@ -131,7 +145,8 @@ def linear_selected_logprob(
     H100 PCP evidence record, h100-pcp.json, section ``validation``): form the
     logits with :func:`linear_logits`, then apply :func:`selected_logprob`.
     ``vocab_block`` only bounds the float64 copy of W that is alive at once; the
-    full [T, V] float64 logits are formed before any reduction.
+    full [T, V] float64 logits are formed before any reduction.  With
+    ``temperature`` tau the logits are H W^T / tau.
     """
     h = np.asarray(h)
     w = np.asarray(w)
@@ -141,4 +156,4 @@ def linear_selected_logprob(
     for v0 in range(0, v, vocab_block):
         v1 = min(v, v0 + vocab_block)
         z[:, v0:v1] = linear_logits(h, w[v0:v1])
-    return selected_logprob(z, y)
+    return selected_logprob(z, y, temperature)

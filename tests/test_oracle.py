@@ -262,6 +262,43 @@ def pin_linear_uniform_weights(impl):
         _close(e[t], mpmath.log(V), 1e-12, "linear uniform entropy")
 
 
+def pin_temperature(impl):
+    """Temperature tau divides every logit: one dominant logit raised by delta
+    gives logp = -ln(1 + (V-1) e^(-delta/tau)); a uniform row is unchanged;
+    brute force at 50 digits on z / tau."""
+    V = 1000
+    for tau in (0.7, 1.6):
+        for delta in (3.0, 9.0):
+            z = np.zeros((2, V))
+            z[:, 17] += delta
+            lp, ent = impl.selected_logprob(z, np.array([17, 18]), temperature=tau)
+            lp_peak, lp_other, e = _dominant_expect(V, delta / tau)
+            _close(lp[0], lp_peak, 1e-12, f"temperature logp tau={tau}")
+            _close(lp[1], lp_other, 1e-12, f"temperature other tau={tau}")
+            _close(ent[0], e, 1e-11, f"temperature entropy tau={tau}")
+        lp, ent = impl.selected_logprob(np.full((1, V), 4.0), np.array([3]), temperature=tau)
+        _close(lp[0], -mpmath.log(V), 1e-13, "temperature uniform")
+    rng = np.random.default_rng(23)
+    z = rng.uniform(-10, 10, size=(3, 37))
+    y = rng.integers(0, 37, size=3)
+    lp, ent = impl.selected_logprob(z, y, temperature=0.7)
+    for t in range(3):
+        zs = [mpmath.mpf(float(x)) / mpmath.mpf("0.7") for x in z[t]]
+        Z = mpmath.fsum(mpmath.e ** x for x in zs)
+        _close(lp[t], zs[int(y[t])] - mpmath.log(Z), 1e-12, "temperature brute logp")
+        H = -mpmath.fsum((mpmath.e ** x / Z) * (x - mpmath.log(Z)) for x in zs)
+        _close(ent[t], H, 1e-11, "temperature brute entropy")
+    h = _bf16_exact(rng, (2, 8), 5)
+    w = _bf16_exact(rng, (40, 8), 5)
+    yy = np.array([3, 39])
+    a = impl.linear_selected_logprob(h, w, yy, temperature=0.7)
+    b = impl.selected_logprob(impl.linear_logits(h, w), yy, temperature=0.7)
+    assert np.allclose(a[0], b[0], rtol=0, atol=1e-13) and np.allclose(a[1], b[1], rtol=0, atol=1e-13)
+    for bad in (0.0, -1.0, float("nan"), float("inf")):
+        with pytest.raises(ValueError):
+            impl.selected_logprob(z, y, temperature=bad)
+
+
 PINS = [
     pin_uniform,
     pin_dominant,
@@ -273,6 +310,7 @@ PINS = [
     pin_specials,
     pin_linear_exact,
     pin_linear_uniform_weights,
+    pin_temperature,
 ]
 
 
@@ -306,9 +344,13 @@ def test_report_pairwise_difference_is_one_ulp_at_uniform_logp():
 # ----------------------------------------------------------------------------
 
 def _sel_variant(*, shift=True, sign=1.0, tgt_off=0, ent_sign=1.0, ent_log=np.log,
-                 drop_last=False, max_axis=1, ent_weight=True):
-    def sel(z, y):
+                 drop_last=False, max_axis=1, ent_weight=True, temp_mul=False):
+    def sel(z, y, temperature=1.0):
+        t = float(temperature)
+        if not (np.isfinite(t) and t > 0.0):
+            raise ValueError("temperature")
         z = np.asarray(z, dtype=np.float64)
+        z = z * t if temp_mul else z / t
         y = np.asarray(y, dtype=np.int64)
         T, V = z.shape
         zz = z[:, :-1] if (drop_last and V > 1) else z
@@ -351,8 +393,8 @@ def _mutant(sel=None, lin=None):
     s = sel or olp.selected_logprob
     lz = lin or olp.linear_logits
 
-    def fused(h, w, y, vocab_block=8192):
-        return s(lz(h, w), y)
+    def fused(h, w, y, vocab_block=8192, temperature=1.0):
+        return s(lz(h, w), y, temperature)
 
     return types.SimpleNamespace(selected_logprob=s, linear_logits=lz, linear_selected_logprob=fused)
 
@@ -369,6 +411,7 @@ MUTANTS = {
     "projection_transposed": _mutant(lin=_linear_variant("transposed")),
     "projection_drops_last_k": _mutant(lin=_linear_variant("drop_k")),
     "projection_operands_swapped": _mutant(lin=_linear_variant("swap_operands")),
+    "temperature_multiplies": _mutant(_sel_variant(temp_mul=True)),
 }
 
 
