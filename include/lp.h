@@ -240,6 +240,44 @@ LP_API lp_status lp_linear_logprob_partials(const void* H, int64_t ld_h, const v
                                      void* stream);
 
 /* ------------------------------------------------------------------------
+ * Temperature-scaled variants: softmax(z / tau) instead of softmax(z).  The
+ * rollout engine of the RL-Kernel H100 PCP evidence record samples at
+ * temperature 0.7 (h100-pcp.json, section "scope"); these return the
+ * log-probability and entropy of the tempered distribution.
+ *
+ * Each logit is scaled as fl(z * fl(1 / tau)) in float32 before any other
+ * step, so every invariance above holds for a fixed tau, and tau == 1 gives
+ * exactly the bits of the unscaled entry points.  temperature must be finite
+ * and > 0 with 1/tau a finite positive float, else LP_ERR_INVALID_ARGUMENT.
+ * All other arguments are those of the unscaled entry point of the same name;
+ * partial states from the *_partials_temperature calls merge with
+ * lp_merge_partials (only states of one tau may be merged together).
+ * ------------------------------------------------------------------------ */
+
+LP_API lp_status lp_logprob_from_logits_temperature(const float* logits, int64_t ld_logits,
+                                                    const int64_t* targets, int64_t T,
+                                                    int64_t V, float temperature,
+                                                    float* logp_out, float* entropy_out,
+                                                    void* stream);
+
+LP_API lp_status lp_logprob_partials_from_logits_temperature(
+    const float* logits_shard, int64_t ld_logits, const int64_t* targets, int64_t T,
+    int64_t vocab_total, int shard_index, int n_shards, float temperature, float* partials_out,
+    void* stream);
+
+LP_API lp_status lp_linear_logprob_temperature(const void* H, int64_t ld_h, const void* W,
+                                               int64_t ld_w, const int64_t* targets, int64_t T,
+                                               int64_t d, int64_t V, float temperature,
+                                               float* logp_out, float* entropy_out,
+                                               void* workspace, size_t workspace_bytes,
+                                               void* stream);
+
+LP_API lp_status lp_linear_logprob_partials_temperature(
+    const void* H, int64_t ld_h, const void* W_shard, int64_t ld_w, const int64_t* targets,
+    int64_t T, int64_t d, int64_t vocab_total, int shard_index, int n_shards, float temperature,
+    float* partials_out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * Diagnostics and tuning.
  * ------------------------------------------------------------------------ */
 

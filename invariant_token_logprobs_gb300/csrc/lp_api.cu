@@ -66,6 +66,16 @@ lp_status current_device(Device* dev) {
 
 namespace {
 
+// 1/tau rounded to float; false unless tau is finite and > 0 and 1/tau is a
+// finite positive float.
+bool inverse_temperature(float temperature, float* inv) {
+  if (!(temperature > 0.0f) || !(temperature < 3.402823466e38f)) return false;
+  const double r = 1.0 / static_cast<double>(temperature);
+  if (!(r > 0.0) || r > 3.402823466e38) return false;
+  *inv = static_cast<float>(r);
+  return *inv > 0.0f;
+}
+
 lp_status check_shard(int shard_index, int n_shards) {
   if (!(n_shards == 1 || n_shards == 2 || n_shards == 4)) return LP_ERR_INVALID_ARGUMENT;
   if (shard_index < 0 || shard_index >= n_shards) return LP_ERR_INVALID_ARGUMENT;
@@ -132,9 +142,12 @@ lp_status lp_vocab_shard_range(int64_t vocab_total, int shard_index, int n_shard
   return LP_OK;
 }
 
-lp_status lp_logprob_from_logits(const float* logits, int64_t ld_logits, const int64_t* targets,
-                                 int64_t T, int64_t V, float* logp_out, float* entropy_out,
-                                 void* stream) {
+lp_status lp_logprob_from_logits_temperature(const float* logits, int64_t ld_logits,
+                                             const int64_t* targets, int64_t T, int64_t V,
+                                             float temperature, float* logp_out,
+                                             float* entropy_out, void* stream) {
+  float inv_tau;
+  if (!lp::inverse_temperature(temperature, &inv_tau)) return LP_ERR_INVALID_ARGUMENT;
   if (T < 0 || T > lp::kMaxDim / 4 || V < 1 || V > lp::kMaxDim || ld_logits < V)
     return LP_ERR_INVALID_ARGUMENT;
   if (T == 0) return LP_OK;
@@ -146,14 +159,18 @@ lp_status lp_logprob_from_logits(const float* logits, int64_t ld_logits, const i
   lp::Device dev;
   const lp_status st = lp::current_device(&dev);
   if (st != LP_OK) return st;
-  return lp::launch_logits_final(logits, ld_logits, targets, T, V, logp_out, entropy_out,
-                                 static_cast<cudaStream_t>(stream));
+  return lp::launch_logits_final(logits, ld_logits, targets, T, V, inv_tau, logp_out,
+                                 entropy_out, static_cast<cudaStream_t>(stream));
 }
 
-lp_status lp_logprob_partials_from_logits(const float* logits_shard, int64_t ld_logits,
-                                          const int64_t* targets, int64_t T,
-                                          int64_t vocab_total, int shard_index, int n_shards,
-                                          float* partials_out, void* stream) {
+lp_status lp_logprob_partials_from_logits_temperature(const float* logits_shard,
+                                                      int64_t ld_logits, const int64_t* targets,
+                                                      int64_t T, int64_t vocab_total,
+                                                      int shard_index, int n_shards,
+                                                      float temperature, float* partials_out,
+                                                      void* stream) {
+  float inv_tau;
+  if (!lp::inverse_temperature(temperature, &inv_tau)) return LP_ERR_INVALID_ARGUMENT;
   lp_status st = lp::check_shard(shard_index, n_shards);
   if (st != LP_OK) return st;
   if (T < 0 || T > lp::kMaxDim / 4 || vocab_total < 1 || vocab_total > lp::kMaxDim)
@@ -174,7 +191,7 @@ lp_status lp_logprob_partials_from_logits(const float* logits_shard, int64_t ld_
   int q_first, n_q;
   lp::shard_quarters(shard_index, n_shards, q_first, n_q);
   return lp::launch_logits_partials(logits_shard, ld_logits, targets, T, vocab_total, q_first,
-                                    n_q, partials_out, static_cast<cudaStream_t>(stream));
+                                    n_q, inv_tau, partials_out, static_cast<cudaStream_t>(stream));
 }
 
 lp_status lp_merge_partials(const float* const* shard_partials, int n_shards, int64_t T,
@@ -209,10 +226,12 @@ size_t lp_linear_logprob_partials_workspace_size(int64_t T, int64_t d, int64_t v
   return lp::linear_workspace_bytes(T, vocab_total, 4 / n_shards);
 }
 
-lp_status lp_linear_logprob(const void* H, int64_t ld_h, const void* W, int64_t ld_w,
-                            const int64_t* targets, int64_t T, int64_t d, int64_t V,
-                            float* logp_out, float* entropy_out, void* workspace,
-                            size_t workspace_bytes, void* stream) {
+lp_status lp_linear_logprob_temperature(const void* H, int64_t ld_h, const void* W, int64_t ld_w,
+                                        const int64_t* targets, int64_t T, int64_t d, int64_t V,
+                                        float temperature, float* logp_out, float* entropy_out,
+                                        void* workspace, size_t workspace_bytes, void* stream) {
+  float inv_tau;
+  if (!lp::inverse_temperature(temperature, &inv_tau)) return LP_ERR_INVALID_ARGUMENT;
   lp_status st = lp::check_fused_args(H, ld_h, W, ld_w, targets, T, d, V);
   if (st != LP_OK || T == 0) return st;
   if (logp_out == nullptr || workspace == nullptr) return LP_ERR_INVALID_ARGUMENT;
@@ -222,8 +241,8 @@ lp_status lp_linear_logprob(const void* H, int64_t ld_h, const void* W, int64_t 
   lp::Device dev;
   st = lp::current_device(&dev);
   if (st != LP_OK) return st;
-  return lp::launch_linear(dev, H, ld_h, W, ld_w, targets, T, d, V, 0, 4, logp_out, entropy_out,
-                           nullptr, workspace, static_cast<cudaStream_t>(stream));
+  return lp::launch_linear(dev, H, ld_h, W, ld_w, targets, T, d, V, 0, 4, inv_tau, logp_out,
+                           entropy_out, nullptr, workspace, static_cast<cudaStream_t>(stream));
 }
 
 lp_status lp_linear_logprob_noalloc(const void* H, int64_t ld_h, const void* W, int64_t ld_w,
@@ -241,15 +260,19 @@ lp_status lp_linear_logprob_noalloc(const void* H, int64_t ld_h, const void* W, 
   void* scratch = nullptr;
   st = lp::static_scratch(dev.ordinal, &scratch);
   if (st != LP_OK) return st;
-  return lp::launch_linear(dev, H, ld_h, W, ld_w, targets, T, d, V, 0, 4, logp_out, entropy_out,
-                           nullptr, scratch, static_cast<cudaStream_t>(stream));
+  return lp::launch_linear(dev, H, ld_h, W, ld_w, targets, T, d, V, 0, 4, 1.0f, logp_out,
+                           entropy_out, nullptr, scratch, static_cast<cudaStream_t>(stream));
 }
 
-lp_status lp_linear_logprob_partials(const void* H, int64_t ld_h, const void* W_shard,
-                                     int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
-                                     int64_t vocab_total, int shard_index, int n_shards,
-                                     float* partials_out, void* workspace,
-                                     size_t workspace_bytes, void* stream) {
+lp_status lp_linear_logprob_partials_temperature(const void* H, int64_t ld_h,
+                                                 const void* W_shard, int64_t ld_w,
+                                                 const int64_t* targets, int64_t T, int64_t d,
+                                                 int64_t vocab_total, int shard_index,
+                                                 int n_shards, float temperature,
+                                                 float* partials_out, void* workspace,
+                                                 size_t workspace_bytes, void* stream) {
+  float inv_tau;
+  if (!lp::inverse_temperature(temperature, &inv_tau)) return LP_ERR_INVALID_ARGUMENT;
   lp_status st = lp::check_shard(shard_index, n_shards);
   if (st != LP_OK) return st;
   st = lp::check_fused_args(H, ld_h, W_shard, ld_w, targets, T, d, vocab_total);
@@ -264,8 +287,42 @@ lp_status lp_linear_logprob_partials(const void* H, int64_t ld_h, const void* W_
   st = lp::current_device(&dev);
   if (st != LP_OK) return st;
   return lp::launch_linear(dev, H, ld_h, W_shard, ld_w, targets, T, d, vocab_total, q_first, n_q,
-                           nullptr, nullptr, partials_out, workspace,
+                           inv_tau, nullptr, nullptr, partials_out, workspace,
                            static_cast<cudaStream_t>(stream));
+}
+
+lp_status lp_logprob_from_logits(const float* logits, int64_t ld_logits, const int64_t* targets,
+                                 int64_t T, int64_t V, float* logp_out, float* entropy_out,
+                                 void* stream) {
+  return lp_logprob_from_logits_temperature(logits, ld_logits, targets, T, V, 1.0f, logp_out,
+                                            entropy_out, stream);
+}
+
+lp_status lp_logprob_partials_from_logits(const float* logits_shard, int64_t ld_logits,
+                                          const int64_t* targets, int64_t T,
+                                          int64_t vocab_total, int shard_index, int n_shards,
+                                          float* partials_out, void* stream) {
+  return lp_logprob_partials_from_logits_temperature(logits_shard, ld_logits, targets, T,
+                                                     vocab_total, shard_index, n_shards, 1.0f,
+                                                     partials_out, stream);
+}
+
+lp_status lp_linear_logprob(const void* H, int64_t ld_h, const void* W, int64_t ld_w,
+                            const int64_t* targets, int64_t T, int64_t d, int64_t V,
+                            float* logp_out, float* entropy_out, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  return lp_linear_logprob_temperature(H, ld_h, W, ld_w, targets, T, d, V, 1.0f, logp_out,
+                                       entropy_out, workspace, workspace_bytes, stream);
+}
+
+lp_status lp_linear_logprob_partials(const void* H, int64_t ld_h, const void* W_shard,
+                                     int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
+                                     int64_t vocab_total, int shard_index, int n_shards,
+                                     float* partials_out, void* workspace,
+                                     size_t workspace_bytes, void* stream) {
+  return lp_linear_logprob_partials_temperature(H, ld_h, W_shard, ld_w, targets, T, d,
+                                                vocab_total, shard_index, n_shards, 1.0f,
+                                                partials_out, workspace, workspace_bytes, stream);
 }
 
 lp_status lp_get_device_error(const void* workspace, size_t workspace_bytes, uint32_t* word_out,

@@ -41,12 +41,14 @@ struct Device {
 lp_status current_device(Device* dev);  // checks compute capability 10.3
 
 // logits path
+// inv_tau: every logit is multiplied by it first (1.0f: no temperature)
 lp_status launch_logits_final(const float* logits, int64_t ld, const int64_t* targets,
-                              int64_t T, int64_t V, float* logp, float* entropy,
+                              int64_t T, int64_t V, float inv_tau, float* logp, float* entropy,
                               cudaStream_t stream);
 lp_status launch_logits_partials(const float* logits_shard, int64_t ld,
                                  const int64_t* targets, int64_t T, int64_t V_total,
-                                 int q_first, int n_q, float* partials, cudaStream_t stream);
+                                 int q_first, int n_q, float inv_tau, float* partials,
+                                 cudaStream_t stream);
 lp_status launch_merge_partials(const float* const* shard_partials, int n_shards, int64_t T,
                                 float* logp, float* entropy, cudaStream_t stream);
 
@@ -54,8 +56,9 @@ lp_status launch_merge_partials(const float* const* shard_partials, int n_shards
 size_t linear_workspace_bytes(int64_t T, int64_t V_total, int n_q);
 lp_status launch_linear(const Device& dev, const void* H, int64_t ld_h, const void* W,
                         int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
-                        int64_t V_total, int q_first, int n_q, float* logp, float* entropy,
-                        float* partials_out, void* workspace, cudaStream_t stream);
+                        int64_t V_total, int q_first, int n_q, float inv_tau, float* logp,
+                        float* entropy, float* partials_out, void* workspace,
+                        cudaStream_t stream);
 
 // fixed device scratch of the no-alloc fused call
 size_t static_scratch_bytes();

@@ -39,6 +39,9 @@
 // are taken round-robin in (tile, row block) order so that the pairs that
 // share a W tile run at the same time and W is read from HBM about once.
 //
+// Temperature: with inv_tau != 1 every logit leaving tensor memory is first
+// multiplied by inv_tau; with inv_tau == 1 nothing changes.
+//
 // Every wait on an mbarrier is bounded by %globaltimer: a wait that gives up
 // sets the workspace error word and an abort flag in shared memory, the other
 // roles of that CTA stop at their next wait (the roles of the other CTA give up
@@ -85,6 +88,7 @@ struct LinearArgs {
   uint32_t* err;
   int64_t V;       // full vocabulary size
   int64_t w_row0;  // global vocabulary index of W row 0
+  float inv_tau;   // every logit is multiplied by it (1: no temperature)
   int T;
   int n_mb;        // 256-row blocks
   int n_kb;
@@ -472,6 +476,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         float v[64];
         __syncwarp();
         tmem_load64(t_lane + static_cast<uint32_t>(acc * kBN + p * 64), v);
+        if (a.inv_tau != 1.f) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) v[i] = __fmul_rn(v[i], a.inv_tau);
+        }
         if (p * 64 + 64 > valid) {
 #pragma unroll
           for (int i = 0; i < 64; ++i)
@@ -633,8 +641,9 @@ size_t linear_workspace_bytes(int64_t T, int64_t V_total, int n_q) {
 
 lp_status launch_linear(const Device& dev, const void* H, int64_t ld_h, const void* W,
                         int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
-                        int64_t V_total, int q_first, int n_q, float* logp, float* entropy,
-                        float* partials_out, void* workspace, cudaStream_t stream) {
+                        int64_t V_total, int q_first, int n_q, float inv_tau, float* logp,
+                        float* entropy, float* partials_out, void* workspace,
+                        cudaStream_t stream) {
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
@@ -657,6 +666,7 @@ lp_status launch_linear(const Device& dev, const void* H, int64_t ld_h, const vo
   a.err = static_cast<uint32_t*>(workspace);
   a.V = V_total;
   a.w_row0 = w_row0;
+  a.inv_tau = inv_tau;
   a.T = static_cast<int>(T);
   a.n_mb = static_cast<int>((T + 2 * kBM - 1) / (2 * kBM));
   a.n_kb = static_cast<int>((d + kBK - 1) / kBK);

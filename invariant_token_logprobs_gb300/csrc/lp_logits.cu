@@ -22,6 +22,10 @@
 // and after the cluster barrier rank 0 merges (Q0 + Q1) + (Q2 + Q3).  Partials
 // variant: each CTA writes its quarter state to global memory for
 // lp_merge_partials.
+//
+// Temperature: with inv_tau != 1 every logit is first multiplied by inv_tau
+// (fl(z * fl(1/tau))); with inv_tau == 1 the results are exactly those of the
+// unscaled computation.
 #include <cuda_runtime.h>
 
 #include "lp_device.cuh"
@@ -58,9 +62,12 @@ __device__ __forceinline__ void load_group(const float* __restrict__ q0, int64_t
   }
 }
 
-// State (M, S, U) of the w columns starting at q0; valid in thread 0.
+// State (M, S, U) of the w columns starting at q0, each logit multiplied by
+// inv_tau first when kScaled; valid in thread 0.
+template <bool kScaled>
 __device__ __forceinline__ void quarter_state(const float* __restrict__ q0, int64_t w,
-                                              float& M_out, float& S_out, float& U_out) {
+                                              float inv_tau, float& M_out, float& S_out,
+                                              float& U_out) {
   __shared__ float red_m[kWarps], red_s[kWarps], red_u[kWarps];
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -74,6 +81,12 @@ __device__ __forceinline__ void quarter_state(const float* __restrict__ q0, int6
     float v[kBatch][4];
 #pragma unroll
     for (int k = 0; k < kBatch; ++k) load_group(q0, w, g0 + k * kThreads + tid, vec, v[k]);
+    if (kScaled) {
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[k][i] = __fmul_rn(v[k][i], inv_tau);
+    }
     float bm = v[0][0];
 #pragma unroll
     for (int k = 0; k < kBatch; ++k)
@@ -134,18 +147,27 @@ __device__ __forceinline__ void quarter_state(const float* __restrict__ q0, int6
   }
 }
 
-// Target logit of a quarter: z[y] if y is in [c0, c1), -inf if y is another
-// valid column, NaN if y is outside [0, V).
+// Target logit of a quarter: z[y] * inv_tau if y is in [c0, c1), -inf if y is
+// another valid column, NaN if y is outside [0, V).
 __device__ __forceinline__ float quarter_target(const float* __restrict__ q0, int64_t y,
-                                                int64_t c0, int64_t c1, int64_t V) {
+                                                int64_t c0, int64_t c1, int64_t V,
+                                                float inv_tau) {
   if (y < 0 || y >= V) return quiet_nan();
-  if (y >= c0 && y < c1) return __ldg(q0 + (y - c0));
+  if (y >= c0 && y < c1) return __fmul_rn(__ldg(q0 + (y - c0)), inv_tau);
   return neg_inf();
+}
+
+__device__ __forceinline__ void quarter_state_any(const float* __restrict__ q0, int64_t w,
+                                                  float inv_tau, float& M, float& S, float& U) {
+  if (inv_tau == 1.f)
+    quarter_state<false>(q0, w, inv_tau, M, S, U);
+  else
+    quarter_state<true>(q0, w, inv_tau, M, S, U);
 }
 
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads)
     lp_logits_final_kernel(const float* __restrict__ logits, int64_t ld,
-                           const int64_t* __restrict__ targets, int64_t V,
+                           const int64_t* __restrict__ targets, int64_t V, float inv_tau,
                            float* __restrict__ logp, float* __restrict__ entropy) {
   __shared__ float4 qstates[kQuarters];
   const int q = blockIdx.x & 3;
@@ -155,9 +177,9 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads)
   const float* q0 = logits + row * ld + c0;
 
   float M, S, U;
-  quarter_state(q0, c1 - c0, M, S, U);
+  quarter_state_any(q0, c1 - c0, inv_tau, M, S, U);
   if (threadIdx.x == 0) {
-    const float t = quarter_target(q0, targets[row], c0, c1, V);
+    const float t = quarter_target(q0, targets[row], c0, c1, V, inv_tau);
     const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(&qstates[q]));
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(0));
@@ -179,7 +201,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(kThreads)
     lp_logits_partials_kernel(const float* __restrict__ logits_shard, int64_t ld,
                               const int64_t* __restrict__ targets, int64_t V, int q_first,
-                              int n_q, float4* __restrict__ partials) {
+                              int n_q, float inv_tau, float4* __restrict__ partials) {
   const int ql = blockIdx.x % n_q;
   const int64_t row = blockIdx.x / n_q;
   const int q = q_first + ql;
@@ -189,9 +211,9 @@ __global__ void __launch_bounds__(kThreads)
   const float* q0 = logits_shard + row * ld + (c0 - shard_c0);
 
   float M, S, U;
-  quarter_state(q0, c1 - c0, M, S, U);
+  quarter_state_any(q0, c1 - c0, inv_tau, M, S, U);
   if (threadIdx.x == 0) {
-    const float t = quarter_target(q0, targets[row], c0, c1, V);
+    const float t = quarter_target(q0, targets[row], c0, c1, V, inv_tau);
     partials[row * n_q + ql] = make_float4(M, S, U, t);
   }
 }
@@ -218,20 +240,22 @@ __global__ void lp_merge_partials_kernel(const float4* __restrict__ p0,
 }  // namespace
 
 lp_status launch_logits_final(const float* logits, int64_t ld, const int64_t* targets,
-                              int64_t T, int64_t V, float* logp, float* entropy,
+                              int64_t T, int64_t V, float inv_tau, float* logp, float* entropy,
                               cudaStream_t stream) {
   const int64_t blocks = T * kQuarters;
   lp_logits_final_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-      logits, ld, targets, V, logp, entropy);
+      logits, ld, targets, V, inv_tau, logp, entropy);
   return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }
 
 lp_status launch_logits_partials(const float* logits_shard, int64_t ld,
                                  const int64_t* targets, int64_t T, int64_t V_total,
-                                 int q_first, int n_q, float* partials, cudaStream_t stream) {
+                                 int q_first, int n_q, float inv_tau, float* partials,
+                                 cudaStream_t stream) {
   const int64_t blocks = T * n_q;
   lp_logits_partials_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-      logits_shard, ld, targets, V_total, q_first, n_q, reinterpret_cast<float4*>(partials));
+      logits_shard, ld, targets, V_total, q_first, n_q, inv_tau,
+      reinterpret_cast<float4*>(partials));
   return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }
 

@@ -35,6 +35,10 @@ __all__ = [
     "lp_linear_logprob_noalloc",
     "lp_linear_logprob_partials_workspace_size",
     "lp_linear_logprob_partials",
+    "lp_logprob_from_logits_temperature",
+    "lp_logprob_partials_from_logits_temperature",
+    "lp_linear_logprob_temperature",
+    "lp_linear_logprob_partials_temperature",
     "lp_get_device_error",
     "lp_set_persistent_grid_limit",
     "lp_set_kernel_timing_events",
@@ -85,6 +89,15 @@ _SIGNATURES = {
     "lp_linear_logprob_partials_workspace_size": (_sz, [_i64, _i64, _i64, _int]),
     "lp_linear_logprob_partials": (
         _int, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _int, _int, _vp, _vp, _sz, _vp]),
+    "lp_logprob_from_logits_temperature": (
+        _int, [_vp, _i64, _vp, _i64, _i64, ctypes.c_float, _vp, _vp, _vp]),
+    "lp_logprob_partials_from_logits_temperature": (
+        _int, [_vp, _i64, _vp, _i64, _i64, _int, _int, ctypes.c_float, _vp, _vp]),
+    "lp_linear_logprob_temperature": (
+        _int, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, ctypes.c_float, _vp, _vp, _vp, _sz, _vp]),
+    "lp_linear_logprob_partials_temperature": (
+        _int, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _int, _int, ctypes.c_float, _vp, _vp,
+               _sz, _vp]),
     "lp_get_device_error": (_int, [_vp, _sz, ctypes.POINTER(ctypes.c_uint32), _vp]),
     "lp_set_persistent_grid_limit": (_int, [_int]),
     "lp_set_kernel_timing_events": (_int, [_vp, _vp]),
@@ -223,6 +236,49 @@ def lp_linear_logprob_partials(H, W_shard, targets, vocab_total, shard_index, n_
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
+def lp_logprob_from_logits_temperature(logits, targets, temperature, logp, entropy=None,
+                                       stream=None) -> None:
+    if logits.dtype != torch.float32 or targets.dtype != torch.int64:
+        raise TypeError("logits must be float32 and targets int64")
+    T, V = logits.shape
+    _check("lp_logprob_from_logits_temperature", load().lp_logprob_from_logits_temperature(
+        _ptr(logits), _row_stride(logits), _ptr(targets), T, V, float(temperature), _ptr(logp),
+        _ptr(entropy), _stream(stream)))
+
+
+def lp_logprob_partials_from_logits_temperature(logits_shard, targets, vocab_total, shard_index,
+                                                n_shards, temperature, partials,
+                                                stream=None) -> None:
+    if logits_shard.dtype != torch.float32 or targets.dtype != torch.int64:
+        raise TypeError("logits must be float32 and targets int64")
+    T = logits_shard.shape[0]
+    _check("lp_logprob_partials_from_logits_temperature",
+           load().lp_logprob_partials_from_logits_temperature(
+               _ptr(logits_shard), _row_stride(logits_shard), _ptr(targets), T, vocab_total,
+               shard_index, n_shards, float(temperature), _ptr(partials), _stream(stream)))
+
+
+def lp_linear_logprob_temperature(H, W, targets, temperature, logp, entropy, workspace,
+                                  stream=None) -> None:
+    _check_bf16(H, W, targets)
+    T, d = H.shape
+    V = W.shape[0]
+    _check("lp_linear_logprob_temperature", load().lp_linear_logprob_temperature(
+        _ptr(H), _row_stride(H), _ptr(W), _row_stride(W), _ptr(targets), T, d, V,
+        float(temperature), _ptr(logp), _ptr(entropy), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def lp_linear_logprob_partials_temperature(H, W_shard, targets, vocab_total, shard_index, n_shards,
+                                           temperature, partials, workspace, stream=None) -> None:
+    _check_bf16(H, W_shard, targets)
+    T, d = H.shape
+    _check("lp_linear_logprob_partials_temperature", load().lp_linear_logprob_partials_temperature(
+        _ptr(H), _row_stride(H), _ptr(W_shard), _row_stride(W_shard), _ptr(targets), T, d,
+        vocab_total, shard_index, n_shards, float(temperature), _ptr(partials), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
 def lp_get_device_error(workspace, stream=None) -> int:
     """The workspace error word (0: no device-side wait gave up)."""
     word = ctypes.c_uint32(0)
@@ -259,11 +315,15 @@ def _workspace(nbytes: int, device) -> torch.Tensor:
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
-def logprob_from_logits(z: torch.Tensor, y: torch.Tensor, with_entropy: bool = True, stream=None):
+def logprob_from_logits(z: torch.Tensor, y: torch.Tensor, with_entropy: bool = True, stream=None,
+                        temperature: Optional[float] = None):
     T = z.shape[0]
     logp = torch.empty(T, dtype=torch.float32, device=z.device)
     ent = torch.empty(T, dtype=torch.float32, device=z.device) if with_entropy else None
-    lp_logprob_from_logits(z, y, logp, ent, stream)
+    if temperature is None:
+        lp_logprob_from_logits(z, y, logp, ent, stream)
+    else:
+        lp_logprob_from_logits_temperature(z, y, temperature, logp, ent, stream)
     return logp, ent
 
 
@@ -271,10 +331,16 @@ def vocab_shard_range(vocab_total: int, shard_index: int, n_shards: int) -> tupl
     return lp_vocab_shard_range(vocab_total, shard_index, n_shards)
 
 
-def logprob_partials_from_logits(z_shard, y, vocab_total, shard_index, n_shards, stream=None):
+def logprob_partials_from_logits(z_shard, y, vocab_total, shard_index, n_shards, stream=None,
+                                 temperature: Optional[float] = None):
     T = z_shard.shape[0]
     partials = torch.empty((T, 4 // n_shards, 4), dtype=torch.float32, device=z_shard.device)
-    lp_logprob_partials_from_logits(z_shard, y, vocab_total, shard_index, n_shards, partials, stream)
+    if temperature is None:
+        lp_logprob_partials_from_logits(z_shard, y, vocab_total, shard_index, n_shards, partials,
+                                        stream)
+    else:
+        lp_logprob_partials_from_logits_temperature(z_shard, y, vocab_total, shard_index, n_shards,
+                                                    temperature, partials, stream)
     return partials
 
 
@@ -287,24 +353,32 @@ def merge_partials(shard_partials: Sequence[torch.Tensor], with_entropy: bool = 
     return logp, ent
 
 
-def linear_logprob(H, W, y, with_entropy: bool = True, workspace=None, stream=None):
+def linear_logprob(H, W, y, with_entropy: bool = True, workspace=None, stream=None,
+                   temperature: Optional[float] = None):
     T, d = H.shape
     V = W.shape[0]
     if workspace is None:
         workspace = _workspace(lp_linear_logprob_workspace_size(T, d, V), H.device)
     logp = torch.empty(T, dtype=torch.float32, device=H.device)
     ent = torch.empty(T, dtype=torch.float32, device=H.device) if with_entropy else None
-    lp_linear_logprob(H, W, y, logp, ent, workspace, stream)
+    if temperature is None:
+        lp_linear_logprob(H, W, y, logp, ent, workspace, stream)
+    else:
+        lp_linear_logprob_temperature(H, W, y, temperature, logp, ent, workspace, stream)
     return logp, ent
 
 
 def linear_logprob_partials(H, W_shard, y, vocab_total, shard_index, n_shards, workspace=None,
-                            stream=None):
+                            stream=None, temperature: Optional[float] = None):
     T, d = H.shape
     if workspace is None:
         workspace = _workspace(
             lp_linear_logprob_partials_workspace_size(T, d, vocab_total, n_shards), H.device)
     partials = torch.empty((T, 4 // n_shards, 4), dtype=torch.float32, device=H.device)
-    lp_linear_logprob_partials(H, W_shard, y, vocab_total, shard_index, n_shards, partials,
-                               workspace, stream)
+    if temperature is None:
+        lp_linear_logprob_partials(H, W_shard, y, vocab_total, shard_index, n_shards, partials,
+                                   workspace, stream)
+    else:
+        lp_linear_logprob_partials_temperature(H, W_shard, y, vocab_total, shard_index, n_shards,
+                                               temperature, partials, workspace, stream)
     return partials

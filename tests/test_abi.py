@@ -22,7 +22,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = lp.declared_symbols()
-    assert len(names) == 14
+    assert len(names) == 18
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(lp._SIGNATURES)
@@ -102,6 +102,17 @@ def test_fused_argument_errors(lib):
     assert g(A, 256, A, 256, A, 64, 256, 8192, 0, 3, A, A, wsp, None) == INVALID  # 3 shards
     assert g(A, 256, A, 256, A, 64, 256, 8192, 1, 4, A + 4, A, wsp, None) == MISALIGNED
     assert g(A, 256, A, 256, A, 64, 256, 8192, 1, 4, A, A, wsp - 16, None) == WS_SMALL
+
+
+def test_temperature_argument_errors(lib):
+    f = lib.lp_logprob_from_logits_temperature
+    for bad in (0.0, -0.7, float("nan"), float("inf"), 1e-45):
+        assert f(A, 100, A, 4, 100, bad, A, A, None) == INVALID, bad
+    assert f(A, 100, A, 0, 100, 0.7, A, A, None) == OK
+    g = lib.lp_linear_logprob_temperature
+    ws = lp.lp_linear_logprob_workspace_size(64, 256, 8192)
+    assert g(A, 256, A, 256, A, 64, 256, 8192, -1.0, A, A, A, ws, None) == INVALID
+    assert g(A, 256, A, 256, A, 64, 256, 8192, 0.7, A, A, A, ws - 1, None) == WS_SMALL
 
 
 def test_merge_argument_errors(lib):
