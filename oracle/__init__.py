@@ -8,6 +8,8 @@ CUDA library never links, imports or calls it, and the two share no code.
 from .logprob import (  # noqa: F401
     linear_logits,
     linear_selected_logprob,
+    linear_selected_logprob_backward,
     logsumexp_rows,
     selected_logprob,
+    selected_logprob_grad_logits,
 )

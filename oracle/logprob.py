@@ -50,6 +50,8 @@ __all__ = [
     "selected_logprob",
     "linear_logits",
     "linear_selected_logprob",
+    "selected_logprob_grad_logits",
+    "linear_selected_logprob_backward",
 ]
 
 
@@ -157,3 +159,56 @@ def linear_selected_logprob(
         v1 = min(v, v0 + vocab_block)
         z[:, v0:v1] = linear_logits(h, w[v0:v1])
     return selected_logprob(z, y, temperature)
+
+
+def selected_logprob_grad_logits(z: np.ndarray, y: np.ndarray, g_logp: np.ndarray,
+                                 g_ent: np.ndarray | None = None,
+                                 temperature: float = 1.0) -> np.ndarray:
+    """dL/dz [T, V] in float64 for L = sum_t g_logp[t] logp[t] + g_ent[t] entropy[t].
+
+    The training side of the same operator (the trainer back-propagates through
+    the log-probabilities it computes: h100-pcp.json, section ``comparison``,
+    ``train/grad_norm``).  With p = softmax(z / tau):
+
+        d logp[t]    / d z[t, v] = (delta(v, y_t) - p[t, v]) / tau
+        d entropy[t] / d z[t, v] = -p[t, v] (log p[t, v] + entropy[t]) / tau
+
+    (the second from entropy = -sum_u p_u log p_u and
+    d p_u / d z_v = p_u (delta_uv - p_v) / tau).  A row whose target is outside
+    [0, V) has no logp, so its logp term contributes no gradient; 0 log 0 is
+    taken as 0.
+    """
+    z = _scaled(np.asarray(z, dtype=np.float64), temperature)
+    y = np.asarray(y, dtype=np.int64)
+    t_rows, v = z.shape
+    g_logp = np.asarray(g_logp, dtype=np.float64).reshape(t_rows)
+    g_ent = (np.zeros(t_rows) if g_ent is None
+             else np.asarray(g_ent, dtype=np.float64).reshape(t_rows))
+    log_z = logsumexp_rows(z)
+    log_p = z - log_z[:, None]
+    p = np.exp(log_p)
+    with np.errstate(invalid="ignore"):
+        ent = -np.where(p > 0.0, p * log_p, 0.0).sum(axis=1)
+        valid = (y >= 0) & (y < v)
+        g_logp = np.where(valid, g_logp, 0.0)
+        grad = -g_logp[:, None] * p
+        rows = np.arange(t_rows)[valid]
+        grad[rows, y[valid]] += g_logp[valid]
+        ent_term = np.where(p > 0.0, p * (log_p + ent[:, None]), 0.0)
+        grad -= g_ent[:, None] * ent_term
+    return grad / float(temperature)
+
+
+def linear_selected_logprob_backward(
+    h: np.ndarray, w: np.ndarray, y: np.ndarray, g_logp: np.ndarray,
+    g_ent: np.ndarray | None = None, temperature: float = 1.0,
+) -> tuple[np.ndarray, np.ndarray]:
+    """(dL/dH [T, d], dL/dW [V, d]) in float64 for the fused operator.
+
+    z = H W^T, so with G = dL/dz from :func:`selected_logprob_grad_logits`:
+    dL/dH = G W and dL/dW = G^T H (two library matrix products).
+    """
+    h64 = np.asarray(h, dtype=np.float64)
+    w64 = np.asarray(w, dtype=np.float64)
+    g = selected_logprob_grad_logits(linear_logits(h64, w64), y, g_logp, g_ent, temperature)
+    return g @ w64, g.T @ h64
