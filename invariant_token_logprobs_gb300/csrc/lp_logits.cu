@@ -96,12 +96,15 @@ __device__ __forceinline__ void quarter_state(const float* __restrict__ q0, int6
     if (st.active()) {
       float sa[4] = {0.f, 0.f, 0.f, 0.f};
       float ua[4] = {0.f, 0.f, 0.f, 0.f};
+      // e = 2^(x log2e - m log2e): one fma and one ex2.approx.ftz per logit;
+      // d = x - m clamped so that a -inf logit adds e * d = 0, NaN stays NaN
+      const float mL = __fmul_rn(st.m, kLog2e);
 #pragma unroll
       for (int k = 0; k < kBatch; ++k)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          float e, d;
-          term(v[k][i], st.m, e, d);
+          const float d = fmax_nan(__fsub_rn(v[k][i], st.m), -3.402823466e38f);
+          const float e = exp2_approx(__fmaf_rn(v[k][i], kLog2e, -mL));
           sa[i] = __fadd_rn(sa[i], e);
           ua[i] = __fmaf_rn(e, d, ua[i]);
         }

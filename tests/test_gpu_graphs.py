@@ -1,0 +1,122 @@
+"""CUDA-graph capture vs eager, byte for byte, at capture sizes 1..8.
+
+The RL-Kernel H100 PCP evidence record (h100-pcp.json, section "validation",
+"cudagraph") checks that the rollout engine captures graphs for batch sizes
+1..8 and that eager and graph-replayed results have 0 byte mismatches
+("eager_and_cuda_graph_byte_mismatches": 0).  Here each entry point is captured
+once per size on static buffers; fresh inputs are copied into those buffers
+before every replay, and the replayed outputs must equal an eager call on the
+same inputs bit for bit.
+"""
+
+import pytest
+import torch
+
+from invariant_token_logprobs_gb300 import lp, synth
+from _gpu_helpers import bits
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+SIZES = range(1, 9)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    lp.load()
+
+
+def _capture(fn):
+    """Warm up fn on a side stream, then capture it into a graph."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+@pytest.mark.parametrize("tau", [None, 0.7])
+def test_fused_graph_replay_bytes_equal_eager(tau):
+    d, V = 1024, 151936
+    W = synth.fused_inputs("fused_qwen3_8b", device=DEV, T=1, d=d, V=V).W
+    for T in SIZES:
+        H = torch.empty((T, d), dtype=torch.bfloat16, device=DEV)
+        y = torch.empty((T,), dtype=torch.int64, device=DEV)
+        logp = torch.empty(T, device=DEV)
+        ent = torch.empty(T, device=DEV)
+        ws = torch.empty(lp.lp_linear_logprob_workspace_size(T, d, V), dtype=torch.uint8, device=DEV)
+        if tau is None:
+            fn = lambda: lp.lp_linear_logprob(H, W, y, logp, ent, ws)
+        else:
+            fn = lambda: lp.lp_linear_logprob_temperature(H, W, y, tau, logp, ent, ws)
+        first = synth.fused_inputs("fused_qwen3_8b", device=DEV, T=T, d=d, V=16, seed=90 + T)
+        H.copy_(first.H)
+        y.random_(0, V)
+        g = _capture(fn)
+        for trial in range(3):
+            x = synth.fused_inputs("fused_qwen3_8b", device=DEV, T=T, d=d, V=16, seed=1000 * T + trial)
+            H.copy_(x.H)
+            y.copy_(torch.randint(0, V, (T,), device=DEV))
+            g.replay()
+            torch.cuda.synchronize()
+            got = (bits(logp), bits(ent))
+            ref = lp.linear_logprob(H.clone(), W, y.clone(), temperature=tau)
+            assert torch.equal(got[0], bits(ref[0])), f"T={T} trial {trial} logp"
+            assert torch.equal(got[1], bits(ref[1])), f"T={T} trial {trial} entropy"
+        assert lp.lp_get_device_error(ws) == 0
+
+
+@pytest.mark.parametrize("tau", [None, 0.7])
+def test_logits_graph_replay_bytes_equal_eager(tau):
+    V = 151936
+    for T in SIZES:
+        z = torch.empty((T, V), device=DEV)
+        y = torch.empty((T,), dtype=torch.int64, device=DEV)
+        logp = torch.empty(T, device=DEV)
+        ent = torch.empty(T, device=DEV)
+        if tau is None:
+            fn = lambda: lp.lp_logprob_from_logits(z, y, logp, ent)
+        else:
+            fn = lambda: lp.lp_logprob_from_logits_temperature(z, y, tau, logp, ent)
+        x0 = synth.logits_inputs("logits_peaked", device=DEV, T=T, V=V, seed=50 + T)
+        z.copy_(x0.z)
+        y.copy_(x0.y)
+        g = _capture(fn)
+        for trial in range(3):
+            x = synth.logits_inputs("logits_peaked", device=DEV, T=T, V=V, seed=700 * T + trial)
+            z.copy_(x.z)
+            y.copy_(x.y)
+            g.replay()
+            torch.cuda.synchronize()
+            ref = lp.logprob_from_logits(z.clone(), y.clone(), temperature=tau)
+            assert torch.equal(bits(logp), bits(ref[0])), f"T={T} trial {trial} logp"
+            assert torch.equal(bits(ent), bits(ref[1])), f"T={T} trial {trial} entropy"
+
+
+def test_sharded_merge_graph_replay_bytes_equal_eager():
+    """The 4-shard fused path (partials of each shard, then the fixed merge)
+    captured as one graph equals the eager unsharded call."""
+    d, V, T = 512, 151936, 8
+    x = synth.fused_inputs("fused_qwen3_next", device=DEV, T=T, d=d, V=V, seed=3)
+    ranges = [lp.vocab_shard_range(V, i, 4) for i in range(4)]
+    parts = [torch.empty((T, 1, 4), device=DEV) for _ in range(4)]
+    wss = [torch.empty(lp.lp_linear_logprob_partials_workspace_size(T, d, V, 4), dtype=torch.uint8,
+                       device=DEV) for _ in range(4)]
+    logp = torch.empty(T, device=DEV)
+    ent = torch.empty(T, device=DEV)
+
+    def fn():
+        for i, (b, e) in enumerate(ranges):
+            lp.lp_linear_logprob_partials(x.H, x.W[b:e], x.y, V, i, 4, parts[i], wss[i])
+        lp.lp_merge_partials(parts, T, logp, ent)
+
+    g = _capture(fn)
+    logp.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    ref = lp.linear_logprob(x.H, x.W, x.y)
+    assert torch.equal(bits(logp), bits(ref[0])) and torch.equal(bits(ent), bits(ref[1]))
