@@ -36,6 +36,13 @@ __host__ __device__ __forceinline__ int64_t quarter_begin(int64_t V, int q) {
 // exp(x) as exp2(x * log2 e) with CUDA's exp2f.
 __device__ __forceinline__ float exp_f(float x) { return exp2f(__fmul_rn(x, kLog2e)); }
 
+// 2^x with the hardware approximation (flushes subnormal results to zero).
+__device__ __forceinline__ float exp2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // max that returns NaN when either operand is NaN.
 __device__ __forceinline__ float fmax_nan(float a, float b) {
   float r;
