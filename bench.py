@@ -54,6 +54,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["lp", "reference"], default="lp")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-logits", action="store_true", help="skip the logits-path line item")
+    p.add_argument("--no-backward", action="store_true", help="skip the backward line item")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle baseline sample")
     return p.parse_args(argv)
@@ -389,6 +390,11 @@ def run_lp(args):
         logits_item = bench_logits(lp, synth, torch, dev, stream, peaks, peaks_kind, max_over,
                                    world, rank)
 
+    backward_item = None
+    if not args.no_backward:
+        backward_item = bench_backward(lp, torch, x, dev, stream, peaks, peaks_kind, max_over,
+                                       world)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(x, args.cpu_seconds)
@@ -408,12 +414,53 @@ def run_lp(args):
         "clocks": clocks,
         "backend": lp.lp_backend_id(),
         "logits_path": logits_item,
+        "backward_path": backward_item,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def bench_backward(lp, torch, x, dev, stream, peaks, peaks_kind, max_over, world):
+    """Line item: lp_linear_logprob_backward (grad_H and grad_W) on the headline shape."""
+    T, d = x.H.shape
+    V = x.W.shape[0]
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    gl = torch.randn(T, generator=g, device=dev)
+    ge = torch.randn(T, generator=g, device=dev)
+    ws = torch.empty(lp.lp_linear_logprob_backward_workspace_size(T, d, V), dtype=torch.uint8,
+                     device=dev)
+    gH = torch.empty((T, d), device=dev)
+    gW = torch.empty((V, d), device=dev)
+    for _ in range(2):
+        lp.lp_linear_logprob_backward(x.H, x.W, x.y, 1.0, gl, ge, gH, gW, ws)
+    K = 10
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(K):
+        lp.lp_linear_logprob_backward(x.H, x.W, x.y, 1.0, gl, ge, gH, gW, ws)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if lp.lp_get_device_error(ws) != 0:
+        raise RuntimeError("device-side wait gave up in the backward")
+    ms = max_over(e0.elapsed_time(e1)) / K
+    flops = 3 * 2.0 * T * d * V  # logits recompute, G W, G^T H
+    tf = flops / (ms / 1e3) / 1e12
+    del ws, gW
+    return {"workload": "fused_qwen3_8b backward (grad_H and grad_W, fp32 out)", "T": T, "d": d,
+            "V": V, "value": world * T / (ms / 1e3), "unit": "tokens/s", "us_per_call": ms * 1e3,
+            "gpu_launches_per_call": 9,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"], "traffic": None,
+                         "kernel": "whole backward call (4 tensor-core kernels + 5 streaming)",
+                         "algorithmic_flops_per_call": flops,
+                         "note": "executed tensor work is 4 x 2TdV (the forward statistics are recomputed)",
+                         "peak_source": f"{peaks_kind} bf16 burst"}}
 
 
 def bench_logits(lp, synth, torch, dev, stream, peaks, peaks_kind, max_over, world, rank):

@@ -278,6 +278,49 @@ LP_API lp_status lp_linear_logprob_partials_temperature(
     float* partials_out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Backward of the fused path: gradients of
+ *     L = sum_t grad_logp[t] * logp[t] + grad_entropy[t] * entropy[t]
+ * with respect to H and W, for logp and entropy of softmax(H W^T / tau).
+ * The trainer of the RL-Kernel H100 PCP evidence record back-propagates
+ * through these log-probabilities (h100-pcp.json, section "comparison",
+ * train/grad_norm).  With p = softmax(z / tau),
+ *     G[t, v] = (grad_logp[t] (delta(v, y_t) - p[t, v])
+ *                - grad_entropy[t] p[t, v] (log p[t, v] + entropy[t])) / tau,
+ *     grad_H = G W,   grad_W = G^T H.
+ * G is formed in fp32 from recomputed logits and rounded to bf16 for the two
+ * tensor-core products (fp32 accumulation).  Results are deterministic; a row
+ * of grad_H depends only on that row's inputs.  A row whose target is outside
+ * [0, V) contributes no logp gradient.
+ * ------------------------------------------------------------------------ */
+
+/* Workspace bytes of lp_linear_logprob_backward (about 2 (T + d) V + 16 T d *
+ * 4 bytes plus the forward's workspace; 0 for invalid sizes). */
+LP_API size_t lp_linear_logprob_backward_workspace_size(int64_t T, int64_t d, int64_t V);
+
+/*
+ * lp_linear_logprob_backward:
+ *   H, ld_h, W, ld_w, targets, T, d, V, temperature: as in
+ *               lp_linear_logprob_temperature (temperature 1: no scaling);
+ *               T <= 2^24.
+ *   grad_logp   [T] float32 upstream gradient of logp, or NULL (zero).
+ *   grad_entropy [T] float32 upstream gradient of entropy, or NULL (zero);
+ *               at least one of the two must be given.
+ *   grad_H      [T, d] float32 output, dense rows (stride d), 16-byte aligned.
+ *   grad_W      [V, d] float32 output, dense rows (stride d), 16-byte aligned,
+ *               or NULL to skip it.
+ *   workspace   device memory, 256-byte aligned, at least
+ *               lp_linear_logprob_backward_workspace_size(T, d, V) bytes.
+ * If a device-side wait gives up, lp_get_device_error reports it and the
+ * outputs are NaN.
+ */
+LP_API lp_status lp_linear_logprob_backward(const void* H, int64_t ld_h, const void* W,
+                                            int64_t ld_w, const int64_t* targets, int64_t T,
+                                            int64_t d, int64_t V, float temperature,
+                                            const float* grad_logp, const float* grad_entropy,
+                                            float* grad_H, float* grad_W, void* workspace,
+                                            size_t workspace_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * Diagnostics and tuning.
  * ------------------------------------------------------------------------ */
 

@@ -19,9 +19,9 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "liblp.so")
-SOURCES = ["lp_api.cu", "lp_logits.cu", "lp_linear.cu"]
+SOURCES = ["lp_api.cu", "lp_logits.cu", "lp_linear.cu", "lp_backward.cu"]
 HEADERS = [os.path.join(ROOT, "include", "lp.h")] + [
-    os.path.join(CSRC, f) for f in ("lp_device.cuh", "lp_internal.h")
+    os.path.join(CSRC, f) for f in ("lp_device.cuh", "lp_internal.h", "lp_tcgen05.cuh")
 ]
 
 NVCC_FLAGS = [

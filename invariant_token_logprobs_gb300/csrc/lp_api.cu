@@ -325,6 +325,36 @@ lp_status lp_linear_logprob_partials(const void* H, int64_t ld_h, const void* W_
                                                 partials_out, workspace, workspace_bytes, stream);
 }
 
+size_t lp_linear_logprob_backward_workspace_size(int64_t T, int64_t d, int64_t V) {
+  if (T < 0 || d < 1 || V < 1 || V > lp::kMaxDim || d > lp::kMaxDim) return 0;
+  return lp::linear_backward_workspace_bytes(T, d, V);
+}
+
+lp_status lp_linear_logprob_backward(const void* H, int64_t ld_h, const void* W, int64_t ld_w,
+                                     const int64_t* targets, int64_t T, int64_t d, int64_t V,
+                                     float temperature, const float* grad_logp,
+                                     const float* grad_entropy, float* grad_H, float* grad_W,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  float inv_tau;
+  if (!lp::inverse_temperature(temperature, &inv_tau)) return LP_ERR_INVALID_ARGUMENT;
+  lp_status st = lp::check_fused_args(H, ld_h, W, ld_w, targets, T, d, V);
+  if (st != LP_OK || T == 0) return st;
+  if (grad_H == nullptr || workspace == nullptr) return LP_ERR_INVALID_ARGUMENT;
+  if (grad_logp == nullptr && grad_entropy == nullptr) return LP_ERR_INVALID_ARGUMENT;
+  if (T > (int64_t(1) << 24)) return LP_ERR_INVALID_ARGUMENT;
+  if (!lp::aligned(grad_logp, 4) || !lp::aligned(grad_entropy, 4) || !lp::aligned(grad_H, 16) ||
+      !lp::aligned(grad_W, 16) || !lp::aligned(workspace, 256))
+    return LP_ERR_MISALIGNED;
+  if (workspace_bytes < lp::linear_backward_workspace_bytes(T, d, V))
+    return LP_ERR_WORKSPACE_TOO_SMALL;
+  lp::Device dev;
+  st = lp::current_device(&dev);
+  if (st != LP_OK) return st;
+  return lp::launch_linear_backward(dev, H, ld_h, W, ld_w, targets, T, d, V, inv_tau, grad_logp,
+                                    grad_entropy, grad_H, grad_W, workspace,
+                                    static_cast<cudaStream_t>(stream));
+}
+
 lp_status lp_get_device_error(const void* workspace, size_t workspace_bytes, uint32_t* word_out,
                               void* stream) {
   if (workspace == nullptr || workspace_bytes < lp::kWorkspaceHeader)
@@ -333,11 +363,12 @@ lp_status lp_get_device_error(const void* workspace, size_t workspace_bytes, uin
   lp::Device dev;
   const lp_status st = lp::current_device(&dev);
   if (st != LP_OK) return st;
-  uint32_t word = 0;
+  uint32_t words[4] = {0, 0, 0, 0};  // one word per pipeline kernel of a call
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+  if (cudaMemcpyAsync(words, workspace, sizeof(words), cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return LP_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return LP_ERR_CUDA;
+  const uint32_t word = words[0] | words[1] | words[2] | words[3];
   if (word_out != nullptr) *word_out = word;
   return word == 0 ? LP_OK : LP_ERR_TIMEOUT;
 }

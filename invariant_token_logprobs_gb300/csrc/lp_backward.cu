@@ -1,0 +1,447 @@
+// lp_backward.cu: gradient of the fused LM-head logprob/entropy loss.
+//
+// For L = sum_t g_logp[t] logp[t] + g_ent[t] entropy[t] with z = H W^T and
+// p = softmax(z / tau):
+//   G[t, v] = dL/dz[t, v]
+//           = (g_logp[t] (delta(v, y_t) - p[t, v])
+//              - g_ent[t] p[t, v] (log p[t, v] + entropy[t])) / tau
+//   dL/dH = G W,   dL/dW = G^T H.
+// This is the training side of the operator whose forward is lp_linear.cu (the
+// trainer of the RL-Kernel H100 PCP evidence record back-propagates through
+// these log-probabilities: h100-pcp.json, section "comparison",
+// train/grad_norm).
+//
+// Steps, all on the tensor-core pair pipeline of lp_tcgen05.cuh or plain
+// streaming kernels:
+//   1. forward kernels again, keeping per row log Z and entropy;
+//   2. lp_grad_kernel: z tiles recomputed in tensor memory; the epilogue forms
+//      G and stores it in bf16 twice, as G [T, V] and as G^T [V, T];
+//   3. lp_transpose_kernel: W^T [d, V] and H^T [d, T] in bf16, so that both
+//      products below contract over the contiguous dimension of both operands;
+//   4. lp_gemm_kernel: dH = G (W^T)^T split over 16 fixed vocabulary ranges
+//      (partial products in fp32), then lp_split_sum_kernel adds the ranges in
+//      order; dW = G^T (H^T)^T directly.
+// Every output element is produced by one CTA pair with a fixed K order and
+// split sums are added in a fixed order: the results are deterministic, and a
+// row of dH depends only on that row's inputs (not on T or its offset).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "lp_device.cuh"
+#include "lp_internal.h"
+#include "lp_tcgen05.cuh"
+
+namespace lp {
+namespace {
+
+using namespace tc;
+
+constexpr int kSplitsDH = 16;  // fixed vocabulary ranges of the dH product
+
+inline int64_t round8(int64_t x) { return (x + 7) / 8 * 8; }
+
+// ------------------------------------------------------------------ gradient
+
+struct GradTiles {  // same work list as the forward kernel: (row block, quarter, tile)
+  int64_t V;
+  int n_mb;
+  int n_kb;
+  int n_tiles_q;
+  int total;
+  __device__ __forceinline__ int units() const { return total; }
+  __device__ __forceinline__ void decode(int u, int& mb, int& q, int& j) const {
+    mb = u % n_mb;
+    const int g = u / n_mb;
+    q = g / n_tiles_q;
+    j = g % n_tiles_q;
+  }
+  __device__ __forceinline__ void coords(int u, uint32_t rank, int& a_row, int& b_row, int& kb0,
+                                         int& kb1) const {
+    int mb, q, j;
+    decode(u, mb, q, j);
+    a_row = mb * (2 * kBM) + static_cast<int>(rank) * kBM;
+    b_row = static_cast<int>(quarter_begin(V, q)) + j * kBN + static_cast<int>(rank) * kBNHalf;
+    kb0 = 0;
+    kb1 = n_kb;
+  }
+};
+
+struct GradArgs {
+  GradTiles tiles;
+  const int64_t* targets;
+  const float* g_logp;    // [T] or NULL
+  const float* g_ent;     // [T] or NULL
+  const float2* stats;    // [T] (log Z, entropy)
+  __nv_bfloat16* G;       // [T][ld_g]
+  __nv_bfloat16* Gt;      // [V][ld_gt]
+  uint32_t* err;
+  int64_t ld_g;
+  int64_t ld_gt;
+  float inv_tau;
+  int T;
+};
+
+struct GradEpilogue {
+  const GradArgs* a;
+
+  __device__ __forceinline__ void consume(int u, uint32_t taddr, uint32_t rank, int lane_grp,
+                                          int lane) {
+    int mb, q, j;
+    a->tiles.decode(u, mb, q, j);
+    const int64_t row = static_cast<int64_t>(mb) * (2 * kBM) + rank * kBM + lane_grp * 32 + lane;
+    const bool row_ok = row < a->T;
+    const int64_t qc0 = quarter_begin(a->tiles.V, q);
+    const int64_t qw = quarter_begin(a->tiles.V, q + 1) - qc0;
+    const int64_t c0 = qc0 + static_cast<int64_t>(j) * kBN;
+    const int valid = static_cast<int>(
+        max(static_cast<int64_t>(0), min(static_cast<int64_t>(kBN), qw - int64_t(j) * kBN)));
+    float gl = 0.f, ge = 0.f, log_z = 0.f, ent = 0.f;
+    int yl = -1;
+    if (row_ok) {
+      const int64_t y = a->targets[row];
+      const bool y_ok = y >= 0 && y < a->tiles.V;
+      gl = (a->g_logp != nullptr && y_ok) ? a->g_logp[row] : 0.f;
+      ge = a->g_ent != nullptr ? a->g_ent[row] : 0.f;
+      const float2 s = a->stats[row];
+      log_z = s.x;
+      ent = s.y;
+      const int64_t yl64 = y - c0;
+      if (y_ok && yl64 >= 0 && yl64 < valid) yl = static_cast<int>(yl64);
+    }
+    const float lzL = __fmul_rn(log_z, kLog2e);
+    const float scale = a->inv_tau;
+#pragma unroll 1
+    for (int p = 0; p < kBN / 64; ++p) {
+      float v[64];
+      __syncwarp();
+      tmem_load64(taddr + static_cast<uint32_t>(p * 64), v);
+      if (!row_ok || p * 64 >= valid) continue;
+      uint32_t pk[32];  // G of columns 2i, 2i+1 as packed bf16x2
+#pragma unroll
+      for (int i = 0; i < 64; i += 2) {
+        float g2[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float zs = __fmul_rn(v[i + h], scale);                   // z / tau
+          const float lp = __fsub_rn(zs, log_z);                         // log p
+          const float pr = exp2_approx(__fmaf_rn(zs, kLog2e, -lzL));     // p
+          // -p (g_logp + g_ent (log p + entropy)) + g_logp [v == y], then / tau
+          float g = -__fmul_rn(pr, __fmaf_rn(ge, __fadd_rn(lp, ent), gl));
+          if (p * 64 + i + h == yl) g = __fadd_rn(g, gl);
+          g2[h] = __fmul_rn(g, scale);
+        }
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(g2[0], g2[1]);
+        pk[i >> 1] = *reinterpret_cast<const uint32_t*>(&b2);
+      }
+      const int n = min(64, valid - p * 64);
+      const int64_t col0 = c0 + p * 64;
+      __nv_bfloat16* grow = a->G + row * a->ld_g + col0;
+      if (n == 64 && ((reinterpret_cast<uintptr_t>(grow) & 15u) == 0)) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 4)
+          *reinterpret_cast<uint4*>(grow + 2 * i) = make_uint4(pk[i], pk[i + 1], pk[i + 2], pk[i + 3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          if (i < n) {
+            const uint16_t bits = static_cast<uint16_t>(pk[i >> 1] >> (16 * (i & 1)));
+            grow[i] = *reinterpret_cast<const __nv_bfloat16*>(&bits);
+          }
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        if (i < n) {
+          const uint16_t bits = static_cast<uint16_t>(pk[i >> 1] >> (16 * (i & 1)));
+          a->Gt[(col0 + i) * a->ld_gt + row] = *reinterpret_cast<const __nv_bfloat16*>(&bits);
+        }
+      }
+    }
+  }
+  __device__ __forceinline__ void after_release(int, uint32_t, int, int) {}
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    lp_grad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ GradArgs a) {
+  GradEpilogue epi{&a};
+  run_pair_pipeline(&tmA, &tmB, a.tiles, epi, a.err);
+}
+
+// ---------------------------------------------------------------------- GEMM
+
+// C[M, N] (fp32, row stride ldc) = A[M, K] B[N, K]^T for the K blocks of split
+// s; split s writes C + s * split_stride.  Units: (row block, column block,
+// split), row block fastest.
+struct GemmTiles {
+  int n_mb, n_nb, n_split, n_kb, kb_per_split, total;
+  __device__ __forceinline__ int units() const { return total; }
+  __device__ __forceinline__ void decode(int u, int& mb, int& nb, int& s) const {
+    mb = u % n_mb;
+    const int g = u / n_mb;
+    nb = g % n_nb;
+    s = g / n_nb;
+  }
+  __device__ __forceinline__ void coords(int u, uint32_t rank, int& a_row, int& b_row, int& kb0,
+                                         int& kb1) const {
+    int mb, nb, s;
+    decode(u, mb, nb, s);
+    a_row = mb * (2 * kBM) + static_cast<int>(rank) * kBM;
+    b_row = nb * kBN + static_cast<int>(rank) * kBNHalf;
+    kb0 = s * kb_per_split;
+    kb1 = min(n_kb, kb0 + kb_per_split);
+  }
+};
+
+struct GemmArgs {
+  GemmTiles tiles;
+  float* C;
+  int64_t ldc;
+  int64_t split_stride;
+  int64_t M;
+  int64_t N;
+  uint32_t* err;
+};
+
+struct GemmEpilogue {
+  const GemmArgs* a;
+  __device__ __forceinline__ void consume(int u, uint32_t taddr, uint32_t rank, int lane_grp,
+                                          int lane) {
+    int mb, nb, s;
+    a->tiles.decode(u, mb, nb, s);
+    const int64_t row = static_cast<int64_t>(mb) * (2 * kBM) + rank * kBM + lane_grp * 32 + lane;
+    const int64_t n0 = static_cast<int64_t>(nb) * kBN;
+    float* crow = a->C + s * a->split_stride + row * a->ldc + n0;
+    const bool row_ok = row < a->M;
+    const bool vec = ((reinterpret_cast<uintptr_t>(crow) & 15u) == 0);
+#pragma unroll 1
+    for (int p = 0; p < kBN / 64; ++p) {
+      float v[64];
+      __syncwarp();
+      tmem_load64(taddr + static_cast<uint32_t>(p * 64), v);
+      if (!row_ok) continue;
+      const int64_t n_left = a->N - (n0 + p * 64);
+      if (n_left <= 0) continue;
+      float* dst = crow + p * 64;
+      if (n_left >= 64 && vec) {
+#pragma unroll
+        for (int i = 0; i < 64; i += 4)
+          *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+      } else {
+        const int n = n_left < 64 ? static_cast<int>(n_left) : 64;
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+          if (i < n) dst[i] = v[i];
+      }
+    }
+  }
+  __device__ __forceinline__ void after_release(int, uint32_t, int, int) {}
+};
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    lp_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ GemmArgs a) {
+  GemmEpilogue epi{&a};
+  run_pair_pipeline(&tmA, &tmB, a.tiles, epi, a.err);
+}
+
+// ------------------------------------------------------------- plain kernels
+
+// out[c][r] = in[r][c] for a bf16 [rows, cols] matrix, through 32 x 32 tiles
+// in shared memory.
+__global__ void __launch_bounds__(256)
+    lp_transpose_kernel(const __nv_bfloat16* __restrict__ in, int64_t rows, int64_t cols,
+                        int64_t ld_in, __nv_bfloat16* __restrict__ out, int64_t ld_out) {
+  __shared__ __nv_bfloat16 tile[32][33];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.y) * 32;
+  const int tx = threadIdx.x & 31;
+  const int ty = threadIdx.x >> 5;  // 0..7
+#pragma unroll
+  for (int k = 0; k < 32; k += 8) {
+    const int64_t r = r0 + ty + k, c = c0 + tx;
+    if (r < rows && c < cols) tile[ty + k][tx] = in[r * ld_in + c];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 32; k += 8) {
+    const int64_t c = c0 + ty + k, r = r0 + tx;
+    if (r < rows && c < cols) out[c * ld_out + r] = tile[tx][ty + k];
+  }
+}
+
+// out[i] = sum_s part[s][i] for s = 0 .. n_split-1 in order; NaN when any
+// error word of the call is set.
+__global__ void lp_split_sum_kernel(const float* __restrict__ part, int64_t n, int n_split,
+                                    const uint32_t* __restrict__ err, float* __restrict__ out) {
+  const bool failed = (err[0] | err[1] | err[2] | err[3]) != 0u;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float s = part[i];
+    for (int k = 1; k < n_split; ++k) s = __fadd_rn(s, part[k * n + i]);
+    out[i] = failed ? quiet_nan() : s;
+  }
+}
+
+// Fill out[0..n) with NaN when any error word of the call is set.
+__global__ void lp_poison_kernel(const uint32_t* __restrict__ err, float* __restrict__ out,
+                                 int64_t n) {
+  if ((err[0] | err[1] | err[2] | err[3]) == 0u) return;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    out[i] = quiet_nan();
+}
+
+struct BackwardLayout {
+  int64_t T8, V8;
+  size_t off_stats, off_logp, off_ent, off_g, off_gt, off_wt, off_ht, off_dh, total;
+};
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+BackwardLayout backward_layout(int64_t T, int64_t d, int64_t V) {
+  BackwardLayout L;
+  L.T8 = round8(T);
+  L.V8 = round8(V);
+  size_t o = align256(linear_workspace_bytes(T, V, 4));
+  L.off_stats = o; o = align256(o + sizeof(float2) * T);
+  L.off_logp = o; o = align256(o + sizeof(float) * T);
+  L.off_ent = o; o = align256(o + sizeof(float) * T);
+  L.off_g = o; o = align256(o + 2 * static_cast<size_t>(T) * L.V8);
+  L.off_gt = o; o = align256(o + 2 * static_cast<size_t>(V) * L.T8);
+  L.off_wt = o; o = align256(o + 2 * static_cast<size_t>(d) * L.V8);
+  L.off_ht = o; o = align256(o + 2 * static_cast<size_t>(d) * L.T8);
+  L.off_dh = o; o = align256(o + sizeof(float) * kSplitsDH * static_cast<size_t>(T) * d);
+  L.total = o;
+  return L;
+}
+
+lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a, const void* B,
+                      int64_t N, int64_t ld_b, int64_t K, int n_split, float* C, int64_t ldc,
+                      int64_t split_stride, uint32_t* err, cudaStream_t stream,
+                      int* n_split_out) {
+  CUtensorMap tmA, tmB;
+  if (!encode_bf16_2d(&tmA, A, M, K, ld_a, kBM)) return LP_ERR_CUDA;
+  if (!encode_bf16_2d(&tmB, B, N, K, ld_b, kBNHalf)) return LP_ERR_CUDA;
+  GemmArgs g;
+  g.tiles.n_mb = static_cast<int>((M + 2 * kBM - 1) / (2 * kBM));
+  g.tiles.n_nb = static_cast<int>((N + kBN - 1) / kBN);
+  g.tiles.n_kb = static_cast<int>((K + kBK - 1) / kBK);
+  g.tiles.kb_per_split = (g.tiles.n_kb + n_split - 1) / n_split;
+  // every split gets at least one K block (the count depends on K alone)
+  n_split = (g.tiles.n_kb + g.tiles.kb_per_split - 1) / g.tiles.kb_per_split;
+  g.tiles.n_split = n_split;
+  if (n_split_out != nullptr) *n_split_out = n_split;
+  const int64_t total = int64_t(g.tiles.n_mb) * g.tiles.n_nb * n_split;
+  if (total >= (int64_t(1) << 31)) return LP_ERR_INVALID_ARGUMENT;
+  g.tiles.total = static_cast<int>(total);
+  g.C = C;
+  g.ldc = ldc;
+  g.split_stride = split_stride;
+  g.M = M;
+  g.N = N;
+  g.err = err;
+  lp_gemm_kernel<<<pair_grid(dev.sm_count, total), kThreads, kSmemBytes, stream>>>(tmA, tmB, g);
+  return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
+}
+
+}  // namespace
+
+size_t linear_backward_workspace_bytes(int64_t T, int64_t d, int64_t V) {
+  return backward_layout(T, d, V).total;
+}
+
+lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h, const void* W,
+                                 int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
+                                 int64_t V, float inv_tau, const float* g_logp,
+                                 const float* g_ent, float* grad_h, float* grad_w,
+                                 void* workspace, cudaStream_t stream) {
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = set_pipeline_smem(reinterpret_cast<const void*>(lp_grad_kernel));
+    if (attr_err == cudaSuccess)
+      attr_err = set_pipeline_smem(reinterpret_cast<const void*>(lp_gemm_kernel));
+  });
+  if (attr_err != cudaSuccess) return LP_ERR_CUDA;
+
+  const BackwardLayout L = backward_layout(T, d, V);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* err = reinterpret_cast<uint32_t*>(ws);  // words 0..3, one per pipeline kernel
+  float2* stats = reinterpret_cast<float2*>(ws + L.off_stats);
+  auto* G = reinterpret_cast<__nv_bfloat16*>(ws + L.off_g);
+  auto* Gt = reinterpret_cast<__nv_bfloat16*>(ws + L.off_gt);
+  auto* Wt = reinterpret_cast<__nv_bfloat16*>(ws + L.off_wt);
+  auto* Ht = reinterpret_cast<__nv_bfloat16*>(ws + L.off_ht);
+  float* dh_part = reinterpret_cast<float*>(ws + L.off_dh);
+
+  // 1. forward statistics (log Z, entropy) of every row
+  lp_status st = launch_linear_stats(dev, H, ld_h, W, ld_w, targets, T, d, V, 0, 4, inv_tau,
+                                     reinterpret_cast<float*>(ws + L.off_logp),
+                                     reinterpret_cast<float*>(ws + L.off_ent), nullptr, stats,
+                                     workspace, stream);
+  if (st != LP_OK) return st;
+
+  // 2. G and G^T
+  {
+    CUtensorMap tmA, tmB;
+    if (!encode_bf16_2d(&tmA, H, T, d, ld_h, kBM)) return LP_ERR_CUDA;
+    if (!encode_bf16_2d(&tmB, W, V, d, ld_w, kBNHalf)) return LP_ERR_CUDA;
+    GradArgs g;
+    g.tiles.V = V;
+    g.tiles.n_mb = static_cast<int>((T + 2 * kBM - 1) / (2 * kBM));
+    g.tiles.n_kb = static_cast<int>((d + kBK - 1) / kBK);
+    g.tiles.n_tiles_q = static_cast<int>(tiles_per_quarter(V));
+    const int64_t total = int64_t(g.tiles.n_mb) * 4 * g.tiles.n_tiles_q;
+    if (total >= (int64_t(1) << 31)) return LP_ERR_INVALID_ARGUMENT;
+    g.tiles.total = static_cast<int>(total);
+    g.targets = targets;
+    g.g_logp = g_logp;
+    g.g_ent = g_ent;
+    g.stats = stats;
+    g.G = G;
+    g.Gt = Gt;
+    g.err = err + 1;
+    g.ld_g = L.V8;
+    g.ld_gt = L.T8;
+    g.inv_tau = inv_tau;
+    g.T = static_cast<int>(T);
+    lp_grad_kernel<<<pair_grid(dev.sm_count, total), kThreads, kSmemBytes, stream>>>(tmA, tmB, g);
+    if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
+  }
+
+  // 3. W^T and H^T
+  {
+    const dim3 gw(static_cast<unsigned>((V + 31) / 32), static_cast<unsigned>((d + 31) / 32));
+    lp_transpose_kernel<<<gw, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(W), V, d, ld_w,
+                                                Wt, L.V8);
+    const dim3 gh(static_cast<unsigned>((T + 31) / 32), static_cast<unsigned>((d + 31) / 32));
+    lp_transpose_kernel<<<gh, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(H), T, d, ld_h,
+                                                Ht, L.T8);
+    if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
+  }
+
+  // 4. dH = G W over 16 fixed vocabulary ranges, summed in order
+  int n_split = kSplitsDH;
+  st = launch_gemm(dev, G, T, L.V8, Wt, d, L.V8, V, kSplitsDH, dh_part, d, T * d, err + 2,
+                   stream, &n_split);
+  if (st != LP_OK) return st;
+  lp_split_sum_kernel<<<dev.sm_count * 4, 256, 0, stream>>>(dh_part, T * d, n_split, err,
+                                                            grad_h);
+  if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
+
+  // 5. dW = G^T H
+  if (grad_w != nullptr) {
+    st = launch_gemm(dev, Gt, V, L.T8, Ht, d, L.T8, T, 1, grad_w, d, 0, err + 3, stream,
+                     nullptr);
+    if (st != LP_OK) return st;
+    lp_poison_kernel<<<dev.sm_count * 4, 256, 0, stream>>>(err, grad_w, V * d);
+    if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
+  }
+  return LP_OK;
+}
+
+}  // namespace lp

@@ -1,0 +1,439 @@
+// lp_tcgen05.cuh: the sm_103a tensor-core pipeline shared by the fused kernels.
+//
+// A persistent grid of CTA pairs (thread-block clusters of 2, one CTA per SM)
+// computes 256 x 256 fp32 tiles D = A B^T of two K-major bf16 operands with
+// tcgen05.mma.cta_group::2 (M=256, N=256, K=16, kind::f16) into tensor memory,
+// and hands every finished tile to an epilogue.  CTA r of a pair holds rows
+// 128r..128r+127 of the A box and rows 128r..128r+127 of the B box in its own
+// shared memory and receives rows 128r.. of D in its own tensor memory, so an
+// SM stages 32 KB per 64-wide K block (a single-CTA 128 x 256 tile needs 48 KB,
+// and with the tensor core reading what TMA writes, shared-memory bandwidth is
+// what bounds it).
+//
+// Roles (6 warps per CTA):
+//   warp 0     TMA loader (both CTAs): this CTA's halves of the A and B boxes
+//              (64 x 128 each, 128-byte swizzle) into a 6-stage ring; the bytes
+//              of both CTAs complete one barrier in the leader CTA;
+//   warp 1     tensor memory: 512 columns (two 128 x 256 fp32 accumulators)
+//              allocated by both CTAs; one lane of the leader issues the MMAs
+//              and commits them to barriers in both CTAs (multicast);
+//   warps 2-5  epilogue (both CTAs): wait for a finished accumulator, run the
+//              caller's epilogue on it (one row per thread), then arrive on the
+//              leader's accumulator-empty barrier.
+// While the epilogues drain one accumulator the MMAs fill the other.
+//
+// Every mbarrier wait is bounded by %globaltimer: a wait that gives up sets
+// the call's error word and an abort flag in shared memory, the other roles of
+// that CTA stop at their next wait (the roles of the other CTA give up on their
+// own bounded waits), in-flight copies and MMAs are drained with bounded waits,
+// tensor memory is freed and the CTAs return.
+//
+// The PTX below follows the public PTX ISA: tcgen05 (alloc, mma, commit, ld,
+// fences), cp.async.bulk.tensor with .cta_group::2, mbarrier, mapa and
+// barrier.cluster.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "lp_internal.h"
+
+namespace lp {
+namespace tc {
+
+constexpr int kBM = 128;       // rows of A per CTA (tensor-memory lanes); 256 per pair
+constexpr int kBN = 256;       // columns of D per tile; 128 rows of B per CTA
+constexpr int kBNHalf = kBN / 2;
+constexpr int kBK = 64;        // K per pipeline stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kUmmaK = 16;
+constexpr int kStages = 6;
+constexpr int kABytes = kBM * kBK * 2;       // 16 KB
+constexpr int kBBytes = kBNHalf * kBK * 2;   // 16 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kThreads = 192;
+constexpr int kEpilogueThreads = 128;
+constexpr uint32_t kTmemCols = 2 * kBN;
+constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;
+constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kNumBars * 8 + 16;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
+
+static_assert(kBN == kTileN, "the vocabulary tile of the fused path is one MMA tile");
+
+// Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B bf16
+// (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 in
+// bits 17-22, M >> 4 in bits 24-28; M = 256 for the CTA pair.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
+                            (uint32_t(kBN >> 3) << 17) | (uint32_t((2 * kBM) >> 4) << 24);
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait for the phase of `bar` with parity `parity`.  Returns false when
+// the CTA is aborting or this wait gave up (then it raises the abort).
+static __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                      uint32_t* err, uint32_t role_bit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicOr(err, role_bit);
+      return false;
+    }
+  }
+}
+
+// Bounded wait used while draining after an abort; never raises anything.
+static __device__ __noinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = global_timer();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer() - t0 > kWaitLimitNs) return;
+  }
+}
+
+// TMA load of a box into this CTA's shared memory; the transferred bytes are
+// counted on `bar`, a shared::cluster address that may lie in the peer CTA.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Arrive on `bar` (same offset) in both CTAs of the pair once every MMA issued
+// so far by this thread has completed.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  const uint16_t both = 3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(bar),
+      "h"(both)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with
+// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+// Start address >> 4 in bits 0-13, leading-dimension offset (unused for this
+// layout, set to 16 bytes) in bits 16-29, stride offset 1024 >> 4 in bits
+// 32-45, descriptor version 1 in bits 46-47, swizzle mode 2 (128-byte) in
+// bits 61-63.  The tile base is 1024-byte aligned, so the K offset of each
+// 16-element MMA step is added to the start address.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(16 >> 4) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// 64 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_load64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, "
+      "%45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, "
+      "%62, %63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]),
+        "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]),
+        "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]),
+        "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]),
+        "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ------------------------------------------------------------------ pipeline
+//
+// Sched (work list, the same on every CTA):
+//   int units() const;
+//   void coords(int u, uint32_t rank, int& a_row, int& b_row, int& kb0, int& kb1) const;
+//     rows of this CTA's A and B boxes and the K blocks [kb0, kb1) of unit u
+//     (kb1 > kb0 always).
+// Epi (one per epilogue thread):
+//   void consume(int u, uint32_t taddr, uint32_t rank, int lane_grp, int lane);
+//     read the finished 128 x 256 accumulator (this thread's lane at taddr,
+//     columns taddr + 0..255, with tmem_load64; warp-collective) and use it;
+//   void after_release(int u, uint32_t rank, int lane_grp, int lane);
+//     work that no longer needs tensor memory (after the accumulator is freed).
+//
+// Called by every thread of a CTA of a 2-CTA cluster launched with kThreads
+// threads and kSmemBytes of dynamic shared memory.
+template <class Sched, class Epi>
+__device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                                  const Sched& sch, Epi& epi, uint32_t* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();  // 0: leader (issues the MMAs), 1: peer
+  const int pair = blockIdx.x >> 1;
+  const int n_pairs = gridDim.x >> 1;
+  const int units = sch.units();
+
+  // The error word of this call starts at zero; a wait can only give up (and
+  // set it) a full time bound after every CTA of the grid has started.
+  if (blockIdx.x == 0 && threadIdx.x == 0) *err = 0u;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 2 * kEpilogueThreads);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmB)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  __syncwarp();
+  cluster_sync();  // both CTAs' barriers initialised and tensor memory allocated
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA loader
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t pending = 0;         // stages with a load in flight (leader: bit mask)
+      uint32_t pending_parity = 0;  // parity of that load's phase
+      bool ok = true;
+      for (int u = pair; ok && u < units; u += n_pairs) {
+        int a_row, b_row, kb0, kb1;
+        sch.coords(u, rank, a_row, b_row, kb0, kb1);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, err, kErrLoader)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+          const uint32_t leader_full = cluster_addr(full_bar(stage), 0);
+          if (rank == 0) {
+            mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytes);
+            pending |= 1u << stage;
+            pending_parity = (pending_parity & ~(1u << stage)) | (phase << stage);
+          }
+          tma_load_2d(sa, tmA, kb * kBK, a_row, leader_full);
+          tma_load_2d(sa + kABytes, tmB, kb * kBK, b_row, leader_full);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && rank == 0) {  // let every issued copy land before the pair can exit
+        for (int s = 0; s < kStages; ++s)
+          if (pending & (1u << s)) drain_wait(full_bar(s), (pending_parity >> s) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      if (rank == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        for (int u = pair; ok && u < units; u += n_pairs) {
+          int a_row, b_row, kb0, kb1;
+          sch.coords(u, rank, a_row, b_row, kb0, kb1);
+          if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, abort_flag, err, kErrMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!wait_bar(full_bar(stage), phase, abort_flag, err, kErrMma)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+            const uint32_t sb = sa + kABytes;
+#pragma unroll
+            for (int k = 0; k < kBK / kUmmaK; ++k) {
+              tc_mma(d_tmem, sw128_desc(sa + k * kUmmaK * 2), sw128_desc(sb + k * kUmmaK * 2),
+                     (kb != kb0 || k != 0) ? 1u : 0u);
+            }
+            tc_commit_pair(empty_bar(stage));  // frees the stage in both CTAs
+            if (++stage == kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          tc_commit_pair(tfull_bar(acc));  // accumulator ready in both CTAs
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1u;
+        }
+        tc_commit_pair(drain_bar);  // arrives once every MMA issued here is done
+      }
+      drain_wait(drain_bar, 0);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int lane_grp = warp & 3;  // tensor-memory lanes 32*lane_grp .. +31
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(lane_grp * 32) << 16);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = pair; u < units; u += n_pairs) {
+      // one lane waits, the warp follows (tcgen05.ld is warp-collective)
+      int go = 1;
+      if (lane == 0) go = wait_bar(tfull_bar(acc), acc_phase, abort_flag, err, kErrEpilogue);
+      go = __shfl_sync(0xffffffffu, go, 0);
+      if (!go) break;
+      tc_fence_after();
+      epi.consume(u, t_lane + static_cast<uint32_t>(acc * kBN), rank, lane_grp, lane);
+      tc_fence_before();
+      mbar_arrive_cluster(cluster_addr(tempty_bar(acc), 0));
+      epi.after_release(u, rank, lane_grp, lane);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  __syncwarp();
+  cluster_sync();  // no remote arrive or copy into either CTA is still pending
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------ host helpers
+
+// 2-D bf16 tensor map over [rows, cols] (cols contiguous, row stride ld
+// elements) with a box of [box_rows, 64] and 128-byte swizzle; out-of-range
+// elements read as zero.  Returns false if the driver rejects it.
+bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
+                    int box_rows);
+
+// Persistent grid (in CTAs, even) for `units` units on `sm_count` SMs under the
+// process-wide CTA limit: one CTA pair per two SMs, never more pairs than units.
+int pair_grid(int sm_count, int64_t units);
+
+// Give `kernel` the dynamic shared memory of the pipeline (once per kernel).
+cudaError_t set_pipeline_smem(const void* kernel);
+
+}  // namespace tc
+}  // namespace lp

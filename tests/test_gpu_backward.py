@@ -1,0 +1,119 @@
+"""Backward of the fused path on a GB300: grad_H and grad_W against the fp64
+oracle, determinism, and row invariance of grad_H.
+
+Tolerance (from the arithmetic): the kernel forms G = dL/dz in fp32 and rounds
+it to bf16 (relative error <= 2^-9) before two tensor-core products with fp32
+accumulation (whose error over K <= 151936 terms is far below that), so an
+element of grad_H = G W may be off by at most about 2^-9 sum_v |G[t,v] W[v,k]|
+and one of grad_W = G^T H by 2^-9 sum_t |G[t,v] H[t,k]|.  The tests allow
+2^-8 times those sums (computed in fp64 from the oracle's G) plus 1e-6.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from invariant_token_logprobs_gb300 import lp, synth
+from _gpu_helpers import bits
+
+import oracle
+from oracle import logprob as olp
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    lp.load()
+
+
+def _upstream(T, seed, with_logp=True, with_ent=True):
+    g = torch.Generator(device=DEV)
+    g.manual_seed(seed)
+    gl = torch.randn(T, generator=g, device=DEV) if with_logp else None
+    ge = torch.randn(T, generator=g, device=DEV) * 0.5 if with_ent else None
+    return gl, ge
+
+
+def _np(t):
+    return None if t is None else t.double().cpu().numpy()
+
+
+def _check_against_oracle(x, gl, ge, tau, gH, gW, rows=None):
+    h = x.H.float().cpu().numpy().astype(np.float64)
+    w = x.W.float().cpu().numpy().astype(np.float64)
+    y = x.y.cpu().numpy()
+    T = h.shape[0]
+    gl_np = np.zeros(T) if gl is None else _np(gl)
+    ge_np = np.zeros(T) if ge is None else _np(ge)
+    z = np.empty((T, w.shape[0]))
+    for v0 in range(0, w.shape[0], 8192):
+        z[:, v0:v0 + 8192] = olp.linear_logits(h, w[v0:v0 + 8192])
+    G = olp.selected_logprob_grad_logits(z, y, gl_np, ge_np, temperature=tau)
+    del z
+    r = np.arange(T) if rows is None else np.asarray(rows)
+    ref_h = G[r] @ w
+    bound_h = 2.0 ** -8 * (np.abs(G[r]) @ np.abs(w)) + 1e-6
+    got_h = gH[torch.as_tensor(r)].double().cpu().numpy()
+    err_h = np.abs(got_h - ref_h)
+    assert np.all(err_h <= bound_h), (float(err_h.max()), float((err_h / bound_h).max()))
+    out = {"grad_H_max_err": float(err_h.max()), "grad_H_max_ratio": float((err_h / bound_h).max())}
+    if gW is not None:
+        vs = np.unique(np.concatenate([np.arange(0, w.shape[0], max(1, w.shape[0] // 97)),
+                                       y[y < w.shape[0]][:16]]))
+        ref_w = G[:, vs].T @ h
+        bound_w = 2.0 ** -8 * (np.abs(G[:, vs]).T @ np.abs(h)) + 1e-6
+        got_w = gW[torch.as_tensor(vs)].double().cpu().numpy()
+        err_w = np.abs(got_w - ref_w)
+        assert np.all(err_w <= bound_w), (float(err_w.max()), float((err_w / bound_w).max()))
+        out["grad_W_max_err"] = float(err_w.max())
+    return out
+
+
+@pytest.mark.parametrize("T,d,V,tau", [(64, 256, 8192, 1.0), (37, 72, 1001, 0.7),
+                                       (300, 128, 20003, 1.0), (1, 64, 512, 1.6)])
+def test_backward_small_against_oracle(T, d, V, tau):
+    x = synth.fused_inputs("fused_tiny", device=DEV, T=T, d=d, V=V, seed=T + V)
+    gl, ge = _upstream(T, seed=T)
+    gH, gW = lp.linear_logprob_backward(x.H, x.W, x.y, gl, ge, temperature=tau)
+    torch.cuda.synchronize()
+    _check_against_oracle(x, gl, ge, tau, gH, gW)
+
+
+def test_backward_one_upstream_and_bad_targets():
+    x = synth.fused_inputs("fused_tiny", device=DEV, T=40, d=128, V=5000, seed=12)
+    x.y[3] = -1
+    x.y[7] = 5000
+    gl, ge = _upstream(40, seed=5)
+    for a, b in ((gl, None), (None, ge)):
+        gH, gW = lp.linear_logprob_backward(x.H, x.W, x.y, a, b)
+        torch.cuda.synchronize()
+        _check_against_oracle(x, a, b, 1.0, gH, gW)
+    gH, none = lp.linear_logprob_backward(x.H, x.W, x.y, gl, ge, with_grad_W=False)
+    assert none is None and torch.isfinite(gH).all()
+
+
+def test_backward_qwen3_8b_head_sampled():
+    x = synth.fused_inputs("fused_qwen3_8b", device=DEV)
+    gl, ge = _upstream(512, seed=2)
+    gH, gW = lp.linear_logprob_backward(x.H, x.W, x.y, gl, ge)
+    torch.cuda.synchronize()
+    out = _check_against_oracle(x, gl, ge, 1.0, gH, gW, rows=[0, 255, 256, 511])
+    print(f"qwen3-8b head backward: {out}")
+
+
+def test_backward_deterministic_and_row_invariant():
+    x = synth.fused_inputs("fused_tiny", device=DEV, T=300, d=256, V=30000, seed=4)
+    gl, ge = _upstream(300, seed=9)
+    ref_h, ref_w = lp.linear_logprob_backward(x.H, x.W, x.y, gl, ge)
+    for _ in range(3):
+        h, w = lp.linear_logprob_backward(x.H, x.W, x.y, gl, ge)
+        assert torch.equal(bits(h.reshape(-1)), bits(ref_h.reshape(-1)))
+        assert torch.equal(bits(w.reshape(-1)), bits(ref_w.reshape(-1)))
+    # rows of grad_H depend only on their own inputs
+    sub = slice(100, 140)
+    h_sub, _ = lp.linear_logprob_backward(x.H[sub].contiguous(), x.W, x.y[sub],
+                                          gl[sub].contiguous(), ge[sub].contiguous(),
+                                          with_grad_W=False)
+    assert torch.equal(bits(h_sub.reshape(-1)), bits(ref_h[sub].reshape(-1)))
