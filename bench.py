@@ -454,10 +454,10 @@ def bench_backward(lp, torch, x, dev, stream, peaks, peaks_kind, max_over, world
     del ws, gW
     return {"workload": "fused_qwen3_8b backward (grad_H and grad_W, fp32 out)", "T": T, "d": d,
             "V": V, "value": world * T / (ms / 1e3), "unit": "tokens/s", "us_per_call": ms * 1e3,
-            "gpu_launches_per_call": 9,
+            "gpu_launches_per_call": 7,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"], "traffic": None,
-                         "kernel": "whole backward call (4 tensor-core kernels + 5 streaming)",
+                         "kernel": "whole backward call (4 tensor-core kernels + 3 small ones)",
                          "algorithmic_flops_per_call": flops,
                          "note": "executed tensor work is 4 x 2TdV (the forward statistics are recomputed)",
                          "peak_source": f"{peaks_kind} bf16 burst"}}

@@ -293,8 +293,9 @@ LP_API lp_status lp_linear_logprob_partials_temperature(
  * [0, V) contributes no logp gradient.
  * ------------------------------------------------------------------------ */
 
-/* Workspace bytes of lp_linear_logprob_backward (about 2 (T + d) V + 16 T d *
- * 4 bytes plus the forward's workspace; 0 for invalid sizes). */
+/* Workspace bytes of lp_linear_logprob_backward: the forward's workspace, the
+ * bf16 G [T, V] (2 T V bytes) and 16 fp32 partial grad_H (64 T d bytes);
+ * 0 for invalid sizes. */
 LP_API size_t lp_linear_logprob_backward_workspace_size(int64_t T, int64_t d, int64_t V);
 
 /*
@@ -351,6 +352,17 @@ LP_API lp_status lp_set_persistent_grid_limit(int max_ctas);
  * stop recording.  Process-wide setting; not for concurrent callers.
  */
 LP_API lp_status lp_set_kernel_timing_events(void* start_event, void* stop_event);
+
+/*
+ * lp_set_fault_injection: tests of the bounded device-side waits.  Mode 1:
+ * every later fused forward call withholds one TMA load of its first CTA pair,
+ * so that pair's pipeline waits give up after their time bound (about a second
+ * each); the call still returns LP_OK, its outputs are NaN and
+ * lp_get_device_error returns LP_ERR_TIMEOUT.  No fault is raised on the
+ * device and the context stays usable.  Mode 0 (the default) turns it off.
+ * Process-wide setting; not for production use.
+ */
+LP_API lp_status lp_set_fault_injection(int mode);
 
 /* Human-readable name of a status code (static storage). */
 LP_API const char* lp_status_string(lp_status status);

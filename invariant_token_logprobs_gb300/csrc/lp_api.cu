@@ -18,6 +18,7 @@ namespace lp {
 
 namespace {
 std::atomic<int> g_grid_limit{0};
+std::atomic<int> g_fault_injection{0};
 std::atomic<cudaEvent_t> g_ev_start{nullptr};
 std::atomic<cudaEvent_t> g_ev_stop{nullptr};
 
@@ -30,6 +31,7 @@ constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 }  // namespace
 
 int persistent_grid_limit() { return g_grid_limit.load(std::memory_order_relaxed); }
+int fault_injection() { return g_fault_injection.load(std::memory_order_relaxed); }
 
 void timing_events(cudaEvent_t* start, cudaEvent_t* stop) {
   *start = g_ev_start.load(std::memory_order_acquire);
@@ -119,6 +121,12 @@ const char* lp_backend_id(void) { return "lp.sm103a.bitwise.v1"; }
 lp_status lp_set_persistent_grid_limit(int max_ctas) {
   if (max_ctas < 0) return LP_ERR_INVALID_ARGUMENT;
   lp::g_grid_limit.store(max_ctas, std::memory_order_relaxed);
+  return LP_OK;
+}
+
+lp_status lp_set_fault_injection(int mode) {
+  if (mode != 0 && mode != 1) return LP_ERR_INVALID_ARGUMENT;
+  lp::g_fault_injection.store(mode, std::memory_order_relaxed);
   return LP_OK;
 }
 

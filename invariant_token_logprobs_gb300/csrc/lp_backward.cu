@@ -11,19 +11,19 @@
 // these log-probabilities: h100-pcp.json, section "comparison",
 // train/grad_norm).
 //
-// Steps, all on the tensor-core pair pipeline of lp_tcgen05.cuh or plain
-// streaming kernels:
+// Steps, all on the tensor-core pair pipeline of lp_tcgen05.cuh:
 //   1. forward kernels again, keeping per row log Z and entropy;
 //   2. lp_grad_kernel: z tiles recomputed in tensor memory; the epilogue forms
-//      G and stores it in bf16 twice, as G [T, V] and as G^T [V, T];
-//   3. lp_transpose_kernel: W^T [d, V] and H^T [d, T] in bf16, so that both
-//      products below contract over the contiguous dimension of both operands;
-//   4. lp_gemm_kernel: dH = G (W^T)^T split over 16 fixed vocabulary ranges
-//      (partial products in fp32), then lp_split_sum_kernel adds the ranges in
-//      order; dW = G^T (H^T)^T directly.
-// Every output element is produced by one CTA pair with a fixed K order and
-// split sums are added in a fixed order: the results are deterministic, and a
-// row of dH depends only on that row's inputs (not on T or its offset).
+//      G in fp32 and stores it in bf16 as G [T, V];
+//   3. lp_gemm_kernel<K-major A, N-major B>: dH = G W, reading W [V, d] as an
+//      N-major operand, over 16 fixed vocabulary ranges (partial products in
+//      fp32), then lp_split_sum_kernel adds the ranges in order;
+//   4. lp_gemm_kernel<M-major A, N-major B>: dW = G^T H, reading G [T, V] as an
+//      M-major operand and H [T, d] as an N-major one.
+// No operand is transposed in memory.  Every output element is produced by one
+// CTA pair with a fixed K order and split sums are added in a fixed order: the
+// results are deterministic, and a row of dH depends only on that row's inputs
+// (not on T or its offset).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -76,10 +76,8 @@ struct GradArgs {
   const float* g_ent;     // [T] or NULL
   const float2* stats;    // [T] (log Z, entropy)
   __nv_bfloat16* G;       // [T][ld_g]
-  __nv_bfloat16* Gt;      // [V][ld_gt]
   uint32_t* err;
   int64_t ld_g;
-  int64_t ld_gt;
   float inv_tau;
   int T;
 };
@@ -150,13 +148,6 @@ struct GradEpilogue {
             const uint16_t bits = static_cast<uint16_t>(pk[i >> 1] >> (16 * (i & 1)));
             grow[i] = *reinterpret_cast<const __nv_bfloat16*>(&bits);
           }
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        if (i < n) {
-          const uint16_t bits = static_cast<uint16_t>(pk[i >> 1] >> (16 * (i & 1)));
-          a->Gt[(col0 + i) * a->ld_gt + row] = *reinterpret_cast<const __nv_bfloat16*>(&bits);
         }
       }
     }
@@ -241,37 +232,15 @@ struct GemmEpilogue {
   __device__ __forceinline__ void after_release(int, uint32_t, int, int) {}
 };
 
+template <bool kAMn, bool kBMn>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     lp_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ GemmArgs a) {
   GemmEpilogue epi{&a};
-  run_pair_pipeline(&tmA, &tmB, a.tiles, epi, a.err);
+  run_pair_pipeline<GemmTiles, GemmEpilogue, kAMn, kBMn>(&tmA, &tmB, a.tiles, epi, a.err);
 }
 
 // ------------------------------------------------------------- plain kernels
-
-// out[c][r] = in[r][c] for a bf16 [rows, cols] matrix, through 32 x 32 tiles
-// in shared memory.
-__global__ void __launch_bounds__(256)
-    lp_transpose_kernel(const __nv_bfloat16* __restrict__ in, int64_t rows, int64_t cols,
-                        int64_t ld_in, __nv_bfloat16* __restrict__ out, int64_t ld_out) {
-  __shared__ __nv_bfloat16 tile[32][33];
-  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32;
-  const int64_t c0 = static_cast<int64_t>(blockIdx.y) * 32;
-  const int tx = threadIdx.x & 31;
-  const int ty = threadIdx.x >> 5;  // 0..7
-#pragma unroll
-  for (int k = 0; k < 32; k += 8) {
-    const int64_t r = r0 + ty + k, c = c0 + tx;
-    if (r < rows && c < cols) tile[ty + k][tx] = in[r * ld_in + c];
-  }
-  __syncthreads();
-#pragma unroll
-  for (int k = 0; k < 32; k += 8) {
-    const int64_t c = c0 + ty + k, r = r0 + tx;
-    if (r < rows && c < cols) out[c * ld_out + r] = tile[tx][ty + k];
-  }
-}
 
 // out[i] = sum_s part[s][i] for s = 0 .. n_split-1 in order; NaN when any
 // error word of the call is set.
@@ -296,36 +265,44 @@ __global__ void lp_poison_kernel(const uint32_t* __restrict__ err, float* __rest
 }
 
 struct BackwardLayout {
-  int64_t T8, V8;
-  size_t off_stats, off_logp, off_ent, off_g, off_gt, off_wt, off_ht, off_dh, total;
+  int64_t V8;
+  size_t off_stats, off_logp, off_ent, off_g, off_dh, total;
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 BackwardLayout backward_layout(int64_t T, int64_t d, int64_t V) {
   BackwardLayout L;
-  L.T8 = round8(T);
   L.V8 = round8(V);
   size_t o = align256(linear_workspace_bytes(T, V, 4));
   L.off_stats = o; o = align256(o + sizeof(float2) * T);
   L.off_logp = o; o = align256(o + sizeof(float) * T);
   L.off_ent = o; o = align256(o + sizeof(float) * T);
   L.off_g = o; o = align256(o + 2 * static_cast<size_t>(T) * L.V8);
-  L.off_gt = o; o = align256(o + 2 * static_cast<size_t>(V) * L.T8);
-  L.off_wt = o; o = align256(o + 2 * static_cast<size_t>(d) * L.V8);
-  L.off_ht = o; o = align256(o + 2 * static_cast<size_t>(d) * L.T8);
   L.off_dh = o; o = align256(o + sizeof(float) * kSplitsDH * static_cast<size_t>(T) * d);
   L.total = o;
   return L;
 }
 
+// C = A B^T over the pipeline.  A is [M, K] (K-major, row stride ld_a) or,
+// with kAMn, [K, M] (M contiguous); B likewise with N.
+template <bool kAMn, bool kBMn>
 lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a, const void* B,
                       int64_t N, int64_t ld_b, int64_t K, int n_split, float* C, int64_t ldc,
                       int64_t split_stride, uint32_t* err, cudaStream_t stream,
                       int* n_split_out) {
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = set_pipeline_smem(reinterpret_cast<const void*>(lp_gemm_kernel<kAMn, kBMn>));
+  });
+  if (attr_err != cudaSuccess) return LP_ERR_CUDA;
   CUtensorMap tmA, tmB;
-  if (!encode_bf16_2d(&tmA, A, M, K, ld_a, kBM)) return LP_ERR_CUDA;
-  if (!encode_bf16_2d(&tmB, B, N, K, ld_b, kBNHalf)) return LP_ERR_CUDA;
+  const bool okA = kAMn ? encode_bf16_2d(&tmA, A, K, M, ld_a, 64)
+                        : encode_bf16_2d(&tmA, A, M, K, ld_a, kBM);
+  const bool okB = kBMn ? encode_bf16_2d(&tmB, B, K, N, ld_b, 64)
+                        : encode_bf16_2d(&tmB, B, N, K, ld_b, kBNHalf);
+  if (!okA || !okB) return LP_ERR_CUDA;
   GemmArgs g;
   g.tiles.n_mb = static_cast<int>((M + 2 * kBM - 1) / (2 * kBM));
   g.tiles.n_nb = static_cast<int>((N + kBN - 1) / kBN);
@@ -344,7 +321,8 @@ lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a,
   g.M = M;
   g.N = N;
   g.err = err;
-  lp_gemm_kernel<<<pair_grid(dev.sm_count, total), kThreads, kSmemBytes, stream>>>(tmA, tmB, g);
+  lp_gemm_kernel<kAMn, kBMn>
+      <<<pair_grid(dev.sm_count, total), kThreads, kSmemBytes, stream>>>(tmA, tmB, g);
   return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }
 
@@ -363,8 +341,6 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
     attr_err = set_pipeline_smem(reinterpret_cast<const void*>(lp_grad_kernel));
-    if (attr_err == cudaSuccess)
-      attr_err = set_pipeline_smem(reinterpret_cast<const void*>(lp_gemm_kernel));
   });
   if (attr_err != cudaSuccess) return LP_ERR_CUDA;
 
@@ -373,9 +349,6 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
   uint32_t* err = reinterpret_cast<uint32_t*>(ws);  // words 0..3, one per pipeline kernel
   float2* stats = reinterpret_cast<float2*>(ws + L.off_stats);
   auto* G = reinterpret_cast<__nv_bfloat16*>(ws + L.off_g);
-  auto* Gt = reinterpret_cast<__nv_bfloat16*>(ws + L.off_gt);
-  auto* Wt = reinterpret_cast<__nv_bfloat16*>(ws + L.off_wt);
-  auto* Ht = reinterpret_cast<__nv_bfloat16*>(ws + L.off_ht);
   float* dh_part = reinterpret_cast<float*>(ws + L.off_dh);
 
   // 1. forward statistics (log Z, entropy) of every row
@@ -403,40 +376,27 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
     g.g_ent = g_ent;
     g.stats = stats;
     g.G = G;
-    g.Gt = Gt;
     g.err = err + 1;
     g.ld_g = L.V8;
-    g.ld_gt = L.T8;
     g.inv_tau = inv_tau;
     g.T = static_cast<int>(T);
     lp_grad_kernel<<<pair_grid(dev.sm_count, total), kThreads, kSmemBytes, stream>>>(tmA, tmB, g);
     if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
   }
 
-  // 3. W^T and H^T
-  {
-    const dim3 gw(static_cast<unsigned>((V + 31) / 32), static_cast<unsigned>((d + 31) / 32));
-    lp_transpose_kernel<<<gw, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(W), V, d, ld_w,
-                                                Wt, L.V8);
-    const dim3 gh(static_cast<unsigned>((T + 31) / 32), static_cast<unsigned>((d + 31) / 32));
-    lp_transpose_kernel<<<gh, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(H), T, d, ld_h,
-                                                Ht, L.T8);
-    if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
-  }
-
-  // 4. dH = G W over 16 fixed vocabulary ranges, summed in order
+  // 3. dH = G W (W read N-major) over 16 fixed vocabulary ranges, summed in order
   int n_split = kSplitsDH;
-  st = launch_gemm(dev, G, T, L.V8, Wt, d, L.V8, V, kSplitsDH, dh_part, d, T * d, err + 2,
-                   stream, &n_split);
+  st = launch_gemm<false, true>(dev, G, T, L.V8, W, d, ld_w, V, kSplitsDH, dh_part, d, T * d,
+                                err + 2, stream, &n_split);
   if (st != LP_OK) return st;
   lp_split_sum_kernel<<<dev.sm_count * 4, 256, 0, stream>>>(dh_part, T * d, n_split, err,
                                                             grad_h);
   if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
 
-  // 5. dW = G^T H
+  // 4. dW = G^T H (G read M-major, H read N-major)
   if (grad_w != nullptr) {
-    st = launch_gemm(dev, Gt, V, L.T8, Ht, d, L.T8, T, 1, grad_w, d, 0, err + 3, stream,
-                     nullptr);
+    st = launch_gemm<true, true>(dev, G, V, L.V8, H, d, ld_h, T, 1, grad_w, d, 0, err + 3, stream,
+                                 nullptr);
     if (st != LP_OK) return st;
     lp_poison_kernel<<<dev.sm_count * 4, 256, 0, stream>>>(err, grad_w, V * d);
     if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;

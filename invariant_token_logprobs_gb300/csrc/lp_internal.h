@@ -81,6 +81,7 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
                                  void* workspace, cudaStream_t stream);
 
 int persistent_grid_limit();
+int fault_injection();
 void timing_events(cudaEvent_t* start, cudaEvent_t* stop);
 
 }  // namespace lp

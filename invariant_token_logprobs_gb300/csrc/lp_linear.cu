@@ -146,6 +146,7 @@ struct LinearArgs {
   float inv_tau;   // every logit is multiplied by it (1: no temperature)
   int T;
   int n_q;
+  int withhold_first_load;  // fault injection for tests of the bounded waits
 };
 
 // Add the 64 logits of a fully valid piece to the online state (whose maximum
@@ -263,7 +264,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // of this kernel starts them at zero too
   if (blockIdx.x == 0 && threadIdx.x == 0) a.err[1] = a.err[2] = a.err[3] = 0u;
   StateEpilogue epi{&a};
-  run_pair_pipeline(&tmA, &tmB, a.tiles, epi, a.err);
+  run_pair_pipeline(&tmA, &tmB, a.tiles, epi, a.err, a.withhold_first_load);
 }
 
 // Merge the tile states of each quarter and then either finalise the row from
@@ -382,6 +383,7 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
   a.inv_tau = inv_tau;
   a.T = static_cast<int>(T);
   a.n_q = n_q;
+  a.withhold_first_load = fault_injection();
 
   const int grid = pair_grid(dev.sm_count, total);
   cudaEvent_t ev_start, ev_stop;

@@ -62,10 +62,14 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
 static_assert(kBN == kTileN, "the vocabulary tile of the fused path is one MMA tile");
 
 // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B bf16
-// (bits 7-9 = 1, bits 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 in
-// bits 17-22, M >> 4 in bits 24-28; M = 256 for the CTA pair.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) |
-                            (uint32_t(kBN >> 3) << 17) | (uint32_t((2 * kBM) >> 4) << 24);
+// (bits 7-9 = 1, bits 10-12 = 1), A / B major-ness in bits 15 / 16 (0: K-major,
+// 1: M- or N-major), N >> 3 in bits 17-22, M >> 4 in bits 24-28; M = 256 for
+// the CTA pair.
+__host__ __device__ constexpr uint32_t idesc(bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) |
+         (uint32_t(kBN >> 3) << 17) | (uint32_t((2 * kBM) >> 4) << 24);
+}
+constexpr uint32_t kIdesc = idesc(false, false);
 
 // ---------------------------------------------------------------- PTX helpers
 
@@ -178,12 +182,12 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
 }
 
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                       uint32_t accumulate) {
+                                       uint32_t accumulate, uint32_t instr = kIdesc) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(instr), "r"(accumulate)
       : "memory");
 }
 
@@ -198,6 +202,24 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
   d |= static_cast<uint64_t>(16 >> 4) << 16;
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Shared-memory matrix descriptor of an M- or N-major bf16 tile of 128 (MN) x
+// 64 (K) written by TMA with 128-byte swizzle as two boxes of 64 (MN) x 64 (K):
+// in each box, K row r sits at r * 128 bytes (64 contiguous MN elements), so a
+// swizzle atom is 64 MN elements x 8 K rows (1024 bytes).  The leading-
+// dimension offset (bits 16-29) is the distance between atoms along MN (the
+// second box, 8192 bytes); the stride offset (bits 32-45) the distance between
+// 8-row groups along K (1024 bytes).  Each 16-element MMA step along K adds
+// 2048 bytes to the start address.
+__device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(8192 >> 4) << 16;
   d |= static_cast<uint64_t>(1024 >> 4) << 32;
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
@@ -246,10 +268,20 @@ __device__ __forceinline__ void tmem_load64(uint32_t taddr, float (&v)[64]) {
 //     work that no longer needs tensor memory (after the accumulator is freed).
 //
 // Called by every thread of a CTA of a 2-CTA cluster launched with kThreads
-// threads and kSmemBytes of dynamic shared memory.
-template <class Sched, class Epi>
+// threads and kSmemBytes of dynamic shared memory.  `withhold_first_load`
+// (tests of the bounded waits only): the leader CTA of pair 0 announces but
+// never issues its first TMA load, so that stage never fills and the waits
+// on it give up after their time bound.
+//
+// Operand layouts: K-major (kAMn / kBMn false) operands are [rows, K] with K
+// contiguous and their tensor maps have 64 x 128 boxes (encode_bf16_2d with
+// box_rows 128); M- or N-major operands (true) are [K, rows] with the rows
+// contiguous and their tensor maps have 64 x 64 boxes (box_rows 64), two per
+// stage.
+template <class Sched, class Epi, bool kAMn = false, bool kBMn = false>
 __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const CUtensorMap* tmB,
-                                                  const Sched& sch, Epi& epi, uint32_t* err) {
+                                                  const Sched& sch, Epi& epi, uint32_t* err,
+                                                  int withhold_first_load = 0) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -326,8 +358,22 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
             pending |= 1u << stage;
             pending_parity = (pending_parity & ~(1u << stage)) | (phase << stage);
           }
-          tma_load_2d(sa, tmA, kb * kBK, a_row, leader_full);
-          tma_load_2d(sa + kABytes, tmB, kb * kBK, b_row, leader_full);
+          const bool withheld = withhold_first_load != 0 && pair == 0 && rank == 0 &&
+                                u == pair && kb == kb0;
+          if (!withheld) {
+            if (kAMn) {
+              tma_load_2d(sa, tmA, a_row, kb * kBK, leader_full);
+              tma_load_2d(sa + kABytes / 2, tmA, a_row + 64, kb * kBK, leader_full);
+            } else {
+              tma_load_2d(sa, tmA, kb * kBK, a_row, leader_full);
+            }
+            if (kBMn) {
+              tma_load_2d(sa + kABytes, tmB, b_row, kb * kBK, leader_full);
+              tma_load_2d(sa + kABytes + kBBytes / 2, tmB, b_row + 64, kb * kBK, leader_full);
+            } else {
+              tma_load_2d(sa + kABytes, tmB, kb * kBK, b_row, leader_full);
+            }
+          }
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -367,8 +413,9 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
             const uint32_t sb = sa + kABytes;
 #pragma unroll
             for (int k = 0; k < kBK / kUmmaK; ++k) {
-              tc_mma(d_tmem, sw128_desc(sa + k * kUmmaK * 2), sw128_desc(sb + k * kUmmaK * 2),
-                     (kb != kb0 || k != 0) ? 1u : 0u);
+              const uint64_t ad = kAMn ? sw128_mn_desc(sa + k * 2048) : sw128_desc(sa + k * kUmmaK * 2);
+              const uint64_t bd = kBMn ? sw128_mn_desc(sb + k * 2048) : sw128_desc(sb + k * kUmmaK * 2);
+              tc_mma(d_tmem, ad, bd, (kb != kb0 || k != 0) ? 1u : 0u, idesc(kAMn, kBMn));
             }
             tc_commit_pair(empty_bar(stage));  // frees the stage in both CTAs
             if (++stage == kStages) {

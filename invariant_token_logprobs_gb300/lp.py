@@ -45,6 +45,7 @@ __all__ = [
     "lp_get_device_error",
     "lp_set_persistent_grid_limit",
     "lp_set_kernel_timing_events",
+    "lp_set_fault_injection",
     "lp_status_string",
     "lp_backend_id",
     "logprob_from_logits",
@@ -108,6 +109,7 @@ _SIGNATURES = {
     "lp_get_device_error": (_int, [_vp, _sz, ctypes.POINTER(ctypes.c_uint32), _vp]),
     "lp_set_persistent_grid_limit": (_int, [_int]),
     "lp_set_kernel_timing_events": (_int, [_vp, _vp]),
+    "lp_set_fault_injection": (_int, [_int]),
     "lp_status_string": (ctypes.c_char_p, [_int]),
     "lp_backend_id": (ctypes.c_char_p, []),
 }
@@ -334,6 +336,10 @@ def lp_set_kernel_timing_events(start_event=None, stop_event=None) -> None:
     a = None if start_event is None else start_event.cuda_event
     b = None if stop_event is None else stop_event.cuda_event
     _check("lp_set_kernel_timing_events", load().lp_set_kernel_timing_events(a, b))
+
+
+def lp_set_fault_injection(mode: int) -> None:
+    _check("lp_set_fault_injection", load().lp_set_fault_injection(mode))
 
 
 def lp_status_string(status: int) -> str:

@@ -22,7 +22,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = lp.declared_symbols()
-    assert len(names) == 20
+    assert len(names) == 21
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(lp._SIGNATURES)
@@ -156,3 +156,5 @@ def test_valid_call_without_gb300_fails_loudly(lib):
     assert lib.lp_merge_partials(arr, 1, 8, A, A, None) == UNSUPPORTED
     assert lib.lp_set_persistent_grid_limit(-1) == INVALID
     assert lib.lp_set_persistent_grid_limit(0) == OK
+    assert lib.lp_set_fault_injection(2) == INVALID
+    assert lib.lp_set_fault_injection(0) == OK
