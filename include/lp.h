@@ -299,10 +299,25 @@ LP_API lp_status lp_linear_logprob_partials_temperature(
 LP_API size_t lp_linear_logprob_backward_workspace_size(int64_t T, int64_t d, int64_t V);
 
 /*
+ * lp_linear_logprob_lse: lp_linear_logprob_temperature that also writes, per
+ * row, lse_out[t] = log sum_v exp(z[t, v] / tau) (float32 [T]).  Keep lse_out
+ * and entropy_out from the forward pass and hand them to the backward to skip
+ * its forward recomputation.  All three outputs are required.
+ */
+LP_API lp_status lp_linear_logprob_lse(const void* H, int64_t ld_h, const void* W, int64_t ld_w,
+                                       const int64_t* targets, int64_t T, int64_t d, int64_t V,
+                                       float temperature, float* logp_out, float* entropy_out,
+                                       float* lse_out, void* workspace, size_t workspace_bytes,
+                                       void* stream);
+
+/*
  * lp_linear_logprob_backward:
  *   H, ld_h, W, ld_w, targets, T, d, V, temperature: as in
  *               lp_linear_logprob_temperature (temperature 1: no scaling);
  *               T <= 2^24.
+ *   saved_lse, saved_entropy  [T] float32 from lp_linear_logprob_lse on the
+ *               same inputs and temperature, or both NULL (the backward then
+ *               recomputes them; the results are the same bits either way).
  *   grad_logp   [T] float32 upstream gradient of logp, or NULL (zero).
  *   grad_entropy [T] float32 upstream gradient of entropy, or NULL (zero);
  *               at least one of the two must be given.
@@ -317,6 +332,7 @@ LP_API size_t lp_linear_logprob_backward_workspace_size(int64_t T, int64_t d, in
 LP_API lp_status lp_linear_logprob_backward(const void* H, int64_t ld_h, const void* W,
                                             int64_t ld_w, const int64_t* targets, int64_t T,
                                             int64_t d, int64_t V, float temperature,
+                                            const float* saved_lse, const float* saved_entropy,
                                             const float* grad_logp, const float* grad_entropy,
                                             float* grad_H, float* grad_W, void* workspace,
                                             size_t workspace_bytes, void* stream);

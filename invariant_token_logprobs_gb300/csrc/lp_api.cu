@@ -272,6 +272,29 @@ lp_status lp_linear_logprob_noalloc(const void* H, int64_t ld_h, const void* W, 
                            entropy_out, nullptr, scratch, static_cast<cudaStream_t>(stream));
 }
 
+lp_status lp_linear_logprob_lse(const void* H, int64_t ld_h, const void* W, int64_t ld_w,
+                                const int64_t* targets, int64_t T, int64_t d, int64_t V,
+                                float temperature, float* logp_out, float* entropy_out,
+                                float* lse_out, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  float inv_tau;
+  if (!lp::inverse_temperature(temperature, &inv_tau)) return LP_ERR_INVALID_ARGUMENT;
+  lp_status st = lp::check_fused_args(H, ld_h, W, ld_w, targets, T, d, V);
+  if (st != LP_OK || T == 0) return st;
+  if (logp_out == nullptr || entropy_out == nullptr || lse_out == nullptr || workspace == nullptr)
+    return LP_ERR_INVALID_ARGUMENT;
+  if (!lp::aligned(logp_out, 4) || !lp::aligned(entropy_out, 4) || !lp::aligned(lse_out, 4) ||
+      !lp::aligned(workspace, 256))
+    return LP_ERR_MISALIGNED;
+  if (workspace_bytes < lp::linear_workspace_bytes(T, V, 4)) return LP_ERR_WORKSPACE_TOO_SMALL;
+  lp::Device dev;
+  st = lp::current_device(&dev);
+  if (st != LP_OK) return st;
+  return lp::launch_linear_stats(dev, H, ld_h, W, ld_w, targets, T, d, V, 0, 4, inv_tau, logp_out,
+                                 entropy_out, nullptr, lse_out, workspace,
+                                 static_cast<cudaStream_t>(stream));
+}
+
 lp_status lp_linear_logprob_partials_temperature(const void* H, int64_t ld_h,
                                                  const void* W_shard, int64_t ld_w,
                                                  const int64_t* targets, int64_t T, int64_t d,
@@ -340,7 +363,8 @@ size_t lp_linear_logprob_backward_workspace_size(int64_t T, int64_t d, int64_t V
 
 lp_status lp_linear_logprob_backward(const void* H, int64_t ld_h, const void* W, int64_t ld_w,
                                      const int64_t* targets, int64_t T, int64_t d, int64_t V,
-                                     float temperature, const float* grad_logp,
+                                     float temperature, const float* saved_lse,
+                                     const float* saved_entropy, const float* grad_logp,
                                      const float* grad_entropy, float* grad_H, float* grad_W,
                                      void* workspace, size_t workspace_bytes, void* stream) {
   float inv_tau;
@@ -349,6 +373,8 @@ lp_status lp_linear_logprob_backward(const void* H, int64_t ld_h, const void* W,
   if (st != LP_OK || T == 0) return st;
   if (grad_H == nullptr || workspace == nullptr) return LP_ERR_INVALID_ARGUMENT;
   if (grad_logp == nullptr && grad_entropy == nullptr) return LP_ERR_INVALID_ARGUMENT;
+  if ((saved_lse == nullptr) != (saved_entropy == nullptr)) return LP_ERR_INVALID_ARGUMENT;
+  if (!lp::aligned(saved_lse, 4) || !lp::aligned(saved_entropy, 4)) return LP_ERR_MISALIGNED;
   if (T > (int64_t(1) << 24)) return LP_ERR_INVALID_ARGUMENT;
   if (!lp::aligned(grad_logp, 4) || !lp::aligned(grad_entropy, 4) || !lp::aligned(grad_H, 16) ||
       !lp::aligned(grad_W, 16) || !lp::aligned(workspace, 256))
@@ -358,9 +384,9 @@ lp_status lp_linear_logprob_backward(const void* H, int64_t ld_h, const void* W,
   lp::Device dev;
   st = lp::current_device(&dev);
   if (st != LP_OK) return st;
-  return lp::launch_linear_backward(dev, H, ld_h, W, ld_w, targets, T, d, V, inv_tau, grad_logp,
-                                    grad_entropy, grad_H, grad_W, workspace,
-                                    static_cast<cudaStream_t>(stream));
+  return lp::launch_linear_backward(dev, H, ld_h, W, ld_w, targets, T, d, V, inv_tau, saved_lse,
+                                    saved_entropy, grad_logp, grad_entropy, grad_H, grad_W,
+                                    workspace, static_cast<cudaStream_t>(stream));
 }
 
 lp_status lp_get_device_error(const void* workspace, size_t workspace_bytes, uint32_t* word_out,

@@ -12,7 +12,8 @@
 // train/grad_norm).
 //
 // Steps, all on the tensor-core pair pipeline of lp_tcgen05.cuh:
-//   1. forward kernels again, keeping per row log Z and entropy;
+//   1. unless the caller passes the forward's log Z and entropy per row, the
+//      forward kernels again, keeping them;
 //   2. lp_grad_kernel: z tiles recomputed in tensor memory; the epilogue forms
 //      G in fp32 and stores it in bf16 as G [T, V];
 //   3. lp_gemm_kernel<K-major A, N-major B>: dH = G W, reading W [V, d] as an
@@ -74,7 +75,8 @@ struct GradArgs {
   const int64_t* targets;
   const float* g_logp;    // [T] or NULL
   const float* g_ent;     // [T] or NULL
-  const float2* stats;    // [T] (log Z, entropy)
+  const float* lse;       // [T] log Z of the scaled logits
+  const float* ent;       // [T] entropy
   __nv_bfloat16* G;       // [T][ld_g]
   uint32_t* err;
   int64_t ld_g;
@@ -103,9 +105,8 @@ struct GradEpilogue {
       const bool y_ok = y >= 0 && y < a->tiles.V;
       gl = (a->g_logp != nullptr && y_ok) ? a->g_logp[row] : 0.f;
       ge = a->g_ent != nullptr ? a->g_ent[row] : 0.f;
-      const float2 s = a->stats[row];
-      log_z = s.x;
-      ent = s.y;
+      log_z = a->lse[row];
+      ent = a->ent[row];
       const int64_t yl64 = y - c0;
       if (y_ok && yl64 >= 0 && yl64 < valid) yl = static_cast<int>(yl64);
     }
@@ -166,15 +167,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // C[M, N] (fp32, row stride ldc) = A[M, K] B[N, K]^T for the K blocks of split
 // s; split s writes C + s * split_stride.  Units: (row block, column block,
-// split), row block fastest.
+// split), with the row block or the column block fastest (the operand that is
+// shared by consecutive units stays in L2).
 struct GemmTiles {
   int n_mb, n_nb, n_split, n_kb, kb_per_split, total;
+  int nb_fastest;
   __device__ __forceinline__ int units() const { return total; }
   __device__ __forceinline__ void decode(int u, int& mb, int& nb, int& s) const {
-    mb = u % n_mb;
-    const int g = u / n_mb;
-    nb = g % n_nb;
-    s = g / n_nb;
+    if (nb_fastest) {
+      nb = u % n_nb;
+      const int g = u / n_nb;
+      mb = g % n_mb;
+      s = g / n_mb;
+    } else {
+      mb = u % n_mb;
+      const int g = u / n_mb;
+      nb = g % n_nb;
+      s = g / n_nb;
+    }
   }
   __device__ __forceinline__ void coords(int u, uint32_t rank, int& a_row, int& b_row, int& kb0,
                                          int& kb1) const {
@@ -266,7 +276,7 @@ __global__ void lp_poison_kernel(const uint32_t* __restrict__ err, float* __rest
 
 struct BackwardLayout {
   int64_t V8;
-  size_t off_stats, off_logp, off_ent, off_g, off_dh, total;
+  size_t off_lse, off_logp, off_ent, off_g, off_dh, total;
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -275,7 +285,7 @@ BackwardLayout backward_layout(int64_t T, int64_t d, int64_t V) {
   BackwardLayout L;
   L.V8 = round8(V);
   size_t o = align256(linear_workspace_bytes(T, V, 4));
-  L.off_stats = o; o = align256(o + sizeof(float2) * T);
+  L.off_lse = o; o = align256(o + sizeof(float) * T);
   L.off_logp = o; o = align256(o + sizeof(float) * T);
   L.off_ent = o; o = align256(o + sizeof(float) * T);
   L.off_g = o; o = align256(o + 2 * static_cast<size_t>(T) * L.V8);
@@ -290,7 +300,7 @@ template <bool kAMn, bool kBMn>
 lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a, const void* B,
                       int64_t N, int64_t ld_b, int64_t K, int n_split, float* C, int64_t ldc,
                       int64_t split_stride, uint32_t* err, cudaStream_t stream,
-                      int* n_split_out) {
+                      int* n_split_out, bool nb_fastest) {
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
@@ -311,6 +321,7 @@ lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a,
   // every split gets at least one K block (the count depends on K alone)
   n_split = (g.tiles.n_kb + g.tiles.kb_per_split - 1) / g.tiles.kb_per_split;
   g.tiles.n_split = n_split;
+  g.tiles.nb_fastest = nb_fastest ? 1 : 0;
   if (n_split_out != nullptr) *n_split_out = n_split;
   const int64_t total = int64_t(g.tiles.n_mb) * g.tiles.n_nb * n_split;
   if (total >= (int64_t(1) << 31)) return LP_ERR_INVALID_ARGUMENT;
@@ -334,7 +345,8 @@ size_t linear_backward_workspace_bytes(int64_t T, int64_t d, int64_t V) {
 
 lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h, const void* W,
                                  int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
-                                 int64_t V, float inv_tau, const float* g_logp,
+                                 int64_t V, float inv_tau, const float* saved_lse,
+                                 const float* saved_entropy, const float* g_logp,
                                  const float* g_ent, float* grad_h, float* grad_w,
                                  void* workspace, cudaStream_t stream) {
   static std::once_flag attr_once;
@@ -347,18 +359,29 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
   const BackwardLayout L = backward_layout(T, d, V);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* err = reinterpret_cast<uint32_t*>(ws);  // words 0..3, one per pipeline kernel
-  float2* stats = reinterpret_cast<float2*>(ws + L.off_stats);
+  const float* lse = saved_lse;
+  const float* ent = saved_entropy;
   auto* G = reinterpret_cast<__nv_bfloat16*>(ws + L.off_g);
   float* dh_part = reinterpret_cast<float*>(ws + L.off_dh);
 
-  // 1. forward statistics (log Z, entropy) of every row
-  lp_status st = launch_linear_stats(dev, H, ld_h, W, ld_w, targets, T, d, V, 0, 4, inv_tau,
-                                     reinterpret_cast<float*>(ws + L.off_logp),
-                                     reinterpret_cast<float*>(ws + L.off_ent), nullptr, stats,
-                                     workspace, stream);
-  if (st != LP_OK) return st;
+  // 1. forward statistics (log Z, entropy) of every row, unless given
+  if (lse == nullptr || ent == nullptr) {
+    float* lse_ws = reinterpret_cast<float*>(ws + L.off_lse);
+    float* ent_ws = reinterpret_cast<float*>(ws + L.off_ent);
+    lp_status st0 = launch_linear_stats(dev, H, ld_h, W, ld_w, targets, T, d, V, 0, 4, inv_tau,
+                                        reinterpret_cast<float*>(ws + L.off_logp), ent_ws,
+                                        nullptr, lse_ws, workspace, stream);
+    if (st0 != LP_OK) return st0;
+    lse = lse_ws;
+    ent = ent_ws;
+  } else {
+    // the error words of this call start at zero (the forward kernel would
+    // have cleared them)
+    if (cudaMemsetAsync(err, 0, 4 * sizeof(uint32_t), stream) != cudaSuccess) return LP_ERR_CUDA;
+  }
+  lp_status st = LP_OK;
 
-  // 2. G and G^T
+  // 2. G
   {
     CUtensorMap tmA, tmB;
     if (!encode_bf16_2d(&tmA, H, T, d, ld_h, kBM)) return LP_ERR_CUDA;
@@ -374,7 +397,8 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
     g.targets = targets;
     g.g_logp = g_logp;
     g.g_ent = g_ent;
-    g.stats = stats;
+    g.lse = lse;
+    g.ent = ent;
     g.G = G;
     g.err = err + 1;
     g.ld_g = L.V8;
@@ -386,8 +410,9 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
 
   // 3. dH = G W (W read N-major) over 16 fixed vocabulary ranges, summed in order
   int n_split = kSplitsDH;
+  // row blocks fastest: the pairs of one W range run together
   st = launch_gemm<false, true>(dev, G, T, L.V8, W, d, ld_w, V, kSplitsDH, dh_part, d, T * d,
-                                err + 2, stream, &n_split);
+                                err + 2, stream, &n_split, false);
   if (st != LP_OK) return st;
   lp_split_sum_kernel<<<dev.sm_count * 4, 256, 0, stream>>>(dh_part, T * d, n_split, err,
                                                             grad_h);
@@ -395,8 +420,9 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
 
   // 4. dW = G^T H (G read M-major, H read N-major)
   if (grad_w != nullptr) {
+    // column blocks fastest: a block of G is used by 16 consecutive units
     st = launch_gemm<true, true>(dev, G, V, L.V8, H, d, ld_h, T, 1, grad_w, d, 0, err + 3, stream,
-                                 nullptr);
+                                 nullptr, true);
     if (st != LP_OK) return st;
     lp_poison_kernel<<<dev.sm_count * 4, 256, 0, stream>>>(err, grad_w, V * d);
     if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;

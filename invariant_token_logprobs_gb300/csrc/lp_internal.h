@@ -64,19 +64,20 @@ lp_status launch_linear(const Device& dev, const void* H, int64_t ld_h, const vo
 size_t static_scratch_bytes();
 lp_status static_scratch(int ordinal, void** out);
 
-// As launch_linear, and when `stats` is not NULL also writes per row the
-// float2 (log Z, entropy) of the (tempered) logits.
+// As launch_linear, and when `lse` is not NULL also writes per row the
+// log-sum-exp log Z of the (tempered) logits.
 lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, const void* W,
                               int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
                               int64_t V_total, int q_first, int n_q, float inv_tau, float* logp,
-                              float* entropy, float* partials_out, void* stats,
+                              float* entropy, float* partials_out, float* lse,
                               void* workspace, cudaStream_t stream);
 
 // backward of the fused path
 size_t linear_backward_workspace_bytes(int64_t T, int64_t d, int64_t V);
 lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h, const void* W,
                                  int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
-                                 int64_t V, float inv_tau, const float* g_logp,
+                                 int64_t V, float inv_tau, const float* saved_lse,
+                                 const float* saved_entropy, const float* g_logp,
                                  const float* g_ent, float* grad_h, float* grad_w,
                                  void* workspace, cudaStream_t stream);
 

@@ -272,13 +272,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // row, one warp per quarter: the quarter's maximum is exact (order-free); lane
 // l rebases tiles l, l+32, l+64, ... to it and sums them, and the 32 lane sums
 // are combined by a fixed shuffle tree.  The result depends only on the
-// quarter's tile states.  When `stats` is given, the row's log-partition
-// log Z = M + log S and entropy are also written there (for the backward).
+// quarter's tile states.  When `lse` is given, the row's log-partition
+// log Z = M + log S (of the scaled logits) is also written there.
 __global__ void __launch_bounds__(128)
     lp_tile_merge_kernel(const float4* __restrict__ chunks, const int64_t* __restrict__ targets,
                          const uint32_t* __restrict__ err, int n_q, int n_tiles_q, int64_t V,
                          float* __restrict__ logp, float* __restrict__ entropy,
-                         float4* __restrict__ partials_out, float2* __restrict__ stats) {
+                         float4* __restrict__ partials_out, float* __restrict__ lse) {
   __shared__ float4 qs[kQuarters];
   const int ql = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(128)
     finalise(q4, lp, ent);
     logp[row] = lp;
     if (entropy != nullptr) entropy[row] = ent;
-    if (stats != nullptr) {
+    if (lse != nullptr) {
       // log Z from the same quarter states: M + log S, in float64
       const float M = fmaxf(fmaxf(q4[0].x, q4[1].x), fmaxf(q4[2].x, q4[3].x));
       double S = 0.0;
@@ -334,7 +334,8 @@ __global__ void __launch_bounds__(128)
           S = __dadd_rn(S, __dmul_rn(exp(__dsub_rn(static_cast<double>(q4[i].x),
                                                    static_cast<double>(M))),
                                      static_cast<double>(q4[i].y)));
-      stats[row] = make_float2(__double2float_rn(__dadd_rn(static_cast<double>(M), log(S))), ent);
+      lse[row] = (*err != 0u) ? quiet_nan()
+                              : __double2float_rn(__dadd_rn(static_cast<double>(M), log(S)));
     }
   }
 }
@@ -350,7 +351,7 @@ size_t linear_workspace_bytes(int64_t T, int64_t V_total, int n_q) {
 lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, const void* W,
                               int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
                               int64_t V_total, int q_first, int n_q, float inv_tau, float* logp,
-                              float* entropy, float* partials_out, void* stats,
+                              float* entropy, float* partials_out, float* lse,
                               void* workspace, cudaStream_t stream) {
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
@@ -394,7 +395,7 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
   if (ev_stop != nullptr && cudaEventRecord(ev_stop, stream) != cudaSuccess) return LP_ERR_CUDA;
   lp_tile_merge_kernel<<<static_cast<unsigned>(T), 128, 0, stream>>>(
       a.chunks, targets, a.err, n_q, a.tiles.n_tiles_q, V_total, logp, entropy,
-      reinterpret_cast<float4*>(partials_out), static_cast<float2*>(stats));
+      reinterpret_cast<float4*>(partials_out), lse);
   return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }
 

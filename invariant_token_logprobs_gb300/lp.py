@@ -40,7 +40,9 @@ __all__ = [
     "lp_linear_logprob_temperature",
     "lp_linear_logprob_partials_temperature",
     "lp_linear_logprob_backward_workspace_size",
+    "lp_linear_logprob_lse",
     "lp_linear_logprob_backward",
+    "linear_logprob_lse",
     "linear_logprob_backward",
     "lp_get_device_error",
     "lp_set_persistent_grid_limit",
@@ -103,9 +105,12 @@ _SIGNATURES = {
         _int, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _int, _int, ctypes.c_float, _vp, _vp,
                _sz, _vp]),
     "lp_linear_logprob_backward_workspace_size": (_sz, [_i64, _i64, _i64]),
+    "lp_linear_logprob_lse": (
+        _int, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, ctypes.c_float, _vp, _vp, _vp, _vp,
+               _sz, _vp]),
     "lp_linear_logprob_backward": (
         _int, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, ctypes.c_float, _vp, _vp, _vp, _vp,
-               _vp, _sz, _vp]),
+               _vp, _vp, _vp, _sz, _vp]),
     "lp_get_device_error": (_int, [_vp, _sz, ctypes.POINTER(ctypes.c_uint32), _vp]),
     "lp_set_persistent_grid_limit": (_int, [_int]),
     "lp_set_kernel_timing_events": (_int, [_vp, _vp]),
@@ -292,19 +297,43 @@ def lp_linear_logprob_backward_workspace_size(T: int, d: int, V: int) -> int:
     return int(load().lp_linear_logprob_backward_workspace_size(T, d, V))
 
 
-def lp_linear_logprob_backward(H, W, targets, temperature, grad_logp, grad_entropy, grad_H,
-                               grad_W, workspace, stream=None) -> None:
+def lp_linear_logprob_lse(H, W, targets, temperature, logp, entropy, lse, workspace,
+                          stream=None) -> None:
+    _check_bf16(H, W, targets)
+    T, d = H.shape
+    V = W.shape[0]
+    _check("lp_linear_logprob_lse", load().lp_linear_logprob_lse(
+        _ptr(H), _row_stride(H), _ptr(W), _row_stride(W), _ptr(targets), T, d, V,
+        float(temperature), _ptr(logp), _ptr(entropy), _ptr(lse), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def lp_linear_logprob_backward(H, W, targets, temperature, saved_lse, saved_entropy, grad_logp,
+                               grad_entropy, grad_H, grad_W, workspace, stream=None) -> None:
     _check_bf16(H, W, targets)
     T, d = H.shape
     V = W.shape[0]
     _check("lp_linear_logprob_backward", load().lp_linear_logprob_backward(
         _ptr(H), _row_stride(H), _ptr(W), _row_stride(W), _ptr(targets), T, d, V,
-        float(temperature), _ptr(grad_logp), _ptr(grad_entropy), _ptr(grad_H), _ptr(grad_W),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+        float(temperature), _ptr(saved_lse), _ptr(saved_entropy), _ptr(grad_logp),
+        _ptr(grad_entropy), _ptr(grad_H), _ptr(grad_W), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def linear_logprob_lse(H, W, y, temperature: float = 1.0, workspace=None, stream=None):
+    """(logp, entropy, lse) [T] fp32 of the fused path; keep entropy and lse for the backward."""
+    T, d = H.shape
+    V = W.shape[0]
+    if workspace is None:
+        workspace = _workspace(lp_linear_logprob_workspace_size(T, d, V), H.device)
+    out = [torch.empty(T, dtype=torch.float32, device=H.device) for _ in range(3)]
+    lp_linear_logprob_lse(H, W, y, temperature, out[0], out[1], out[2], workspace, stream)
+    return tuple(out)
 
 
 def linear_logprob_backward(H, W, y, grad_logp=None, grad_entropy=None, temperature: float = 1.0,
-                            with_grad_W: bool = True, workspace=None, stream=None):
+                            with_grad_W: bool = True, saved_lse=None, saved_entropy=None,
+                            workspace=None, stream=None):
     """(grad_H [T, d] fp32, grad_W [V, d] fp32 or None) of the fused path."""
     T, d = H.shape
     V = W.shape[0]
@@ -312,8 +341,8 @@ def linear_logprob_backward(H, W, y, grad_logp=None, grad_entropy=None, temperat
         workspace = _workspace(lp_linear_logprob_backward_workspace_size(T, d, V), H.device)
     gH = torch.empty((T, d), dtype=torch.float32, device=H.device)
     gW = torch.empty((V, d), dtype=torch.float32, device=H.device) if with_grad_W else None
-    lp_linear_logprob_backward(H, W, y, temperature, grad_logp, grad_entropy, gH, gW, workspace,
-                               stream)
+    lp_linear_logprob_backward(H, W, y, temperature, saved_lse, saved_entropy, grad_logp,
+                               grad_entropy, gH, gW, workspace, stream)
     return gH, gW
 
 

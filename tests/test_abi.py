@@ -22,7 +22,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = lp.declared_symbols()
-    assert len(names) == 21
+    assert len(names) == 22
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(lp._SIGNATURES)
@@ -119,7 +119,8 @@ def test_backward_argument_errors(lib):
     f = lib.lp_linear_logprob_backward
     ws = lp.lp_linear_logprob_backward_workspace_size(64, 256, 8192)
     assert ws > lp.lp_linear_logprob_workspace_size(64, 256, 8192)
-    base = [A, 256, A, 256, A, 64, 256, 8192, 1.0, A, A, A, A, A, ws, None]
+    #       H  ldh  W  ldw y  T   d    V     tau  lse ent gl ge gH gW ws  wsb stream
+    base = [A, 256, A, 256, A, 64, 256, 8192, 1.0, A, A, A, A, A, A, A, ws, None]
 
     def call(i, v):
         a = list(base)
@@ -128,11 +129,12 @@ def test_backward_argument_errors(lib):
 
     assert f(*base[:5], 0, *base[6:]) == OK          # T == 0
     assert call(8, 0.0) == INVALID                    # temperature
-    assert call(11, None) == INVALID                  # grad_H
-    a = list(base); a[9] = None; a[10] = None
+    assert call(13, None) == INVALID                  # grad_H
+    assert call(9, None) == INVALID                   # lse without entropy
+    a = list(base); a[11] = None; a[12] = None
     assert f(*a) == INVALID                           # no upstream gradient
-    assert call(11, A + 4) == MISALIGNED              # grad_H 16-byte aligned
-    assert call(14, ws - 1) == WS_SMALL
+    assert call(13, A + 4) == MISALIGNED              # grad_H 16-byte aligned
+    assert call(16, ws - 1) == WS_SMALL
     assert lp.lp_linear_logprob_backward_workspace_size(-1, 8, 8) == 0
 
 

@@ -16,7 +16,6 @@ import torch
 from invariant_token_logprobs_gb300 import lp, synth
 from _gpu_helpers import bits
 
-import oracle
 from oracle import logprob as olp
 
 pytestmark = pytest.mark.gpu
@@ -101,6 +100,25 @@ def test_backward_qwen3_8b_head_sampled():
     torch.cuda.synchronize()
     out = _check_against_oracle(x, gl, ge, 1.0, gH, gW, rows=[0, 255, 256, 511])
     print(f"qwen3-8b head backward: {out}")
+
+
+def test_backward_with_saved_forward_statistics():
+    """Entropy and log-sum-exp kept from the forward give the same bits as the
+    backward's own recomputation."""
+    x = synth.fused_inputs("fused_tiny", device=DEV, T=200, d=256, V=30000, seed=14)
+    gl, ge = _upstream(200, seed=3)
+    for tau in (1.0, 0.7):
+        logp, ent, lse = lp.linear_logprob_lse(x.H, x.W, x.y, temperature=tau)
+        ref_lp, ref_ent = lp.linear_logprob(x.H, x.W, x.y, temperature=tau)
+        assert torch.equal(bits(logp), bits(ref_lp)) and torch.equal(bits(ent), bits(ref_ent))
+        z = olp.linear_logits(x.H.float().cpu().numpy(), x.W.float().cpu().numpy()) / tau
+        lse_ref = olp.logsumexp_rows(z)
+        assert float(np.max(np.abs(lse.double().cpu().numpy() - lse_ref))) <= 1e-4
+        a = lp.linear_logprob_backward(x.H, x.W, x.y, gl, ge, temperature=tau)
+        b = lp.linear_logprob_backward(x.H, x.W, x.y, gl, ge, temperature=tau, saved_lse=lse,
+                                       saved_entropy=ent)
+        assert torch.equal(bits(a[0].reshape(-1)), bits(b[0].reshape(-1)))
+        assert torch.equal(bits(a[1].reshape(-1)), bits(b[1].reshape(-1)))
 
 
 def test_backward_deterministic_and_row_invariant():
