@@ -316,11 +316,13 @@ def run_lp(args):
     barrier()
     torch.cuda.synchronize()
     t_begin = time.time()
+    torch.cuda.nvtx.range_push("lp.bench.fused_timed")
     ev0.record(stream)
     for i in range(K):
         lp.lp_set_kernel_timing_events(k_start[i], k_stop[i])
         lp.lp_linear_logprob(x.H, x.W, x.y, logp, ent, ws)
     ev1.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     t_end = time.time()
     barrier()

@@ -207,37 +207,59 @@ struct GemmArgs {
   uint32_t* err;
 };
 
+// Epilogue of the products: each warp stages its 32 rows x 64 columns of a
+// piece in shared memory (16-byte chunks placed at chunk ^ (row % 16), so the
+// writes by row and the reads by column are free of bank conflicts) and then
+// stores them two rows per instruction, 256 contiguous bytes per row.
+constexpr int kStageFloatsPerWarp = 32 * 64;
+constexpr int kGemmStagingBytes = 4 * kStageFloatsPerWarp * 4;  // 4 epilogue warps, 32 KB
+// dynamic shared memory of the product kernels: alignment slack, the
+// pipeline, then the staging area
+constexpr int kGemmSmemBytes = 1024 + kPipelineSmemEnd + kGemmStagingBytes;
+static_assert(kGemmSmemBytes <= 232448, "fits the 227 KB per-CTA limit");
+
 struct GemmEpilogue {
   const GemmArgs* a;
   __device__ __forceinline__ void consume(int u, uint32_t taddr, uint32_t rank, int lane_grp,
                                           int lane) {
     int mb, nb, s;
     a->tiles.decode(u, mb, nb, s);
-    const int64_t row = static_cast<int64_t>(mb) * (2 * kBM) + rank * kBM + lane_grp * 32 + lane;
+    const int64_t row0 = static_cast<int64_t>(mb) * (2 * kBM) + rank * kBM + lane_grp * 32;
     const int64_t n0 = static_cast<int64_t>(nb) * kBN;
-    float* crow = a->C + s * a->split_stride + row * a->ldc + n0;
-    const bool row_ok = row < a->M;
-    const bool vec = ((reinterpret_cast<uintptr_t>(crow) & 15u) == 0);
+    float* cbase = a->C + s * a->split_stride;
+    float* stg = reinterpret_cast<float*>(pipeline_smem_base() + kPipelineSmemEnd) +
+                 lane_grp * kStageFloatsPerWarp;
+    const int c = lane & 15;     // 16-byte chunk this lane stores
+    const int half = lane >> 4;  // which of the two rows of an instruction
 #pragma unroll 1
     for (int p = 0; p < kBN / 64; ++p) {
       float v[64];
       __syncwarp();
       tmem_load64(taddr + static_cast<uint32_t>(p * 64), v);
-      if (!row_ok) continue;
-      const int64_t n_left = a->N - (n0 + p * 64);
-      if (n_left <= 0) continue;
-      float* dst = crow + p * 64;
-      if (n_left >= 64 && vec) {
 #pragma unroll
-        for (int i = 0; i < 64; i += 4)
-          *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-      } else {
-        const int n = n_left < 64 ? static_cast<int>(n_left) : 64;
+      for (int k = 0; k < 16; ++k)
+        *reinterpret_cast<float4*>(stg + lane * 64 + ((k ^ (lane & 15)) * 4)) =
+            make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+      __syncwarp();
+      const int64_t col = n0 + p * 64 + c * 4;
+#pragma unroll 4
+      for (int i = 0; i < 16; ++i) {
+        const int r = 2 * i + half;
+        const float4 x = *reinterpret_cast<const float4*>(stg + r * 64 + ((c ^ (r & 15)) * 4));
+        const int64_t grow = row0 + r;
+        if (grow >= a->M || col >= a->N) continue;
+        float* dst = cbase + grow * a->ldc + col;
+        if (col + 3 < a->N && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+          *reinterpret_cast<float4*>(dst) = x;
+        } else {
+          const float xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
-          if (i < n) dst[i] = v[i];
+          for (int e = 0; e < 4; ++e)
+            if (col + e < a->N) dst[e] = xs[e];
+        }
       }
     }
+    __syncwarp();
   }
   __device__ __forceinline__ void after_release(int, uint32_t, int, int) {}
 };
@@ -304,7 +326,8 @@ lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a,
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = set_pipeline_smem(reinterpret_cast<const void*>(lp_gemm_kernel<kAMn, kBMn>));
+    attr_err = set_pipeline_smem(reinterpret_cast<const void*>(lp_gemm_kernel<kAMn, kBMn>),
+                                 kGemmSmemBytes - kSmemBytes);
   });
   if (attr_err != cudaSuccess) return LP_ERR_CUDA;
   CUtensorMap tmA, tmB;
@@ -333,7 +356,7 @@ lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a,
   g.N = N;
   g.err = err;
   lp_gemm_kernel<kAMn, kBMn>
-      <<<pair_grid(dev.sm_count, total), kThreads, kSmemBytes, stream>>>(tmA, tmB, g);
+      <<<pair_grid(dev.sm_count, total), kThreads, kGemmSmemBytes, stream>>>(tmA, tmB, g);
   return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }
 

@@ -88,8 +88,9 @@ int pair_grid(int sm_count, int64_t units) {
   return 2 * pairs;
 }
 
-cudaError_t set_pipeline_smem(const void* kernel) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+cudaError_t set_pipeline_smem(const void* kernel, int extra) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmemBytes + extra);
 }
 
 }  // namespace tc

@@ -58,8 +58,12 @@ constexpr uint32_t kTmemCols = 2 * kBN;
 constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;
 constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kNumBars * 8 + 16;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
+// Bytes past the 1024-aligned dynamic shared-memory base the pipeline uses
+// (ring, barriers, tensor-memory slot); an epilogue may use what follows.
+constexpr int kPipelineSmemEnd = kStages * kStageBytes + 1024;
 
 static_assert(kBN == kTileN, "the vocabulary tile of the fused path is one MMA tile");
+static_assert(kNumBars * 8 + 16 <= 1024, "barriers fit below kPipelineSmemEnd");
 
 // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B bf16
 // (bits 7-9 = 1, bits 10-12 = 1), A / B major-ness in bits 15 / 16 (0: K-major,
@@ -253,6 +257,13 @@ __device__ __forceinline__ void tmem_load64(uint32_t taddr, float (&v)[64]) {
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 1024-aligned base of the dynamic shared memory (the pipeline's ring).
+__device__ __forceinline__ uint8_t* pipeline_smem_base() {
+  extern __shared__ uint8_t smem_raw[];
+  return reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+
 // ------------------------------------------------------------------ pipeline
 //
 // Sched (work list, the same on every CTA):
@@ -282,9 +293,7 @@ template <class Sched, class Epi, bool kAMn = false, bool kBMn = false>
 __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const CUtensorMap* tmB,
                                                   const Sched& sch, Epi& epi, uint32_t* err,
                                                   int withhold_first_load = 0) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = pipeline_smem_base();
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -479,8 +488,9 @@ bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t co
 // process-wide CTA limit: one CTA pair per two SMs, never more pairs than units.
 int pair_grid(int sm_count, int64_t units);
 
-// Give `kernel` the dynamic shared memory of the pipeline (once per kernel).
-cudaError_t set_pipeline_smem(const void* kernel);
+// Give `kernel` the dynamic shared memory of the pipeline plus `extra` bytes
+// for its epilogue (once per kernel).
+cudaError_t set_pipeline_smem(const void* kernel, int extra = 0);
 
 }  // namespace tc
 }  // namespace lp
