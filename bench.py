@@ -43,7 +43,9 @@ WORKLOAD = "fused_qwen3_8b"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "lp_linear_kernel.fused_qwen3_8b.txt")
-LINEAR_SOURCE = os.path.join(ROOT, "invariant_token_logprobs_gb300", "csrc", "lp_linear.cu")
+# the sources that define the fused kernel, hashed in this order
+LINEAR_SOURCES = [os.path.join(ROOT, "invariant_token_logprobs_gb300", "csrc", f)
+                  for f in ("lp_linear.cu", "lp_tcgen05.cuh", "lp_device.cuh")]
 
 
 def parse_args(argv=None):
@@ -102,10 +104,12 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
-def sha256_file(path: str) -> str:
+def sha256_files(paths) -> str:
+    """SHA-256 of the files' bytes concatenated in the given order."""
     h = hashlib.sha256()
-    with open(path, "rb") as f:
-        h.update(f.read())
+    for path in paths:
+        with open(path, "rb") as f:
+            h.update(f.read())
     return h.hexdigest()
 
 
@@ -120,7 +124,7 @@ def profile_traffic():
             if ":" in line:
                 k, v = line.split(":", 1)
                 fields[k.strip()] = v.strip()
-    if fields.get("source_sha256") != sha256_file(LINEAR_SOURCE):
+    if fields.get("source_sha256") != sha256_files(LINEAR_SOURCES):
         return None
     try:
         return float(fields["dram_bytes_per_launch_full_size"])

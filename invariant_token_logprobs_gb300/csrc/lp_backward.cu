@@ -21,10 +21,11 @@
 //      fp32), then lp_split_sum_kernel adds the ranges in order;
 //   4. lp_gemm_kernel<M-major A, N-major B>: dW = G^T H, reading G [T, V] as an
 //      M-major operand and H [T, d] as an N-major one.
-// No operand is transposed in memory.  Every output element is produced by one
-// CTA pair with a fixed K order and split sums are added in a fixed order: the
-// results are deterministic, and a row of dH depends only on that row's inputs
-// (not on T or its offset).
+// Both products write their fp32 output through TMA bulk stores from a
+// swizzled staging area.  No operand is transposed in memory.  Every output
+// element is produced by one CTA pair with a fixed K order and split sums are
+// added in a fixed order: the results are deterministic, and a row of dH
+// depends only on that row's inputs (not on T or its offset).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -154,6 +155,7 @@ struct GradEpilogue {
     }
   }
   __device__ __forceinline__ void after_release(int, uint32_t, int, int) {}
+  __device__ __forceinline__ void finish(int, int) {}
 };
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -199,69 +201,82 @@ struct GemmTiles {
 
 struct GemmArgs {
   GemmTiles tiles;
-  float* C;
-  int64_t ldc;
-  int64_t split_stride;
+  CUtensorMap tmC;  // bulk-store map of C
   int64_t M;
   int64_t N;
   uint32_t* err;
 };
 
-// Epilogue of the products: each warp stages its 32 rows x 64 columns of a
-// piece in shared memory (16-byte chunks placed at chunk ^ (row % 16), so the
-// writes by row and the reads by column are free of bank conflicts) and then
-// stores them two rows per instruction, 256 contiguous bytes per row.
-constexpr int kStageFloatsPerWarp = 32 * 64;
-constexpr int kGemmStagingBytes = 4 * kStageFloatsPerWarp * 4;  // 4 epilogue warps, 32 KB
+// Epilogue of the products.  Each warp owns 32 rows of the tile and writes
+// them in 32 x 32 boxes: a box is staged in shared memory with the 128-byte
+// swizzle of C's store map (16-byte chunk c of row r at chunk c ^ (r % 8)), and
+// one lane issues its TMA bulk store.  The warp's two staging buffers
+// alternate, one per store, each reused once the store that last read it has
+// finished reading.  Boxes wholly outside C are skipped (the map clips partial
+// ones).  C's row stride is a multiple of 16 bytes (d % 8 == 0).
+constexpr int kBoxFloats = 32 * 32;
+constexpr int kBoxes = 2;  // staging buffers per epilogue warp
 // dynamic shared memory of the product kernels: alignment slack, the
-// pipeline, then the staging area
-constexpr int kGemmSmemBytes = 1024 + kPipelineSmemEnd + kGemmStagingBytes;
+// pipeline, then 4 warps' staging buffers
+constexpr int kGemmSmemBytes = 1024 + kPipelineSmemEnd + 4 * kBoxes * kBoxFloats * 4;
 static_assert(kGemmSmemBytes <= 232448, "fits the 227 KB per-CTA limit");
+
+__device__ __forceinline__ void bulk_store_3d(const CUtensorMap* map, int c0, int c1, int c2,
+                                              uint32_t src) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(src)
+      : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
 
 struct GemmEpilogue {
   const GemmArgs* a;
+  int next = 0;  // staging buffer of this warp's next store
   __device__ __forceinline__ void consume(int u, uint32_t taddr, uint32_t rank, int lane_grp,
                                           int lane) {
     int mb, nb, s;
     a->tiles.decode(u, mb, nb, s);
     const int64_t row0 = static_cast<int64_t>(mb) * (2 * kBM) + rank * kBM + lane_grp * 32;
     const int64_t n0 = static_cast<int64_t>(nb) * kBN;
-    float* cbase = a->C + s * a->split_stride;
     float* stg = reinterpret_cast<float*>(pipeline_smem_base() + kPipelineSmemEnd) +
-                 lane_grp * kStageFloatsPerWarp;
-    const int c = lane & 15;     // 16-byte chunk this lane stores
-    const int half = lane >> 4;  // which of the two rows of an instruction
+                 lane_grp * kBoxes * kBoxFloats;
+    if (row0 >= a->M) return;
 #pragma unroll 1
     for (int p = 0; p < kBN / 64; ++p) {
+      if (n0 + p * 64 >= a->N) break;
       float v[64];
       __syncwarp();
       tmem_load64(taddr + static_cast<uint32_t>(p * 64), v);
 #pragma unroll
-      for (int k = 0; k < 16; ++k)
-        *reinterpret_cast<float4*>(stg + lane * 64 + ((k ^ (lane & 15)) * 4)) =
-            make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-      __syncwarp();
-      const int64_t col = n0 + p * 64 + c * 4;
-#pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
-        const int r = 2 * i + half;
-        const float4 x = *reinterpret_cast<const float4*>(stg + r * 64 + ((c ^ (r & 15)) * 4));
-        const int64_t grow = row0 + r;
-        if (grow >= a->M || col >= a->N) continue;
-        float* dst = cbase + grow * a->ldc + col;
-        if (col + 3 < a->N && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
-          *reinterpret_cast<float4*>(dst) = x;
-        } else {
-          const float xs[4] = {x.x, x.y, x.z, x.w};
+      for (int b = 0; b < 2; ++b) {
+        const int64_t col = n0 + p * 64 + b * 32;
+        if (col >= a->N) continue;
+        float* box = stg + next * kBoxFloats;
+        // the store that last read this buffer (kBoxes stores ago) has read it
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kBoxes - 1) : "memory");
+        __syncwarp();
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (col + e < a->N) dst[e] = xs[e];
+        for (int c = 0; c < 8; ++c) {
+          const int k = b * 8 + c;
+          *reinterpret_cast<float4*>(box + lane * 32 + ((c ^ (lane & 7)) * 4)) =
+              make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
         }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0)
+          bulk_store_3d(&a->tmC, static_cast<int>(col), static_cast<int>(row0), s, smem_u32(box));
+        if (++next == kBoxes) next = 0;
       }
     }
-    __syncwarp();
   }
   __device__ __forceinline__ void after_release(int, uint32_t, int, int) {}
+  __device__ __forceinline__ void finish(int, int lane) {
+    // every bulk store of this warp has written global memory
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
+  }
 };
 
 template <bool kAMn, bool kBMn>
@@ -349,12 +364,10 @@ lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a,
   const int64_t total = int64_t(g.tiles.n_mb) * g.tiles.n_nb * n_split;
   if (total >= (int64_t(1) << 31)) return LP_ERR_INVALID_ARGUMENT;
   g.tiles.total = static_cast<int>(total);
-  g.C = C;
-  g.ldc = ldc;
-  g.split_stride = split_stride;
   g.M = M;
   g.N = N;
   g.err = err;
+  if (!encode_f32_3d_store(&g.tmC, C, n_split, M, N, ldc, split_stride)) return LP_ERR_CUDA;
   lp_gemm_kernel<kAMn, kBMn>
       <<<pair_grid(dev.sm_count, total), kThreads, kGemmSmemBytes, stream>>>(tmA, tmB, g);
   return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;

@@ -79,6 +79,24 @@ bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t co
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_f32_3d_store(CUtensorMap* map, void* base, int64_t S, int64_t rows, int64_t cols,
+                         int64_t ld, int64_t split_stride) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  if (((ld * 4) % 16) != 0 || ((split_stride * 4) % 16) != 0 ||
+      (reinterpret_cast<uintptr_t>(base) % 16) != 0)
+    return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(S)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 4,
+                                 static_cast<cuuint64_t>(S > 1 ? split_stride : rows * ld) * 4};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int pair_grid(int sm_count, int64_t units) {
   int pairs = sm_count / 2;
   const int limit = persistent_grid_limit();
@@ -248,6 +266,8 @@ struct StateEpilogue {
       }
     }
   }
+
+  __device__ __forceinline__ void finish(int, int) {}
 
   __device__ __forceinline__ void after_release(int u, uint32_t rank, int lane_grp, int lane) {
     int mb, ql, j;

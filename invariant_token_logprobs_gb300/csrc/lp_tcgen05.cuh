@@ -276,7 +276,9 @@ __device__ __forceinline__ uint8_t* pipeline_smem_base() {
 //     read the finished 128 x 256 accumulator (this thread's lane at taddr,
 //     columns taddr + 0..255, with tmem_load64; warp-collective) and use it;
 //   void after_release(int u, uint32_t rank, int lane_grp, int lane);
-//     work that no longer needs tensor memory (after the accumulator is freed).
+//     work that no longer needs tensor memory (after the accumulator is freed);
+//   void finish(int lane_grp, int lane);
+//     once after the last unit (e.g. wait for asynchronous stores).
 //
 // Called by every thread of a CTA of a 2-CTA cluster launched with kThreads
 // threads and kSmemBytes of dynamic shared memory.  `withhold_first_load`
@@ -461,6 +463,7 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    epi.finish(lane_grp, lane);
   }
 
   tc_fence_before();
@@ -483,6 +486,14 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
 // elements read as zero.  Returns false if the driver rejects it.
 bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
                     int box_rows);
+
+// 3-D fp32 tensor map over [S, rows, cols] (cols contiguous, row stride ld
+// elements, S matrices split_stride elements apart) with 32 x 32 x 1 boxes and
+// 128-byte swizzle, for bulk stores of output tiles; elements outside the
+// tensor are not written.  Returns false if the driver rejects it (e.g. a
+// stride that is not a multiple of 16 bytes).
+bool encode_f32_3d_store(CUtensorMap* map, void* base, int64_t S, int64_t rows, int64_t cols,
+                         int64_t ld, int64_t split_stride);
 
 // Persistent grid (in CTAs, even) for `units` units on `sm_count` SMs under the
 // process-wide CTA limit: one CTA pair per two SMs, never more pairs than units.
