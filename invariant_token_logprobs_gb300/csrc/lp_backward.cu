@@ -289,16 +289,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------- plain kernels
 
-// out[i] = sum_s part[s][i] for s = 0 .. n_split-1 in order; NaN when any
-// error word of the call is set.
-__global__ void lp_split_sum_kernel(const float* __restrict__ part, int64_t n, int n_split,
-                                    const uint32_t* __restrict__ err, float* __restrict__ out) {
+// out[i] = sum_s part[s][i] for s = 0 .. n_split-1 in order (n_split <=
+// kSplitsDH); NaN when any error word of the call is set.  Four elements per
+// thread and step (n4 = n / 4; part and out 16-byte aligned).
+__global__ void lp_split_sum_kernel(const float4* __restrict__ part, int64_t n4, int n_split,
+                                    const uint32_t* __restrict__ err, float4* __restrict__ out) {
   const bool failed = (err[0] | err[1] | err[2] | err[3]) != 0u;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    float s = part[i];
-    for (int k = 1; k < n_split; ++k) s = __fadd_rn(s, part[k * n + i]);
-    out[i] = failed ? quiet_nan() : s;
+    float4 x[kSplitsDH];
+#pragma unroll
+    for (int k = 0; k < kSplitsDH; ++k)
+      if (k < n_split) x[k] = part[k * n4 + i];
+    float4 s = x[0];
+#pragma unroll
+    for (int k = 1; k < kSplitsDH; ++k) {
+      if (k < n_split) {
+        s.x = __fadd_rn(s.x, x[k].x);
+        s.y = __fadd_rn(s.y, x[k].y);
+        s.z = __fadd_rn(s.z, x[k].z);
+        s.w = __fadd_rn(s.w, x[k].w);
+      }
+    }
+    const float q = quiet_nan();
+    out[i] = failed ? make_float4(q, q, q, q) : s;
   }
 }
 
@@ -450,8 +464,10 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
   st = launch_gemm<false, true>(dev, G, T, L.V8, W, d, ld_w, V, kSplitsDH, dh_part, d, T * d,
                                 err + 2, stream, &n_split, false);
   if (st != LP_OK) return st;
-  lp_split_sum_kernel<<<dev.sm_count * 4, 256, 0, stream>>>(dh_part, T * d, n_split, err,
-                                                            grad_h);
+  // T * d is a multiple of 4 (d % 8 == 0); dh_part and grad_h are 16-byte aligned
+  lp_split_sum_kernel<<<dev.sm_count * 4, 256, 0, stream>>>(
+      reinterpret_cast<const float4*>(dh_part), T * d / 4, n_split, err,
+      reinterpret_cast<float4*>(grad_h));
   if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
 
   // 4. dW = G^T H (G read M-major, H read N-major)
