@@ -483,14 +483,14 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
 
 // 2-D bf16 tensor map over [rows, cols] (cols contiguous, row stride ld
 // elements) with a box of [box_rows, 64] and 128-byte swizzle; out-of-range
-// elements read as zero.  Returns false if the driver rejects it.
+// elements read as zero.  Returns false if the CUDA driver rejects it.
 bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int64_t ld,
                     int box_rows);
 
 // 3-D fp32 tensor map over [S, rows, cols] (cols contiguous, row stride ld
 // elements, S matrices split_stride elements apart) with 32 x 32 x 1 boxes and
 // 128-byte swizzle, for bulk stores of output tiles; elements outside the
-// tensor are not written.  Returns false if the driver rejects it (e.g. a
+// tensor are not written.  Returns false if the CUDA driver rejects it (e.g. a
 // stride that is not a multiple of 16 bytes).
 bool encode_f32_3d_store(CUtensorMap* map, void* base, int64_t S, int64_t rows, int64_t cols,
                          int64_t ld, int64_t split_stride);
