@@ -27,6 +27,7 @@
 namespace lp {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr double kLn2 = 0.6931471805599453;
 constexpr int kQuarters = 4;
 
 __host__ __device__ __forceinline__ int64_t quarter_begin(int64_t V, int q) {
@@ -104,8 +105,29 @@ __device__ __forceinline__ void rebase(float m, float s, float u, float M, float
   u_out = __fmul_rn(a, __fmaf_rn(delta, s, u));
 }
 
+// exp(delta) for delta <= 0 given exactly in double, through float: the
+// relative error is that of rounding delta to float plus CUDA's expf, a few
+// times 1e-7 for the terms that matter (|delta| of order 1); terms with large
+// |delta| are negligible in the sums they enter.  Double-precision
+// transcendentals are slow on this GPU and the four quarters need only this.
+__device__ __forceinline__ double exp_nonpos(double delta) {
+  return static_cast<double>(expf(static_cast<float>(delta)));
+}
+
+// log(S) for finite S > 0: with S = m 2^e, m in [0.5, 1) (frexp),
+// log S = log m + e ln 2, log m taken with CUDA's logf (|log m| < 0.7, so its
+// absolute error is about 1e-7) and the rest in double.  log S itself can be
+// ~12 or more, where a float would carry an error of ~1e-6.
+__device__ __forceinline__ double log_pos(double S) {
+  int e;
+  const double m = frexp(S, &e);
+  return __dadd_rn(static_cast<double>(logf(static_cast<float>(m))),
+                   __dmul_rn(static_cast<double>(e), kLn2));
+}
+
 // Final merge of the four quarter states, fixed order (Q0 + Q1) + (Q2 + Q3),
-// in float64, and the row's results.
+// in float64 (the exponentials and the logarithm through float, above), and
+// the row's results.
 __device__ __forceinline__ void finalise(const float4 (&q)[kQuarters], float& logp,
                                          float& entropy) {
   const float M = fmaxf(fmaxf(q[0].x, q[1].x), fmaxf(q[2].x, q[3].x));
@@ -117,7 +139,7 @@ __device__ __forceinline__ void finalise(const float4 (&q)[kQuarters], float& lo
       U_q[i] = 0.0;
     } else {
       const double delta = __dsub_rn(static_cast<double>(q[i].x), static_cast<double>(M));
-      const double a = exp(delta);
+      const double a = exp_nonpos(delta);
       S_q[i] = __dmul_rn(a, static_cast<double>(q[i].y));
       U_q[i] = __dmul_rn(a, __fma_rn(delta, static_cast<double>(q[i].y),
                                      static_cast<double>(q[i].z)));
@@ -131,7 +153,7 @@ __device__ __forceinline__ void finalise(const float4 (&q)[kQuarters], float& lo
     entropy = quiet_nan();
     return;
   }
-  const double log_s = log(S);
+  const double log_s = log_pos(S);
   logp = __double2float_rn(
       __dsub_rn(__dsub_rn(static_cast<double>(t), static_cast<double>(M)), log_s));
   entropy = __double2float_rn(__dsub_rn(log_s, __ddiv_rn(U, S)));

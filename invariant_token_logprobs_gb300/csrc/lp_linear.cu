@@ -352,11 +352,11 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
       for (int i = 0; i < kQuarters; ++i)
         if (q4[i].x != neg_inf())
-          S = __dadd_rn(S, __dmul_rn(exp(__dsub_rn(static_cast<double>(q4[i].x),
-                                                   static_cast<double>(M))),
+          S = __dadd_rn(S, __dmul_rn(exp_nonpos(__dsub_rn(static_cast<double>(q4[i].x),
+                                                          static_cast<double>(M))),
                                      static_cast<double>(q4[i].y)));
       lse[row] = (*err != 0u) ? quiet_nan()
-                              : __double2float_rn(__dadd_rn(static_cast<double>(M), log(S)));
+                              : __double2float_rn(__dadd_rn(static_cast<double>(M), log_pos(S)));
     }
   }
 }
