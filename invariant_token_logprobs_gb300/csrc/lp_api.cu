@@ -223,7 +223,7 @@ lp_status lp_merge_partials(const float* const* shard_partials, int n_shards, in
 size_t lp_linear_logprob_workspace_size(int64_t T, int64_t d, int64_t V) {
   (void)d;
   if (T < 0 || V < 1 || V > lp::kMaxDim) return 0;
-  return lp::linear_workspace_bytes(T, V, 4);
+  return lp::linear_workspace_bytes(T, d, V, 4);
 }
 
 size_t lp_linear_logprob_partials_workspace_size(int64_t T, int64_t d, int64_t vocab_total,
@@ -231,7 +231,7 @@ size_t lp_linear_logprob_partials_workspace_size(int64_t T, int64_t d, int64_t v
   (void)d;
   if (T < 0 || vocab_total < 1 || vocab_total > lp::kMaxDim) return 0;
   if (!(n_shards == 1 || n_shards == 2 || n_shards == 4)) return 0;
-  return lp::linear_workspace_bytes(T, vocab_total, 4 / n_shards);
+  return lp::linear_workspace_bytes(T, d, vocab_total, 4 / n_shards);
 }
 
 lp_status lp_linear_logprob_temperature(const void* H, int64_t ld_h, const void* W, int64_t ld_w,
@@ -245,7 +245,7 @@ lp_status lp_linear_logprob_temperature(const void* H, int64_t ld_h, const void*
   if (logp_out == nullptr || workspace == nullptr) return LP_ERR_INVALID_ARGUMENT;
   if (!lp::aligned(logp_out, 4) || !lp::aligned(entropy_out, 4) || !lp::aligned(workspace, 256))
     return LP_ERR_MISALIGNED;
-  if (workspace_bytes < lp::linear_workspace_bytes(T, V, 4)) return LP_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < lp::linear_workspace_bytes(T, d, V, 4)) return LP_ERR_WORKSPACE_TOO_SMALL;
   lp::Device dev;
   st = lp::current_device(&dev);
   if (st != LP_OK) return st;
@@ -260,7 +260,7 @@ lp_status lp_linear_logprob_noalloc(const void* H, int64_t ld_h, const void* W, 
   if (st != LP_OK || T == 0) return st;
   if (logp_out == nullptr) return LP_ERR_INVALID_ARGUMENT;
   if (!lp::aligned(logp_out, 4) || !lp::aligned(entropy_out, 4)) return LP_ERR_MISALIGNED;
-  if (lp::linear_workspace_bytes(T, V, 4) > lp::static_scratch_bytes())
+  if (lp::linear_workspace_bytes(T, d, V, 4) > lp::static_scratch_bytes())
     return LP_ERR_WORKSPACE_TOO_SMALL;
   lp::Device dev;
   st = lp::current_device(&dev);
@@ -286,7 +286,7 @@ lp_status lp_linear_logprob_lse(const void* H, int64_t ld_h, const void* W, int6
   if (!lp::aligned(logp_out, 4) || !lp::aligned(entropy_out, 4) || !lp::aligned(lse_out, 4) ||
       !lp::aligned(workspace, 256))
     return LP_ERR_MISALIGNED;
-  if (workspace_bytes < lp::linear_workspace_bytes(T, V, 4)) return LP_ERR_WORKSPACE_TOO_SMALL;
+  if (workspace_bytes < lp::linear_workspace_bytes(T, d, V, 4)) return LP_ERR_WORKSPACE_TOO_SMALL;
   lp::Device dev;
   st = lp::current_device(&dev);
   if (st != LP_OK) return st;
@@ -312,7 +312,7 @@ lp_status lp_linear_logprob_partials_temperature(const void* H, int64_t ld_h,
   if (!lp::aligned(partials_out, 16) || !lp::aligned(workspace, 256)) return LP_ERR_MISALIGNED;
   int q_first, n_q;
   lp::shard_quarters(shard_index, n_shards, q_first, n_q);
-  if (workspace_bytes < lp::linear_workspace_bytes(T, vocab_total, n_q))
+  if (workspace_bytes < lp::linear_workspace_bytes(T, d, vocab_total, n_q))
     return LP_ERR_WORKSPACE_TOO_SMALL;
   lp::Device dev;
   st = lp::current_device(&dev);

@@ -335,7 +335,7 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 BackwardLayout backward_layout(int64_t T, int64_t d, int64_t V) {
   BackwardLayout L;
   L.V8 = round8(V);
-  size_t o = align256(linear_workspace_bytes(T, V, 4));
+  size_t o = align256(linear_workspace_bytes(T, d, V, 4));
   L.off_lse = o; o = align256(o + sizeof(float) * T);
   L.off_logp = o; o = align256(o + sizeof(float) * T);
   L.off_ent = o; o = align256(o + sizeof(float) * T);

@@ -53,7 +53,7 @@ lp_status launch_merge_partials(const float* const* shard_partials, int n_shards
                                 float* logp, float* entropy, cudaStream_t stream);
 
 // fused path
-size_t linear_workspace_bytes(int64_t T, int64_t V_total, int n_q);
+size_t linear_workspace_bytes(int64_t T, int64_t d, int64_t V_total, int n_q);
 lp_status launch_linear(const Device& dev, const void* H, int64_t ld_h, const void* W,
                         int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
                         int64_t V_total, int q_first, int n_q, float inv_tau, float* logp,

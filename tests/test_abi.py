@@ -56,6 +56,11 @@ def test_workspace_sizes(lib):
     assert lp.lp_linear_logprob_workspace_size(512, 4096, 151936) == 256 + 4 * tiles * 512 * 16
     assert lp.lp_linear_logprob_partials_workspace_size(512, 4096, 151936, 2) == 256 + 2 * tiles * 512 * 16
     assert lp.lp_linear_logprob_workspace_size(0, 8, 10) == 256
+    # fewer than 16 rows: a 16-row bf16 copy of H follows, 256-byte aligned
+    t1000 = -(-((1000 + 3) // 4) // 256)  # tiles per quarter of V = 1000
+    assert lp.lp_linear_logprob_workspace_size(5, 64, 1000) == \
+        -(-(256 + 4 * t1000 * 5 * 16) // 256) * 256 + 16 * 64 * 2
+    assert lp.lp_linear_logprob_workspace_size(16, 64, 1000) == 256 + 4 * t1000 * 16 * 16
     assert lp.lp_linear_logprob_workspace_size(-1, 8, 10) == 0
 
 

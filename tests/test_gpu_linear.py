@@ -65,6 +65,26 @@ def test_qwen3_8b_head_full_size_sampled_rows():
     assert e_lp <= FUSED_TOL and e_ent <= FUSED_TOL
 
 
+def test_wide_hidden_large_vocabulary_sampled_rows():
+    """The largest shapes of the tests: d = 8192 (128 K blocks per tile) and
+    V = 262147 (256 tiles per quarter, ragged quarters), sampled rows; plus
+    2-shard bitwise equality at that size."""
+    T, d, V = 96, 8192, 262147
+    x = synth.fused_inputs("fused_qwen3_8b", device=DEV, T=T, d=d, V=V, seed=11)
+    logp, ent = lp.linear_logprob(x.H, x.W, x.y)
+    rows = torch.tensor([0, 37, 64, 95])
+    ref_lp, ref_ent = oracle_fused(x.H, x.W, x.y, rows)
+    e_lp, e_ent = max_err(logp[rows], ref_lp), max_err(ent[rows], ref_ent)
+    print(f"d=8192, V=262147: logp err {e_lp:.3e}, entropy err {e_ent:.3e}")
+    assert e_lp <= FUSED_TOL and e_ent <= FUSED_TOL
+    parts = []
+    for i in range(2):
+        b, e = lp.vocab_shard_range(V, i, 2)
+        parts.append(lp.linear_logprob_partials(x.H, x.W[b:e], x.y, V, i, 2))
+    m_lp, m_ent = lp.merge_partials(parts)
+    assert torch.equal(bits(m_lp), bits(logp)) and torch.equal(bits(m_ent), bits(ent))
+
+
 def test_qwen3_next_head_shards_bitwise_and_sampled_parity():
     x = synth.fused_inputs("fused_qwen3_next", device=DEV)
     V = x.W.shape[0]

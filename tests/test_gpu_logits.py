@@ -43,6 +43,15 @@ def test_small_all_rows(T, V):
     _check(x.z, x.y)
 
 
+def test_large_vocabulary_all_rows():
+    """V = 262147 (ragged quarters of 65536/65537 columns), every row."""
+    x = synth.logits_inputs("logits_peaked", device=DEV, T=8, V=262147, seed=21)
+    logp, ent = lp.logprob_from_logits(x.z, x.y)
+    ref_lp, ref_ent = oracle_logits(x.z, x.y)
+    e_lp, e_ent = max_err(logp, ref_lp), max_err(ent, ref_ent)
+    assert e_lp <= LOGITS_LOGP_TOL and e_ent <= LOGITS_ENT_TOL, (e_lp, e_ent)
+
+
 def test_peaked_workload_full_size_sampled_rows():
     x = synth.logits_inputs("logits_peaked", device=DEV)
     assert x.z.shape == (1024, 151936)
