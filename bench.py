@@ -43,9 +43,13 @@ WORKLOAD = "fused_qwen3_8b"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "lp_linear_kernel.fused_qwen3_8b.txt")
-# the sources that define the fused kernel, hashed in this order
+LOGITS_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "lp_logits_final_kernel.logits_peaked.txt")
+# the sources that define the fused kernel and the logits kernel, hashed in
+# this order
 LINEAR_SOURCES = [os.path.join(ROOT, "invariant_token_logprobs_gb300", "csrc", f)
                   for f in ("lp_linear.cu", "lp_tcgen05.cuh", "lp_device.cuh")]
+LOGITS_SOURCES = [os.path.join(ROOT, "invariant_token_logprobs_gb300", "csrc", f)
+                  for f in ("lp_logits.cu", "lp_device.cuh")]
 
 
 def parse_args(argv=None):
@@ -113,18 +117,18 @@ def sha256_files(paths) -> str:
     return h.hexdigest()
 
 
-def profile_traffic():
-    """DRAM bytes per launch of the fused kernel from the committed ncu summary,
-    or None when absent or taken on a different kernel source."""
-    if not os.path.exists(PROFILE_SUMMARY):
+def profile_traffic(summary=PROFILE_SUMMARY, sources=LINEAR_SOURCES):
+    """DRAM bytes per launch of a kernel from its committed ncu summary, or None
+    when the summary is absent or was taken on different kernel sources."""
+    if not os.path.exists(summary):
         return None
     fields = {}
-    with open(PROFILE_SUMMARY) as f:
+    with open(summary) as f:
         for line in f:
             if ":" in line:
                 k, v = line.split(":", 1)
                 fields[k.strip()] = v.strip()
-    if fields.get("source_sha256") != sha256_files(LINEAR_SOURCES):
+    if fields.get("source_sha256") != sha256_files(sources):
         return None
     try:
         return float(fields["dram_bytes_per_launch_full_size"])
@@ -548,7 +552,8 @@ def bench_logits(lp, synth, torch, dev, stream, peaks, peaks_kind, max_over, wor
     return {"workload": "logits_peaked", "T": T, "V": V, "value": whole_job_throughput(T, 1, world, ms),
             "unit": "rows/s", "us_per_call": ms * 1e3, "gpu_launches_per_call": 1,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                         "frac": gbs / peaks["hbm_gbs"],
+                         "traffic": profile_traffic(LOGITS_PROFILE_SUMMARY, LOGITS_SOURCES),
                          "kernel": "lp_logits_final_kernel",
                          "algorithmic_bytes_per_launch": nbytes,
                          "peak_source": f"{peaks_kind} copy bandwidth"}}

@@ -374,8 +374,10 @@ size_t chunk_bytes(int64_t T, int64_t V_total, int n_q) {
          static_cast<size_t>(T) * sizeof(float4);
 }
 
-// dst [rows_out, d] (dense) = H [T, d] (row stride ld_h) followed by zero
-// rows; 16 bytes per thread and step (d % 8 == 0, both 16-byte aligned).
+// dst [rows_out, d8] (dense, d8 = d rounded up to 8) = H [T, d8] (row stride
+// ld_h >= d8, a multiple of 8) followed by zero rows; 16 bytes per thread and
+// step (both 16-byte aligned).  Columns d .. d8-1 come from the padding of
+// H's rows and are never read through the tensor map (its width is d).
 __global__ void lp_pad_rows_kernel(const uint4* __restrict__ H, int64_t ld_h16, int64_t T,
                                    int64_t d16, int64_t rows_out, uint4* __restrict__ dst) {
   const int64_t n = rows_out * d16;
@@ -391,7 +393,7 @@ __global__ void lp_pad_rows_kernel(const uint4* __restrict__ H, int64_t ld_h16, 
 size_t linear_workspace_bytes(int64_t T, int64_t d, int64_t V_total, int n_q) {
   size_t bytes = kWorkspaceHeader + chunk_bytes(T, V_total, n_q);
   if (T > 0 && T < kPadRows)
-    bytes = (bytes + 255) / 256 * 256 + static_cast<size_t>(kPadRows * d) * 2;
+    bytes = (bytes + 255) / 256 * 256 + static_cast<size_t>(kPadRows * ((d + 7) / 8 * 8)) * 2;
   return bytes;
 }
 
@@ -415,11 +417,13 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
   if (T > 0 && T < kPadRows) {
     const size_t off = (kWorkspaceHeader + chunk_bytes(T, V_total, n_q) + 255) / 256 * 256;
     void* padded = static_cast<uint8_t*>(workspace) + off;
-    lp_pad_rows_kernel<<<(kPadRows * d / 8 + 255) / 256, 256, 0, stream>>>(
-        static_cast<const uint4*>(H), ld_h / 8, T, d / 8, kPadRows, static_cast<uint4*>(padded));
+    const int64_t d8 = (d + 7) / 8 * 8;
+    lp_pad_rows_kernel<<<static_cast<unsigned>((kPadRows * d8 / 8 + 255) / 256), 256, 0,
+                         stream>>>(static_cast<const uint4*>(H), ld_h / 8, T, d8 / 8, kPadRows,
+                                   static_cast<uint4*>(padded));
     if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
     H = padded;
-    ld_h = d;
+    ld_h = d8;
     h_rows = kPadRows;
   }
   CUtensorMap tmA, tmB;

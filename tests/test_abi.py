@@ -61,6 +61,9 @@ def test_workspace_sizes(lib):
     assert lp.lp_linear_logprob_workspace_size(5, 64, 1000) == \
         -(-(256 + 4 * t1000 * 5 * 16) // 256) * 256 + 16 * 64 * 2
     assert lp.lp_linear_logprob_workspace_size(16, 64, 1000) == 256 + 4 * t1000 * 16 * 16
+    # the copy's rows are d rounded up to 8 wide
+    assert lp.lp_linear_logprob_workspace_size(5, 60, 1000) == \
+        -(-(256 + 4 * t1000 * 5 * 16) // 256) * 256 + 16 * 64 * 2
     assert lp.lp_linear_logprob_workspace_size(-1, 8, 10) == 0
 
 

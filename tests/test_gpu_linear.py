@@ -55,6 +55,26 @@ def test_ragged_shapes_all_rows(T, d, V):
     _check_all_rows(x)
 
 
+@pytest.mark.parametrize("T", [5, 40])
+def test_hidden_size_not_a_multiple_of_8(T):
+    """d = 60 with rows padded to a stride of 64 (the boundary requires
+    16-byte row strides, not d % 8 == 0); T = 5 goes through the 16-row copy
+    of H, T = 40 reads H in place."""
+    d, V = 60, 777
+    x = synth.fused_inputs("fused_tiny", device=DEV, T=T, d=d, V=V, seed=3)
+    Hs = torch.zeros((T, 64), dtype=x.H.dtype, device=DEV)
+    Ws = torch.zeros((V, 64), dtype=x.W.dtype, device=DEV)
+    Hs[:, :d] = x.H
+    Ws[:, :d] = x.W
+    Hs[:, d:] = 1.0  # the row padding must never be read as data
+    Ws[:, d:] = 1.0
+    logp, ent = lp.linear_logprob(Hs[:, :d], Ws[:, :d], x.y)
+    torch.cuda.synchronize()
+    ref_lp, ref_ent = oracle_fused(x.H, x.W, x.y)
+    e_lp, e_ent = max_err(logp, ref_lp), max_err(ent, ref_ent)
+    assert e_lp <= FUSED_TOL and e_ent <= FUSED_TOL, (e_lp, e_ent)
+
+
 def test_qwen3_8b_head_full_size_sampled_rows():
     x = synth.fused_inputs("fused_qwen3_8b", device=DEV)
     logp, ent = lp.linear_logprob(x.H, x.W, x.y)
