@@ -55,7 +55,9 @@ LOGITS_SOURCES = [os.path.join(ROOT, "invariant_token_logprobs_gb300", "csrc", f
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
+    # 1000 steps of the headline workload keep the GPU busy ~0.4 s, several
+    # refreshes of nvidia-smi's clock readings (about every 100 ms)
+    p.add_argument("--steps", type=int, default=1000)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["lp", "reference"], default="lp")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -190,7 +192,12 @@ class ClockSampler:
                     except ValueError:
                         continue
             os.unlink(self.path)
-        inside = [r for r in rows if t_begin - 0.05 <= r[0] <= t_end + 0.05]
+        # nvidia-smi refreshes these readings about every 100 ms, so a sample
+        # shows the state up to ~100 ms earlier: the window runs to 150 ms past
+        # the end of the timed region and starts 100 ms into it when it is long
+        # enough (earlier samples still show the GPU before the load)
+        lo = t_begin + 0.1 if t_end - t_begin > 0.3 else t_begin
+        inside = [r for r in rows if lo <= r[0] <= t_end + 0.15]
         use = inside if inside else rows
         if not use:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
@@ -198,7 +205,8 @@ class ClockSampler:
         reasons = sorted({names[i] for r in use for i in range(4) if r[3][i].lower() == "active"})
         return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
                 "reasons": reasons, "samples": len(inside),
-                "window": "timed region" if inside else "nearest samples (timed region shorter than sampling)"}
+                "window": ("timed region, shifted by nvidia-smi's ~100 ms refresh"
+                           if inside else "nearest samples (timed region shorter than sampling)")}
 
 
 # ------------------------------------------------------------- CPU oracle legs
@@ -355,6 +363,7 @@ def run_lp(args):
     roofline = {
         "bound": "tensor", "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s",
         "frac": achieved_tf / peak_tf, "traffic": profile_traffic(),
+        "frac_vs_sustained": achieved_tf / peaks.get("bf16_tflops_sustained", peak_tf),
         "kernel": "lp_linear_kernel", "kernel_us": kernel_ms * 1e3,
         "algorithmic_flops_per_launch": flops, "roofline_us": roofline_us,
         "peak_source": f"{peaks_kind} bf16 burst ({'MEASURED_PEAKS.json' if peaks_kind == 'measured' else 'fallback'})",
@@ -374,7 +383,7 @@ def run_lp(args):
     lp_dev = [torch.empty(T, device=dev) for _ in range(2)]
     ent_dev = [torch.empty(T, device=dev) for _ in range(2)]
     copy_stream = torch.cuda.Stream(device=dev)
-    K2 = max(1, min(K, 100))
+    K2 = K  # as many steps as the device-resident loop, so both run in the same power state
 
     def pipelined(n):
         in_ready = [torch.cuda.Event() for _ in range(2)]
