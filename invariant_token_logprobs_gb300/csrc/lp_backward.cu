@@ -387,9 +387,76 @@ lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a,
   return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }
 
+// Batches of fewer than kSmallRows rows run the whole backward on copies
+// padded with zero rows to kSmallRows (zero upstream gradients, so the padded
+// rows add nothing to grad_W and their grad_H rows are dropped): with a row
+// extent this small the operand loads of all three tensor-core kernels ran
+// slowly (T = 1: ~1040 us against ~880 us at T = 16).  The padded rows carry
+// exactly the zeros the loads filled in before, so the results are the same
+// bits.
+constexpr int64_t kSmallRows = 16;
+
+struct SmallLayout {
+  size_t inner;  // workspace of the padded backward (at offset 0)
+  size_t off_h, off_y, off_gl, off_ge, off_lse, off_ent, off_gh, total;
+};
+
+SmallLayout small_layout(int64_t d, int64_t V) {
+  SmallLayout L;
+  const int64_t d8 = (d + 7) / 8 * 8;
+  size_t o = align256(backward_layout(kSmallRows, d, V).total);
+  L.inner = o;
+  L.off_h = o; o = align256(o + 2 * static_cast<size_t>(kSmallRows * d8));
+  L.off_y = o; o = align256(o + 8 * kSmallRows);
+  L.off_gl = o; o = align256(o + 4 * kSmallRows);
+  L.off_ge = o; o = align256(o + 4 * kSmallRows);
+  L.off_lse = o; o = align256(o + 4 * kSmallRows);
+  L.off_ent = o; o = align256(o + 4 * kSmallRows);
+  L.off_gh = o; o = align256(o + 4 * static_cast<size_t>(kSmallRows * d));
+  L.total = o;
+  return L;
+}
+
+// Zero-padded kSmallRows-row copies of the backward's per-row inputs: H (rows
+// d8 = d rounded up to 8 wide, zeros past column d), targets (0 past T), and
+// the optional per-row floats (0 past T).
+__global__ void lp_pad_backward_kernel(const uint16_t* __restrict__ H, int64_t ld_h, int64_t d,
+                                       int64_t T, const int64_t* __restrict__ y,
+                                       const float* __restrict__ gl, const float* __restrict__ ge,
+                                       const float* __restrict__ lse, const float* __restrict__ ent,
+                                       uint4* __restrict__ H_out, int64_t* __restrict__ y_out,
+                                       float* __restrict__ gl_out, float* __restrict__ ge_out,
+                                       float* __restrict__ lse_out, float* __restrict__ ent_out) {
+  const int64_t d16 = (d + 7) / 8;
+  const int64_t n = kSmallRows * d16;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / d16, c = i % d16;
+    H_out[i] = r < T ? load_row_chunk(H + r * ld_h, d, c) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (blockIdx.x == 0 && threadIdx.x < kSmallRows) {
+    const int r = threadIdx.x;
+    const bool in = r < T;
+    y_out[r] = in ? y[r] : 0;
+    if (gl != nullptr) gl_out[r] = in ? gl[r] : 0.f;
+    if (ge != nullptr) ge_out[r] = in ? ge[r] : 0.f;
+    if (lse != nullptr) lse_out[r] = in ? lse[r] : 0.f;
+    if (ent != nullptr) ent_out[r] = in ? ent[r] : 0.f;
+  }
+}
+
+// grad_h [T, d] = the first T rows of gh [kSmallRows, d].
+__global__ void lp_copy_rows_kernel(const float* __restrict__ gh, int64_t n,
+                                    float* __restrict__ grad_h) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    grad_h[i] = gh[i];
+}
+
 }  // namespace
 
 size_t linear_backward_workspace_bytes(int64_t T, int64_t d, int64_t V) {
+  if (T > 0 && T < kSmallRows) return small_layout(d, V).total;
   return backward_layout(T, d, V).total;
 }
 
@@ -399,6 +466,30 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
                                  const float* saved_entropy, const float* g_logp,
                                  const float* g_ent, float* grad_h, float* grad_w,
                                  void* workspace, cudaStream_t stream) {
+  if (T > 0 && T < kSmallRows) {
+    const SmallLayout S = small_layout(d, V);
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    const int64_t d8 = (d + 7) / 8 * 8;
+    uint4* h16 = reinterpret_cast<uint4*>(base + S.off_h);
+    int64_t* y16 = reinterpret_cast<int64_t*>(base + S.off_y);
+    float* gl16 = g_logp != nullptr ? reinterpret_cast<float*>(base + S.off_gl) : nullptr;
+    float* ge16 = g_ent != nullptr ? reinterpret_cast<float*>(base + S.off_ge) : nullptr;
+    float* lse16 = saved_lse != nullptr ? reinterpret_cast<float*>(base + S.off_lse) : nullptr;
+    float* ent16 = saved_entropy != nullptr ? reinterpret_cast<float*>(base + S.off_ent) : nullptr;
+    float* gh16 = reinterpret_cast<float*>(base + S.off_gh);
+    lp_pad_backward_kernel<<<static_cast<unsigned>((kSmallRows * d8 / 8 + 255) / 256), 256, 0,
+                             stream>>>(static_cast<const uint16_t*>(H), ld_h, d, T, targets,
+                                       g_logp, g_ent, saved_lse, saved_entropy, h16, y16, gl16,
+                                       ge16, lse16, ent16);
+    if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
+    const lp_status st =
+        launch_linear_backward(dev, h16, d8, W, ld_w, y16, kSmallRows, d, V, inv_tau, lse16,
+                               ent16, gl16, ge16, gh16, grad_w, workspace, stream);
+    if (st != LP_OK) return st;
+    lp_copy_rows_kernel<<<static_cast<unsigned>((T * d + 255) / 256), 256, 0, stream>>>(
+        gh16, T * d, grad_h);
+    return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
+  }
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {

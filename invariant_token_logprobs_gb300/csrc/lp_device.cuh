@@ -51,6 +51,23 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
   return r;
 }
 
+// Chunk c (8 bf16 values, 16 bytes) of a row of d bf16 values starting at row
+// (16-byte aligned): read whole when it lies inside the row, value by value
+// with zeros past d otherwise, so nothing past the row's d values is read.
+__device__ __forceinline__ uint4 load_row_chunk(const uint16_t* __restrict__ row, int64_t d,
+                                                int64_t c) {
+  if (c * 8 + 8 <= d) return *reinterpret_cast<const uint4*>(row + c * 8);
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t k = c * 8 + 2 * i;
+    const uint32_t lo = k < d ? row[k] : 0u;
+    const uint32_t hi = k + 1 < d ? row[k + 1] : 0u;
+    w[i] = lo | (hi << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000u); }
 __device__ __forceinline__ float quiet_nan() { return __int_as_float(0x7fffffffu); }
 

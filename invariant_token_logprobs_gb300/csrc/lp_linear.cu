@@ -374,17 +374,17 @@ size_t chunk_bytes(int64_t T, int64_t V_total, int n_q) {
          static_cast<size_t>(T) * sizeof(float4);
 }
 
-// dst [rows_out, d8] (dense, d8 = d rounded up to 8) = H [T, d8] (row stride
-// ld_h >= d8, a multiple of 8) followed by zero rows; 16 bytes per thread and
-// step (both 16-byte aligned).  Columns d .. d8-1 come from the padding of
-// H's rows and are never read through the tensor map (its width is d).
-__global__ void lp_pad_rows_kernel(const uint4* __restrict__ H, int64_t ld_h16, int64_t T,
-                                   int64_t d16, int64_t rows_out, uint4* __restrict__ dst) {
+// dst [rows_out, d8] (dense, d8 = d rounded up to 8) = H [T, d] (row stride
+// ld_h, a multiple of 8) with zeros past column d and past row T; 16 bytes per
+// thread and step (both 16-byte aligned).
+__global__ void lp_pad_rows_kernel(const uint16_t* __restrict__ H, int64_t ld_h, int64_t T,
+                                   int64_t d, int64_t rows_out, uint4* __restrict__ dst) {
+  const int64_t d16 = (d + 7) / 8;
   const int64_t n = rows_out * d16;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t r = i / d16, c = i % d16;
-    dst[i] = r < T ? H[r * ld_h16 + c] : make_uint4(0u, 0u, 0u, 0u);
+    dst[i] = r < T ? load_row_chunk(H + r * ld_h, d, c) : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
@@ -419,7 +419,7 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
     void* padded = static_cast<uint8_t*>(workspace) + off;
     const int64_t d8 = (d + 7) / 8 * 8;
     lp_pad_rows_kernel<<<static_cast<unsigned>((kPadRows * d8 / 8 + 255) / 256), 256, 0,
-                         stream>>>(static_cast<const uint4*>(H), ld_h / 8, T, d8 / 8, kPadRows,
+                         stream>>>(static_cast<const uint16_t*>(H), ld_h, T, d, kPadRows,
                                    static_cast<uint4*>(padded));
     if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
     H = padded;

@@ -81,6 +81,22 @@ def test_backward_small_against_oracle(T, d, V, tau):
     _check_against_oracle(x, gl, ge, tau, gH, gW)
 
 
+@pytest.mark.parametrize("T", [5, 40])
+def test_backward_hidden_size_not_a_multiple_of_8(T):
+    """d = 60 with H and W rows at a stride of 64 (their padding holds ones,
+    which must not be read); T = 5 goes through the padded small-batch path."""
+    d, V = 60, 777
+    x = synth.fused_inputs("fused_tiny", device=DEV, T=T, d=d, V=V, seed=8)
+    Hs = torch.ones((T, 64), dtype=x.H.dtype, device=DEV)
+    Ws = torch.ones((V, 64), dtype=x.W.dtype, device=DEV)
+    Hs[:, :d] = x.H
+    Ws[:, :d] = x.W
+    gl, ge = _upstream(T, seed=T + 1)
+    gH, gW = lp.linear_logprob_backward(Hs[:, :d], Ws[:, :d], x.y, gl, ge, temperature=0.8)
+    torch.cuda.synchronize()
+    _check_against_oracle(x, gl, ge, 0.8, gH, gW)
+
+
 def test_backward_one_upstream_and_bad_targets():
     x = synth.fused_inputs("fused_tiny", device=DEV, T=40, d=128, V=5000, seed=12)
     x.y[3] = -1
