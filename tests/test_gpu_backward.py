@@ -138,6 +138,22 @@ def test_backward_with_saved_forward_statistics():
         assert torch.equal(bits(a[1].reshape(-1)), bits(b[1].reshape(-1)))
 
 
+def test_backward_grid_size_invariant():
+    """The backward's results do not depend on the persistent grid size."""
+    x = synth.fused_inputs("fused_tiny", device=DEV, T=300, d=256, V=30000, seed=6)
+    gl, ge = _upstream(300, seed=4)
+    ref_h, ref_w = lp.linear_logprob_backward(x.H, x.W, x.y, gl, ge)
+    try:
+        for limit in (2, 16, 50):
+            lp.lp_set_persistent_grid_limit(limit)
+            h, w = lp.linear_logprob_backward(x.H, x.W, x.y, gl, ge)
+            torch.cuda.synchronize()
+            assert torch.equal(bits(h.reshape(-1)), bits(ref_h.reshape(-1))), limit
+            assert torch.equal(bits(w.reshape(-1)), bits(ref_w.reshape(-1))), limit
+    finally:
+        lp.lp_set_persistent_grid_limit(0)
+
+
 def test_backward_deterministic_and_row_invariant():
     x = synth.fused_inputs("fused_tiny", device=DEV, T=300, d=256, V=30000, seed=4)
     gl, ge = _upstream(300, seed=9)

@@ -36,8 +36,10 @@ def test_noalloc_matches_workspace_call_twice_in_a_row():
     lp.load()
     a = synth.fused_inputs("fused_tiny", device=DEV)
     b = synth.fused_inputs("fused_tiny", device=DEV, T=300, d=512, V=20000 + 3, seed=11)
+    c = synth.fused_inputs("fused_tiny", device=DEV, T=5, d=256, V=3001, seed=12)
     _compare(a)
     _compare(b)
+    _compare(c)  # fewer than 16 rows: the 16-row copy of H lives in the scratch too
     _compare(a)
 
 
