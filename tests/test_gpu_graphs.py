@@ -120,3 +120,51 @@ def test_sharded_merge_graph_replay_bytes_equal_eager():
     torch.cuda.synchronize()
     ref = lp.linear_logprob(x.H, x.W, x.y)
     assert torch.equal(bits(logp), bits(ref[0])) and torch.equal(bits(ent), bits(ref[1]))
+
+
+@pytest.mark.parametrize("saved", [False, True])
+def test_backward_graph_replay_bytes_equal_eager(saved):
+    """The backward (with and without the forward's saved statistics) captured
+    once on static buffers; replays on fresh rows equal eager calls."""
+    T, d, V = 40, 256, 20000
+    W = synth.fused_inputs("fused_tiny", device=DEV, T=1, d=d, V=V, seed=3).W
+    H = torch.empty((T, d), dtype=torch.bfloat16, device=DEV)
+    y = torch.empty(T, dtype=torch.int64, device=DEV)
+    gl = torch.empty(T, device=DEV)
+    ge = torch.empty(T, device=DEV)
+    lse = torch.empty(T, device=DEV)
+    ent = torch.empty(T, device=DEV)
+    logp = torch.empty(T, device=DEV)
+    fws = torch.empty(lp.lp_linear_logprob_workspace_size(T, d, V), dtype=torch.uint8, device=DEV)
+    ws = torch.empty(lp.lp_linear_logprob_backward_workspace_size(T, d, V), dtype=torch.uint8,
+                     device=DEV)
+    gH = torch.empty((T, d), device=DEV)
+    gW = torch.empty((V, d), device=DEV)
+
+    def fill(seed):
+        x = synth.fused_inputs("fused_tiny", device=DEV, T=T, d=d, V=V, seed=seed)
+        H.copy_(x.H)
+        y.copy_(x.y)
+        g = torch.Generator(device=DEV)
+        g.manual_seed(seed)
+        gl.copy_(torch.randn(T, generator=g, device=DEV))
+        ge.copy_(torch.randn(T, generator=g, device=DEV))
+        if saved:
+            lp.lp_linear_logprob_lse(H, W, y, 1.0, logp, ent, lse, fws)
+
+    def call():
+        lp.lp_linear_logprob_backward(H, W, y, 1.0, lse if saved else None,
+                                      ent if saved else None, gl, ge, gH, gW, ws)
+
+    fill(100)
+    graph = _capture(call)
+    for seed in (101, 102):
+        fill(seed)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        got_h, got_w = gH.clone(), gW.clone()
+        call()
+        torch.cuda.synchronize()
+        assert torch.equal(bits(got_h.reshape(-1)), bits(gH.reshape(-1)))
+        assert torch.equal(bits(got_w.reshape(-1)), bits(gW.reshape(-1)))
