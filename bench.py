@@ -28,6 +28,7 @@ import datetime as _dt
 import hashlib
 import json
 import os
+import shutil
 import statistics
 import subprocess
 import sys
@@ -156,10 +157,11 @@ class ClockSampler:
         os.close(fd)
         try:
             self.out = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
-                stdout=self.out, stderr=subprocess.DEVNULL)
+            cmd = ["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.QUERY}",
+                   "--format=csv,noheader,nounits", "-lms", str(self.period_ms)]
+            if shutil.which("stdbuf"):  # line-buffered, so no sample is lost when it stops
+                cmd = ["stdbuf", "-oL"] + cmd
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
             return
@@ -171,6 +173,7 @@ class ClockSampler:
 
     def stop(self):
         if self.proc is not None:
+            time.sleep(0.3)  # readings lag the GPU by up to ~100 ms: take those after the end
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
