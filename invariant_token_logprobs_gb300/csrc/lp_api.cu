@@ -221,15 +221,14 @@ lp_status lp_merge_partials(const float* const* shard_partials, int n_shards, in
 }
 
 size_t lp_linear_logprob_workspace_size(int64_t T, int64_t d, int64_t V) {
-  (void)d;
-  if (T < 0 || V < 1 || V > lp::kMaxDim) return 0;
+  if (T < 0 || d < 1 || d > lp::kMaxDim || V < 1 || V > lp::kMaxDim) return 0;
   return lp::linear_workspace_bytes(T, d, V, 4);
 }
 
 size_t lp_linear_logprob_partials_workspace_size(int64_t T, int64_t d, int64_t vocab_total,
                                                  int n_shards) {
-  (void)d;
-  if (T < 0 || vocab_total < 1 || vocab_total > lp::kMaxDim) return 0;
+  if (T < 0 || d < 1 || d > lp::kMaxDim || vocab_total < 1 || vocab_total > lp::kMaxDim)
+    return 0;
   if (!(n_shards == 1 || n_shards == 2 || n_shards == 4)) return 0;
   return lp::linear_workspace_bytes(T, d, vocab_total, 4 / n_shards);
 }

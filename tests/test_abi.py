@@ -65,6 +65,7 @@ def test_workspace_sizes(lib):
     assert lp.lp_linear_logprob_workspace_size(5, 60, 1000) == \
         -(-(256 + 4 * t1000 * 5 * 16) // 256) * 256 + 16 * 64 * 2
     assert lp.lp_linear_logprob_workspace_size(-1, 8, 10) == 0
+    assert lp.lp_linear_logprob_workspace_size(5, 0, 10) == 0  # no hidden size
 
 
 def test_logits_argument_errors(lib):
