@@ -72,7 +72,8 @@ def _check_against_oracle(x, gl, ge, tau, gH, gW, rows=None):
 
 @pytest.mark.parametrize("T,d,V,tau", [(64, 256, 8192, 1.0), (37, 72, 1001, 0.7),
                                        (300, 128, 20003, 1.0), (1, 64, 512, 1.6),
-                                       (600, 136, 5003, 1.0), (513, 64, 3000, 0.9)])
+                                       (600, 136, 5003, 1.0), (513, 64, 3000, 0.9),
+                                       (9, 64, 3, 1.0), (20, 72, 1, 1.0)])
 def test_backward_small_against_oracle(T, d, V, tau):
     x = synth.fused_inputs("fused_tiny", device=DEV, T=T, d=d, V=V, seed=T + V)
     gl, ge = _upstream(T, seed=T)
