@@ -75,13 +75,14 @@ def test_hidden_size_not_a_multiple_of_8(T):
     assert e_lp <= FUSED_TOL and e_ent <= FUSED_TOL, (e_lp, e_ent)
 
 
-def test_qwen3_8b_head_full_size_sampled_rows():
+def test_qwen3_8b_head_full_size_all_rows():
+    """The headline shape, every row against the oracle (3.2e11 fp64
+    multiply-adds on the host, a few seconds)."""
     x = synth.fused_inputs("fused_qwen3_8b", device=DEV)
     logp, ent = lp.linear_logprob(x.H, x.W, x.y)
-    rows = torch.tensor([0, 1, 127, 128, 255, 256, 300, 383, 384, 450, 510, 511])
-    ref_lp, ref_ent = oracle_fused(x.H, x.W, x.y, rows)
-    e_lp, e_ent = max_err(logp[rows], ref_lp), max_err(ent[rows], ref_ent)
-    print(f"qwen3-8b head: logp err {e_lp:.3e}, entropy err {e_ent:.3e}")
+    ref_lp, ref_ent = oracle_fused(x.H, x.W, x.y)
+    e_lp, e_ent = max_err(logp, ref_lp), max_err(ent, ref_ent)
+    print(f"qwen3-8b head, all 512 rows: logp err {e_lp:.3e}, entropy err {e_ent:.3e}")
     assert e_lp <= FUSED_TOL and e_ent <= FUSED_TOL
 
 

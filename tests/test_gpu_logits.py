@@ -52,12 +52,11 @@ def test_large_vocabulary_all_rows():
     assert e_lp <= LOGITS_LOGP_TOL and e_ent <= LOGITS_ENT_TOL, (e_lp, e_ent)
 
 
-def test_peaked_workload_full_size_sampled_rows():
+def test_peaked_workload_full_size_all_rows():
     x = synth.logits_inputs("logits_peaked", device=DEV)
     assert x.z.shape == (1024, 151936)
-    rows = torch.arange(0, 1024, 8)
-    logp, ent, e_lp, e_ent = _check(x.z, x.y, rows)
-    print(f"peaked 1024x151936: logp err {e_lp:.3e}, entropy err {e_ent:.3e}")
+    logp, ent, e_lp, e_ent = _check(x.z, x.y)
+    print(f"peaked 1024x151936, all rows: logp err {e_lp:.3e}, entropy err {e_ent:.3e}")
 
 
 def test_near_uniform_rows_within_report_scale():
