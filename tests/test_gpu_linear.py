@@ -216,3 +216,23 @@ def test_empty_batch_and_device_error_word():
     ws = torch.empty(lp.lp_linear_logprob_workspace_size(64, 256, 8192), dtype=torch.uint8, device=DEV)
     lp.linear_logprob(x.H, x.W, x.y, workspace=ws)
     assert lp.lp_get_device_error(ws) == 0
+
+
+def test_one_distinct_result_over_sustained_load():
+    """500 back-to-back calls at the headline shape (~0.2 s of load, long
+    enough for the GPU to reach its power limit and lower its clocks) give one
+    distinct result."""
+    x = synth.fused_inputs("fused_qwen3_8b", device=DEV)
+    T, d = x.H.shape
+    V = x.W.shape[0]
+    ws = torch.empty(lp.lp_linear_logprob_workspace_size(T, d, V), dtype=torch.uint8, device=DEV)
+    ref_lp, ref_ent = lp.linear_logprob(x.H, x.W, x.y, workspace=ws)
+    logp = torch.empty(T, device=DEV)
+    ent = torch.empty(T, device=DEV)
+    mismatches = torch.zeros((), dtype=torch.int64, device=DEV)
+    for _ in range(500):
+        lp.lp_linear_logprob(x.H, x.W, x.y, logp, ent, ws)
+        mismatches += (logp.view(torch.int32) != ref_lp.view(torch.int32)).sum()
+        mismatches += (ent.view(torch.int32) != ref_ent.view(torch.int32)).sum()
+    assert int(mismatches) == 0
+
