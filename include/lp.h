@@ -200,13 +200,18 @@ LP_API lp_status lp_linear_logprob(const void* H, int64_t ld_h, const void* W, i
  *   Limit: the call needs lp_linear_logprob_workspace_size(T, d, V) <= 32 MiB
  *   (at V = 151936 that is T <= 3518 rows); larger calls return
  *   LP_ERR_WORKSPACE_TOO_SMALL before anything is enqueued.
- *   Set-up: the first call on each device looks up the array's device address
- *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.
- *   Sharing: all calls on a device share the array, which keeps the last
+ *   Set-up: the array's device address belongs to the module as loaded into
+ *   one CUDA context.  The first call in each context (each device's primary
+ *   context, a context the caller created, or the primary context re-created
+ *   after cudaDeviceReset) looks it up with cudaGetSymbolAddress and keeps it
+ *   under that context's id; make that first call before any stream capture.
+ *   Sharing: all calls in a context share the array, which keeps the last
  *   call's contents (each call clears what must start at zero).  Calls whose
  *   work can overlap on the GPU, e.g. on two unsynchronised streams, race on
  *   the array: order them on one stream.
+ *   Errors on the device: the error word lives in the hidden array, so
+ *   lp_get_device_error cannot read it; a call whose bounded device-side wait
+ *   gave up shows it as NaN in every logp and entropy it writes.
  */
 LP_API lp_status lp_linear_logprob_noalloc(const void* H, int64_t ld_h, const void* W,
                                            int64_t ld_w, const int64_t* targets, int64_t T,

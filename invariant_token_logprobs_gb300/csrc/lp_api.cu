@@ -6,6 +6,7 @@
 // then the current device (LP_ERR_UNSUPPORTED_DEVICE unless compute capability
 // 10.3).  Nothing is enqueued before all checks pass.  There is no fallback
 // path of any kind: on another device, or without a device, calls fail.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -38,6 +39,33 @@ void timing_events(cudaEvent_t* start, cudaEvent_t* stop) {
   *stop = g_ev_stop.load(std::memory_order_acquire);
 }
 
+namespace {
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <class Fn>
+Fn driver_fn(const char* name) {
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return reinterpret_cast<Fn>(p);
+  cudaGetLastError();
+  return nullptr;
+}
+}  // namespace
+
+uint64_t current_context_id() {
+  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  if (get_current == nullptr || get_id == nullptr) return 0;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return static_cast<uint64_t>(id);
+}
+
 lp_status current_device(Device* dev) {
   int ordinal = 0;
   if (cudaGetDevice(&ordinal) != cudaSuccess) {
@@ -63,6 +91,7 @@ lp_status current_device(Device* dev) {
   if (state != 1) return LP_ERR_UNSUPPORTED_DEVICE;
   dev->ordinal = ordinal;
   dev->sm_count = g_dev_sms[ordinal].load(std::memory_order_relaxed);
+  dev->ctx_id = current_context_id();
   return LP_OK;
 }
 
@@ -265,7 +294,7 @@ lp_status lp_linear_logprob_noalloc(const void* H, int64_t ld_h, const void* W, 
   st = lp::current_device(&dev);
   if (st != LP_OK) return st;
   void* scratch = nullptr;
-  st = lp::static_scratch(dev.ordinal, &scratch);
+  st = lp::static_scratch(&scratch);
   if (st != LP_OK) return st;
   return lp::launch_linear(dev, H, ld_h, W, ld_w, targets, T, d, V, 0, 4, 1.0f, logp_out,
                            entropy_out, nullptr, scratch, static_cast<cudaStream_t>(stream));

@@ -352,13 +352,12 @@ lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a,
                       int64_t N, int64_t ld_b, int64_t K, int n_split, float* C, int64_t ldc,
                       int64_t split_stride, uint32_t* err, cudaStream_t stream,
                       int* n_split_out, bool nb_fastest) {
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = set_pipeline_smem(reinterpret_cast<const void*>(lp_gemm_kernel<kAMn, kBMn>),
+  static PerContextOnce attr;
+  if (attr.run(dev.ctx_id, [] {
+        return set_pipeline_smem(reinterpret_cast<const void*>(lp_gemm_kernel<kAMn, kBMn>),
                                  kGemmSmemBytes - kSmemBytes);
-  });
-  if (attr_err != cudaSuccess) return LP_ERR_CUDA;
+      }) != cudaSuccess)
+    return LP_ERR_CUDA;
   CUtensorMap tmA, tmB;
   const bool okA = kAMn ? encode_bf16_2d(&tmA, A, K, M, ld_a, 64)
                         : encode_bf16_2d(&tmA, A, M, K, ld_a, kBM);
@@ -490,12 +489,11 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
         gh16, T * d, grad_h);
     return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
   }
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = set_pipeline_smem(reinterpret_cast<const void*>(lp_grad_kernel));
-  });
-  if (attr_err != cudaSuccess) return LP_ERR_CUDA;
+  static PerContextOnce attr;
+  if (attr.run(dev.ctx_id, [] {
+        return set_pipeline_smem(reinterpret_cast<const void*>(lp_grad_kernel));
+      }) != cudaSuccess)
+    return LP_ERR_CUDA;
 
   const BackwardLayout L = backward_layout(T, d, V);
   uint8_t* ws = static_cast<uint8_t*>(workspace);

@@ -7,6 +7,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "../../include/lp.h"
 
 namespace lp {
@@ -37,8 +39,43 @@ inline int64_t tiles_per_quarter(int64_t V) {
 struct Device {
   int ordinal;
   int sm_count;
+  uint64_t ctx_id;  // current_context_id() at the time of the call
 };
 lp_status current_device(Device* dev);  // checks compute capability 10.3
+
+// Identifier of the CUDA context current on the calling thread, 0 when none is
+// current or it cannot be read.  Identifiers are unique for the life of the
+// process: the primary context re-created after cudaDeviceReset, or a context
+// the caller created with the driver API, gets a new one.
+uint64_t current_context_id();
+
+// Runs a setter once per CUDA context.  Function attributes (the dynamic
+// shared-memory limit of a kernel) and device addresses of module variables
+// belong to the module as loaded into one context, so they are set or looked
+// up again whenever the calling thread's context is one not seen before.
+// A context id of 0 (unknown) runs the setter every time.
+class PerContextOnce {
+ public:
+  template <class F>
+  cudaError_t run(uint64_t ctx_id, F&& set) {
+    std::lock_guard<std::mutex> lock(mu_);
+    if (ctx_id != 0)
+      for (int i = 0; i < kSlots; ++i)
+        if (ids_[i] == ctx_id) return cudaSuccess;
+    const cudaError_t e = set();
+    if (e == cudaSuccess && ctx_id != 0) {
+      ids_[next_] = ctx_id;
+      next_ = (next_ + 1) % kSlots;
+    }
+    return e;
+  }
+
+ private:
+  static constexpr int kSlots = 16;
+  std::mutex mu_;
+  uint64_t ids_[kSlots] = {};
+  int next_ = 0;
+};
 
 // logits path
 // inv_tau: every logit is multiplied by it first (1.0f: no temperature)
@@ -60,9 +97,10 @@ lp_status launch_linear(const Device& dev, const void* H, int64_t ld_h, const vo
                         float* entropy, float* partials_out, void* workspace,
                         cudaStream_t stream);
 
-// fixed device scratch of the no-alloc fused call
+// fixed device scratch of the no-alloc fused call: its device address in the
+// calling thread's current context
 size_t static_scratch_bytes();
-lp_status static_scratch(int ordinal, void** out);
+lp_status static_scratch(void** out);
 
 // As launch_linear, and when `lse` is not NULL also writes per row the
 // log-sum-exp log Z of the (tempered) logits.

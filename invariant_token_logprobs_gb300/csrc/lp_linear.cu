@@ -402,12 +402,11 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
                               int64_t V_total, int q_first, int n_q, float inv_tau, float* logp,
                               float* entropy, float* partials_out, float* lse,
                               void* workspace, cudaStream_t stream) {
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = set_pipeline_smem(reinterpret_cast<const void*>(lp_linear_kernel));
-  });
-  if (attr_err != cudaSuccess) return LP_ERR_CUDA;
+  static PerContextOnce attr;
+  if (attr.run(dev.ctx_id, [] {
+        return set_pipeline_smem(reinterpret_cast<const void*>(lp_linear_kernel));
+      }) != cudaSuccess)
+    return LP_ERR_CUDA;
 
   const int64_t w_row0 = quarter_begin(V_total, q_first);
   // An empty shard (only possible when V < 4) still maps one row; all of its
@@ -486,26 +485,41 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 
 size_t static_scratch_bytes() { return kStaticScratchBytes; }
 
-// Device address of g_static_scratch on the current device.  In host code the
-// array's name is only a host-side stand-in; the device address comes from
-// cudaGetSymbolAddress, called once per device with that device current (the
-// first no-alloc call on each device does it).
-lp_status static_scratch(int ordinal, void** out) {
-  constexpr int kMaxDev = 64;
+// Device address of g_static_scratch in the calling thread's current context.
+// In host code the array's name is only a host-side stand-in; the device
+// address comes from cudaGetSymbolAddress with the context current.  The
+// address belongs to the module as loaded into that context, so it is cached
+// per context id and looked up again in a context not seen before (another
+// device, a context the caller created, or the primary context re-created after
+// cudaDeviceReset).  The first no-alloc call in each context does the look-up.
+lp_status static_scratch(void** out) {
+  constexpr int kSlots = 16;
   static std::mutex mu;
-  static void* addr[kMaxDev] = {};
-  if (ordinal < 0 || ordinal >= kMaxDev) return LP_ERR_UNSUPPORTED_DEVICE;
+  static uint64_t ids[kSlots] = {};
+  static void* addr[kSlots] = {};
+  static int next = 0;
+  uint64_t ctx = current_context_id();
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[ordinal] == nullptr) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      return LP_ERR_CUDA;
-    }
-    addr[ordinal] = p;
+  if (ctx != 0)
+    for (int i = 0; i < kSlots; ++i)
+      if (ids[i] == ctx) {
+        *out = addr[i];
+        return LP_OK;
+      }
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+  if (e != cudaSuccess || p == nullptr) {
+    cudaGetLastError();
+    return LP_ERR_CUDA;
   }
-  *out = addr[ordinal];
+  // the look-up makes the device's primary context current when none was
+  if (ctx == 0) ctx = current_context_id();
+  if (ctx != 0) {
+    ids[next] = ctx;
+    addr[next] = p;
+    next = (next + 1) % kSlots;
+  }
+  *out = p;
   return LP_OK;
 }
 

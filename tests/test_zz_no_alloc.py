@@ -51,3 +51,42 @@ def test_noalloc_rejects_calls_beyond_its_scratch():
     assert lp.lp_linear_logprob_workspace_size(3519, d, V) > 32 << 20
     st = lib.lp_linear_logprob_noalloc(A, d, A, d, A, 3519, d, V, A, A, None)
     assert st == 4  # LP_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_noalloc_follows_the_current_context():
+    """The scratch array's device address belongs to one CUDA context: a call in
+    another context (a second context on the device, or the primary context
+    re-created after a reset) must look it up again, never reuse a stale one.
+    Run in a child process that drives the device through the driver API only."""
+    import os
+    import subprocess
+    import sys
+    child = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_noalloc_context_child.py")
+    res = subprocess.run([sys.executable, child], capture_output=True, text=True, timeout=300)
+    print(res.stdout)
+    assert res.returncode == 0, res.stdout + res.stderr
+    assert res.stdout.strip().endswith("ok")
+
+
+def test_noalloc_timeout_shows_as_nan_then_recovers():
+    """A no-alloc call whose bounded device-side wait gives up has no workspace
+    for lp_get_device_error to read: its logp and entropy are NaN instead.  The
+    next call on the same context is exact again."""
+    import math
+    lp.load()
+    x = synth.fused_inputs("fused_tiny", device=DEV)
+    T = x.H.shape[0]
+    ref_lp, ref_ent = lp.linear_logprob(x.H, x.W, x.y)
+    logp = torch.empty(T, device=DEV)
+    ent = torch.empty(T, device=DEV)
+    lp.lp_set_fault_injection(1)
+    try:
+        lp.lp_linear_logprob_noalloc(x.H, x.W, x.y, logp, ent)
+        torch.cuda.synchronize()
+    finally:
+        lp.lp_set_fault_injection(0)
+    assert all(math.isnan(v) for v in logp.tolist())
+    assert all(math.isnan(v) for v in ent.tolist())
+    lp.lp_linear_logprob_noalloc(x.H, x.W, x.y, logp, ent)
+    torch.cuda.synchronize()
+    assert torch.equal(bits(logp), bits(ref_lp)) and torch.equal(bits(ent), bits(ref_ent))
