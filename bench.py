@@ -16,9 +16,14 @@ during the timed region, and a secondary line item for the logits-given path
 on the peaked 1024 x 151936 fp32 logits.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lp|reference]
+                       [--tp N]
 For N > 1 launch one process per GPU with torch.distributed.run; every rank
 runs its own batch of rows (weak scaling, no collective on the data path) and
 rank 0 prints the whole-job throughput over the slowest rank's time.
+With --tp N (N = the number of ranks, 2 or 4) the ranks instead split the
+vocabulary: each holds 1/N of W, computes its quarter states, all-gathers them
+over NCCL and merges (vocab parallel, strong scaling: the same 512 rows per
+step whatever N).
 """
 
 from __future__ import annotations
@@ -64,6 +69,9 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-logits", action="store_true", help="skip the logits-path line item")
     p.add_argument("--no-backward", action="store_true", help="skip the backward line item")
+    p.add_argument("--tp", type=int, default=0,
+                   help="vocabulary-parallel ranks, 1, 2 or 4 (must equal the number of "
+                        "processes); 0: the default replica mode")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle baseline sample")
     return p.parse_args(argv)
@@ -326,37 +334,43 @@ def run_lp(args):
     for _ in range(max(3, args.warmup)):
         lp.lp_linear_logprob(x.H, x.W, x.y, logp, ent, ws)
     K = args.steps
-    k_start = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    k_stop = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    for ev in k_start + k_stop:  # torch creates an event on its first record
-        ev.record(stream)
     barrier()
     torch.cuda.synchronize()
     t_begin = time.time()
     torch.cuda.nvtx.range_push("lp.bench.fused_timed")
     ev0.record(stream)
-    for i in range(K):
-        lp.lp_set_kernel_timing_events(k_start[i], k_stop[i])
+    for _ in range(K):
         lp.lp_linear_logprob(x.H, x.W, x.y, logp, ent, ws)
     ev1.record(stream)
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     t_end = time.time()
     barrier()
-    lp.lp_set_kernel_timing_events(None, None)
     sampler.stop()
     clocks = sampler.summary(t_begin, t_end)
     err_word = lp.lp_get_device_error(ws)
     if err_word != 0:
         raise RuntimeError(f"device-side wait gave up (error word {err_word})")
-
     total_ms = max_over(ev0.elapsed_time(ev1))
-    kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(k_start, k_stop))
-    kernel_ms = max_over(kernel_ms)
     ms_per_step = total_ms / K
     value = whole_job_throughput(T, K, world, total_ms)
+
+    # the dominant kernel alone: a second loop of the same length, in which the
+    # library records an event pair around every tensor-core kernel launch
+    k_start = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    k_stop = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for ev in k_start + k_stop:  # torch creates an event on its first record
+        ev.record(stream)
+    torch.cuda.synchronize()
+    for i in range(K):
+        lp.lp_set_kernel_timing_events(k_start[i], k_stop[i])
+        lp.lp_linear_logprob(x.H, x.W, x.y, logp, ent, ws)
+    torch.cuda.synchronize()
+    lp.lp_set_kernel_timing_events(None, None)
+    kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(k_start, k_stop))
+    kernel_ms = max_over(kernel_ms)
 
     flops = 2.0 * T * d * V
     w_bytes = 2.0 * V * d + 2.0 * T * d + 8.0 * T + 8.0 * T
@@ -368,6 +382,8 @@ def run_lp(args):
         "frac": achieved_tf / peak_tf, "traffic": profile_traffic(),
         "frac_vs_sustained": achieved_tf / peaks.get("bf16_tflops_sustained", peak_tf),
         "kernel": "lp_linear_kernel", "kernel_us": kernel_ms * 1e3,
+        "timing": "kernel_us from a second loop of the same length with an event pair around "
+                  "every tensor-core kernel; value and ms_per_step from the plain loop",
         "algorithmic_flops_per_launch": flops, "roofline_us": roofline_us,
         "peak_source": f"{peaks_kind} bf16 burst ({'MEASURED_PEAKS.json' if peaks_kind == 'measured' else 'fallback'})",
     }
@@ -529,9 +545,27 @@ def bench_backward(lp, torch, x, dev, stream, peaks, peaks_kind, max_over, world
     ms = max_over(e0.elapsed_time(e1)) / K
     flops = 3 * 2.0 * T * d * V  # logits recompute, G W, G^T H (forward statistics saved)
     tf = flops / (ms / 1e3) / 1e12
-    del ws, gW
+    del gW
+    # the same call with grad_W in bf16 (lp_linear_logprob_backward_ex)
+    gW16 = torch.empty((V, d), device=dev, dtype=torch.bfloat16)
+    for _ in range(2):
+        lp.lp_linear_logprob_backward_ex(x.H, x.W, x.y, 1.0, lse, ent, gl, ge, gH, gW16, ws)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(K):
+        lp.lp_linear_logprob_backward_ex(x.H, x.W, x.y, 1.0, lse, ent, gl, ge, gH, gW16, ws)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if lp.lp_get_device_error(ws) != 0:
+        raise RuntimeError("device-side wait gave up in the backward")
+    ms16 = max_over(e0.elapsed_time(e1)) / K
+    tf16 = flops / (ms16 / 1e3) / 1e12
+    del ws, gW16
     return {"workload": "fused_qwen3_8b backward (grad_H and grad_W, fp32 out)", "T": T, "d": d,
             "V": V, "value": world * T / (ms / 1e3), "unit": "tokens/s", "us_per_call": ms * 1e3,
+            "bf16_grad_W": {"us_per_call": ms16 * 1e3, "achieved_tflops": tf16,
+                            "frac": tf16 / peaks["bf16_tflops"],
+                            "note": "grad_W written in bf16 (lp_linear_logprob_backward_ex)"},
             "gpu_launches_per_call": 5,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"], "traffic": None,
@@ -571,10 +605,77 @@ def bench_logits(lp, synth, torch, dev, stream, peaks, peaks_kind, max_over, wor
                          "peak_source": f"{peaks_kind} copy bandwidth"}}
 
 
+def run_tp(args):
+    """--tp N: the vocabulary-parallel step (partials on 1/N of W, NCCL
+    all-gather of the 32-byte quarter states, fixed merge) on N ranks."""
+    import torch
+    import torch.distributed as dist
+    from invariant_token_logprobs_gb300 import lp, synth
+    from invariant_token_logprobs_gb300 import vocab_parallel as vp
+
+    world, rank, local = dist_env()
+    if world != args.tp or args.tp not in (1, 2, 4):
+        raise SystemExit(f"--tp {args.tp} needs exactly that many processes (1, 2 or 4); got {world}")
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lp.load()
+    x = synth.fused_inputs(WORKLOAD, device=dev)  # every rank: the same rows
+    T, d = x.H.shape
+    V = x.W.shape[0]
+    _, n, b, e = vp.shard_of_rank(V)
+    w_shard = x.W[b:e].clone()
+    del x.W
+    ws = torch.empty(lp.lp_linear_logprob_partials_workspace_size(T, d, V, n), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        return vp.vocab_parallel_linear_logprob(x.H, w_shard, x.y, V, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    K = args.steps
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(K):
+        out = step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    line = {
+        "metric": METRIC, "value": T * K / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms / K, "higher_is_better": True,
+        "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded bf16 H (RMS-normalised N(0,1)) and W ~ N(0, 0.02^2), uniform targets",
+        "config": {"workload": WORKLOAD, "T": T, "d": d, "V": V, "seed": 2,
+                   "parallelism": f"vocab-parallel tp{world} (1/{world} of W per rank, all-gather "
+                                  f"of quarter states, fixed merge)",
+                   "l2": "inputs larger than L2, no flush"},
+        "gpu_launches": 3 * K, "e2e": None, "roofline": None, "cpu_baseline": None,
+        "backend": lp.lp_backend_id(),
+        "logp_checksum": float(out[0].double().sum()),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.tp:
+        return run_tp(args)
     return run_lp(args)
 
 

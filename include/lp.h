@@ -119,12 +119,14 @@ LP_API lp_status lp_vocab_shard_range(int64_t vocab_total, int shard_index, int 
  *   targets      [T] int64 GLOBAL token ids.
  *   vocab_total  V of the unsharded vocabulary.
  *   shard_index, n_shards: which shard (n_shards in {1, 2, 4}).
- *   partials_out [T][4 / n_shards][4] float32 (16-byte aligned): for each row
- *                and quarter of the shard, the state (m, s, u, t): the
- *                quarter's maximum logit m, s = sum exp(z - m),
- *                u = sum exp(z - m) (z - m), and the target logit t (-inf when
- *                the target is not in this quarter, NaN when the target is
- *                outside [0, vocab_total)).
+ *   partials_out [T][4 / n_shards][8] float32 (16-byte aligned): for each row
+ *                and quarter of the shard, the 32-byte state
+ *                (m, s_hi, s_lo, u, t, tau, 0, 0) of the distribution
+ *                softmax(z / tau) (tau = 1 here): the quarter's maximum raw
+ *                logit m; s = s_hi + s_lo = sum exp((z - m) / tau), held as an
+ *                unevaluated float pair; u = sum exp((z - m) / tau) (z - m) / tau;
+ *                the raw target logit t (-inf when the target is not in this
+ *                quarter, NaN when it is outside [0, vocab_total)); and tau.
  */
 LP_API lp_status lp_logprob_partials_from_logits(const float* logits_shard, int64_t ld_logits,
                                           const int64_t* targets, int64_t T,
@@ -137,10 +139,14 @@ LP_API lp_status lp_logprob_partials_from_logits(const float* logits_shard, int6
  * order (Q0 + Q1) + (Q2 + Q3) and finalise logp and entropy.
  *
  *   shard_partials  HOST array of n_shards DEVICE pointers, in shard order;
- *                   element i is shard i's partials_out ([T][4 / n_shards][4]
+ *                   element i is shard i's partials_out ([T][4 / n_shards][8]
  *                   float32, 16-byte aligned) from either partials entry point.
  *   n_shards        1, 2 or 4.
  *   logp_out        [T] float32; entropy_out [T] float32 or NULL.
+ * The four states of a row are rebased to the row's largest m in float64,
+ * summed as (Q0 + Q1) + (Q2 + Q3), and logp = (t - M) / tau - log S,
+ * entropy = log S - U / S formed in float64 and rounded once.  A row whose
+ * states carry different tau gives NaN.
  */
 LP_API lp_status lp_merge_partials(const float* const* shard_partials, int n_shards,
                             int64_t T, float* logp_out, float* entropy_out,
@@ -250,13 +256,17 @@ LP_API lp_status lp_linear_logprob_partials(const void* H, int64_t ld_h, const v
  * temperature 0.7 (h100-pcp.json, section "scope"); these return the
  * log-probability and entropy of the tempered distribution.
  *
- * Each logit is scaled as fl(z * fl(1 / tau)) in float32 before any other
- * step, so every invariance above holds for a fixed tau, and tau == 1 gives
- * exactly the bits of the unscaled entry points.  temperature must be finite
- * and > 0 with 1/tau a finite positive float, else LP_ERR_INVALID_ARGUMENT.
- * All other arguments are those of the unscaled entry point of the same name;
- * partial states from the *_partials_temperature calls merge with
- * lp_merge_partials (only states of one tau may be merged together).
+ * No logit is rounded after scaling: maxima are taken over the raw logits,
+ * each difference z - m is multiplied by 1/tau (on the logits path as the
+ * float pair fl(1/tau) + fl(1/tau - fl(1/tau)); on the fused path by
+ * fl(1/tau)) before its exponential, and the target enters as (t - M) / tau
+ * formed in float64.  Every invariance above holds for a fixed tau, and
+ * tau == 1 gives exactly the bits of the unscaled entry points.  temperature
+ * must be finite and > 0 with 1/tau a finite positive float, else
+ * LP_ERR_INVALID_ARGUMENT.  All other arguments are those of the unscaled
+ * entry point of the same name; partial states from the *_partials_temperature
+ * calls carry tau and merge with lp_merge_partials (a row whose states carry
+ * different tau gives NaN).
  * ------------------------------------------------------------------------ */
 
 LP_API lp_status lp_logprob_from_logits_temperature(const float* logits, int64_t ld_logits,
@@ -305,7 +315,8 @@ LP_API size_t lp_linear_logprob_backward_workspace_size(int64_t T, int64_t d, in
 
 /*
  * lp_linear_logprob_lse: lp_linear_logprob_temperature that also writes, per
- * row, lse_out[t] = log sum_v exp(z[t, v] / tau) (float32 [T]).  Keep lse_out
+ * row, lse_out[t] = log sum_v exp(z[t, v] / tau) (float32 [T], formed as
+ * M / tau + log S in float64 and rounded once).  Keep lse_out
  * and entropy_out from the forward pass and hand them to the backward to skip
  * its forward recomputation.  All three outputs are required.
  */
@@ -341,6 +352,33 @@ LP_API lp_status lp_linear_logprob_backward(const void* H, int64_t ld_h, const v
                                             const float* grad_logp, const float* grad_entropy,
                                             float* grad_H, float* grad_W, void* workspace,
                                             size_t workspace_bytes, void* stream);
+
+/* Element type of grad_W for lp_linear_logprob_backward_ex. */
+typedef enum lp_grad_w_dtype {
+  LP_GRAD_W_FLOAT32 = 0,  /* float32 [V, d] */
+  LP_GRAD_W_BFLOAT16 = 1  /* bfloat16 [V, d], each element the float32 result rounded to
+                             nearest even */
+} lp_grad_w_dtype;
+
+/*
+ * lp_linear_logprob_backward_ex: lp_linear_logprob_backward with the element
+ * type of grad_W chosen by grad_W_dtype (an lp_grad_w_dtype).  With
+ * LP_GRAD_W_BFLOAT16, grad_W is [V, d] bfloat16 (dense rows, 16-byte aligned):
+ * the same float32 products rounded once to bf16 on the way out, which halves
+ * the product's 4 V d bytes of output (the trainer of the RL-Kernel H100 PCP
+ * evidence record keeps bf16 weights; its fp32 main gradients can accumulate
+ * these).  If a device-side wait gives up, the bf16 output is NaN too.  Other
+ * arguments as in lp_linear_logprob_backward; an unknown dtype gives
+ * LP_ERR_INVALID_ARGUMENT.
+ */
+LP_API lp_status lp_linear_logprob_backward_ex(const void* H, int64_t ld_h, const void* W,
+                                               int64_t ld_w, const int64_t* targets, int64_t T,
+                                               int64_t d, int64_t V, float temperature,
+                                               const float* saved_lse, const float* saved_entropy,
+                                               const float* grad_logp, const float* grad_entropy,
+                                               float* grad_H, void* grad_W, int grad_W_dtype,
+                                               void* workspace, size_t workspace_bytes,
+                                               void* stream);
 
 /* ------------------------------------------------------------------------
  * Diagnostics and tuning.
@@ -385,10 +423,26 @@ LP_API lp_status lp_set_kernel_timing_events(void* start_event, void* stop_event
  */
 LP_API lp_status lp_set_fault_injection(int mode);
 
+/*
+ * lp_get_check_word: the index checks of the checked build.  A library built
+ * with -DLP_CHECKED (lp_backend_id() then ends in "+checked") tests, in every
+ * kernel, the indexes and TMA coordinates it computes against the extents
+ * derived from the call's arguments; a failed test skips the access and sets
+ * a bit of a check word instead of faulting (bit 0 logit read outside its
+ * quarter, 1 row outside [0, T), 2 quarter or tile state outside its buffer,
+ * 3 negative TMA load coordinate, 4 store of G outside its buffer, 5 output
+ * box outside C, 6 split-sum index, 7 padding or row-copy index).  This call
+ * synchronises the device, writes the OR of the check words of every kernel
+ * since the previous call to *word_out and clears them.  In the normal build
+ * the word is always 0.  LP_ERR_CUDA if the read failed.
+ */
+LP_API lp_status lp_get_check_word(uint32_t* word_out);
+
 /* Human-readable name of a status code (static storage). */
 LP_API const char* lp_status_string(lp_status status);
 
-/* Fixed identifier of this backend, "lp.sm103a.bitwise.v1". */
+/* Fixed identifier of this backend, "lp.sm103a.bitwise.v1" ("+checked"
+ * appended in the checked build). */
 LP_API const char* lp_backend_id(void);
 
 #ifdef __cplusplus

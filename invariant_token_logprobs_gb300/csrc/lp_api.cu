@@ -12,6 +12,7 @@
 #include <atomic>
 #include <cstdint>
 
+#include "lp_check.cuh"
 #include "lp_device.cuh"
 #include "lp_internal.h"
 
@@ -97,14 +98,19 @@ lp_status current_device(Device* dev) {
 
 namespace {
 
-// 1/tau rounded to float; false unless tau is finite and > 0 and 1/tau is a
-// finite positive float.
-bool inverse_temperature(float temperature, float* inv) {
+// The temperature arguments of a call: false unless tau is finite and > 0 and
+// 1/tau is a finite positive float.  1/tau is split into inv_hi = fl(1/tau)
+// and inv_lo = fl(1/tau - inv_hi), both from float64.
+bool make_tau(float temperature, TauArgs* out) {
   if (!(temperature > 0.0f) || !(temperature < 3.402823466e38f)) return false;
   const double r = 1.0 / static_cast<double>(temperature);
   if (!(r > 0.0) || r > 3.402823466e38) return false;
-  *inv = static_cast<float>(r);
-  return *inv > 0.0f;
+  const float hi = static_cast<float>(r);
+  if (!(hi > 0.0f) || !(hi < 3.402823466e38f)) return false;
+  out->tau = temperature;
+  out->inv_hi = hi;
+  out->inv_lo = static_cast<float>(r - static_cast<double>(hi));
+  return true;
 }
 
 lp_status check_shard(int shard_index, int n_shards) {
@@ -145,7 +151,27 @@ const char* lp_status_string(lp_status status) {
   return "LP_ERR_UNKNOWN";
 }
 
-const char* lp_backend_id(void) { return "lp.sm103a.bitwise.v1"; }
+const char* lp_backend_id(void) {
+  return lp::kChecked ? "lp.sm103a.bitwise.v1+checked" : "lp.sm103a.bitwise.v1";
+}
+
+lp_status lp_get_check_word(uint32_t* word_out) {
+  if (word_out == nullptr) return LP_ERR_INVALID_ARGUMENT;
+  *word_out = 0;
+  lp::Device dev;
+  const lp_status st = lp::current_device(&dev);
+  if (st != LP_OK) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return LP_ERR_CUDA;
+  uint32_t a = 0, b = 0, c = 0;
+  if (lp::take_check_word_logits(&a) != cudaSuccess ||
+      lp::take_check_word_linear(&b) != cudaSuccess ||
+      lp::take_check_word_backward(&c) != cudaSuccess) {
+    cudaGetLastError();
+    return LP_ERR_CUDA;
+  }
+  *word_out = a | b | c;
+  return LP_OK;
+}
 
 lp_status lp_set_persistent_grid_limit(int max_ctas) {
   if (max_ctas < 0) return LP_ERR_INVALID_ARGUMENT;
@@ -183,8 +209,8 @@ lp_status lp_logprob_from_logits_temperature(const float* logits, int64_t ld_log
                                              const int64_t* targets, int64_t T, int64_t V,
                                              float temperature, float* logp_out,
                                              float* entropy_out, void* stream) {
-  float inv_tau;
-  if (!lp::inverse_temperature(temperature, &inv_tau)) return LP_ERR_INVALID_ARGUMENT;
+  lp::TauArgs tau;
+  if (!lp::make_tau(temperature, &tau)) return LP_ERR_INVALID_ARGUMENT;
   if (T < 0 || T > lp::kMaxDim / 4 || V < 1 || V > lp::kMaxDim || ld_logits < V)
     return LP_ERR_INVALID_ARGUMENT;
   if (T == 0) return LP_OK;
@@ -196,7 +222,7 @@ lp_status lp_logprob_from_logits_temperature(const float* logits, int64_t ld_log
   lp::Device dev;
   const lp_status st = lp::current_device(&dev);
   if (st != LP_OK) return st;
-  return lp::launch_logits_final(logits, ld_logits, targets, T, V, inv_tau, logp_out,
+  return lp::launch_logits_final(logits, ld_logits, targets, T, V, tau, logp_out,
                                  entropy_out, static_cast<cudaStream_t>(stream));
 }
 
@@ -206,8 +232,8 @@ lp_status lp_logprob_partials_from_logits_temperature(const float* logits_shard,
                                                       int shard_index, int n_shards,
                                                       float temperature, float* partials_out,
                                                       void* stream) {
-  float inv_tau;
-  if (!lp::inverse_temperature(temperature, &inv_tau)) return LP_ERR_INVALID_ARGUMENT;
+  lp::TauArgs tau;
+  if (!lp::make_tau(temperature, &tau)) return LP_ERR_INVALID_ARGUMENT;
   lp_status st = lp::check_shard(shard_index, n_shards);
   if (st != LP_OK) return st;
   if (T < 0 || T > lp::kMaxDim / 4 || vocab_total < 1 || vocab_total > lp::kMaxDim)
@@ -228,7 +254,7 @@ lp_status lp_logprob_partials_from_logits_temperature(const float* logits_shard,
   int q_first, n_q;
   lp::shard_quarters(shard_index, n_shards, q_first, n_q);
   return lp::launch_logits_partials(logits_shard, ld_logits, targets, T, vocab_total, q_first,
-                                    n_q, inv_tau, partials_out, static_cast<cudaStream_t>(stream));
+                                    n_q, tau, partials_out, static_cast<cudaStream_t>(stream));
 }
 
 lp_status lp_merge_partials(const float* const* shard_partials, int n_shards, int64_t T,
@@ -266,8 +292,8 @@ lp_status lp_linear_logprob_temperature(const void* H, int64_t ld_h, const void*
                                         const int64_t* targets, int64_t T, int64_t d, int64_t V,
                                         float temperature, float* logp_out, float* entropy_out,
                                         void* workspace, size_t workspace_bytes, void* stream) {
-  float inv_tau;
-  if (!lp::inverse_temperature(temperature, &inv_tau)) return LP_ERR_INVALID_ARGUMENT;
+  lp::TauArgs tau;
+  if (!lp::make_tau(temperature, &tau)) return LP_ERR_INVALID_ARGUMENT;
   lp_status st = lp::check_fused_args(H, ld_h, W, ld_w, targets, T, d, V);
   if (st != LP_OK || T == 0) return st;
   if (logp_out == nullptr || workspace == nullptr) return LP_ERR_INVALID_ARGUMENT;
@@ -277,7 +303,7 @@ lp_status lp_linear_logprob_temperature(const void* H, int64_t ld_h, const void*
   lp::Device dev;
   st = lp::current_device(&dev);
   if (st != LP_OK) return st;
-  return lp::launch_linear(dev, H, ld_h, W, ld_w, targets, T, d, V, 0, 4, inv_tau, logp_out,
+  return lp::launch_linear(dev, H, ld_h, W, ld_w, targets, T, d, V, 0, 4, tau, logp_out,
                            entropy_out, nullptr, workspace, static_cast<cudaStream_t>(stream));
 }
 
@@ -296,7 +322,9 @@ lp_status lp_linear_logprob_noalloc(const void* H, int64_t ld_h, const void* W, 
   void* scratch = nullptr;
   st = lp::static_scratch(&scratch);
   if (st != LP_OK) return st;
-  return lp::launch_linear(dev, H, ld_h, W, ld_w, targets, T, d, V, 0, 4, 1.0f, logp_out,
+  lp::TauArgs tau;
+  lp::make_tau(1.0f, &tau);
+  return lp::launch_linear(dev, H, ld_h, W, ld_w, targets, T, d, V, 0, 4, tau, logp_out,
                            entropy_out, nullptr, scratch, static_cast<cudaStream_t>(stream));
 }
 
@@ -305,8 +333,8 @@ lp_status lp_linear_logprob_lse(const void* H, int64_t ld_h, const void* W, int6
                                 float temperature, float* logp_out, float* entropy_out,
                                 float* lse_out, void* workspace, size_t workspace_bytes,
                                 void* stream) {
-  float inv_tau;
-  if (!lp::inverse_temperature(temperature, &inv_tau)) return LP_ERR_INVALID_ARGUMENT;
+  lp::TauArgs tau;
+  if (!lp::make_tau(temperature, &tau)) return LP_ERR_INVALID_ARGUMENT;
   lp_status st = lp::check_fused_args(H, ld_h, W, ld_w, targets, T, d, V);
   if (st != LP_OK || T == 0) return st;
   if (logp_out == nullptr || entropy_out == nullptr || lse_out == nullptr || workspace == nullptr)
@@ -318,7 +346,7 @@ lp_status lp_linear_logprob_lse(const void* H, int64_t ld_h, const void* W, int6
   lp::Device dev;
   st = lp::current_device(&dev);
   if (st != LP_OK) return st;
-  return lp::launch_linear_stats(dev, H, ld_h, W, ld_w, targets, T, d, V, 0, 4, inv_tau, logp_out,
+  return lp::launch_linear_stats(dev, H, ld_h, W, ld_w, targets, T, d, V, 0, 4, tau, logp_out,
                                  entropy_out, nullptr, lse_out, workspace,
                                  static_cast<cudaStream_t>(stream));
 }
@@ -330,8 +358,8 @@ lp_status lp_linear_logprob_partials_temperature(const void* H, int64_t ld_h,
                                                  int n_shards, float temperature,
                                                  float* partials_out, void* workspace,
                                                  size_t workspace_bytes, void* stream) {
-  float inv_tau;
-  if (!lp::inverse_temperature(temperature, &inv_tau)) return LP_ERR_INVALID_ARGUMENT;
+  lp::TauArgs tau;
+  if (!lp::make_tau(temperature, &tau)) return LP_ERR_INVALID_ARGUMENT;
   lp_status st = lp::check_shard(shard_index, n_shards);
   if (st != LP_OK) return st;
   st = lp::check_fused_args(H, ld_h, W_shard, ld_w, targets, T, d, vocab_total);
@@ -346,7 +374,7 @@ lp_status lp_linear_logprob_partials_temperature(const void* H, int64_t ld_h,
   st = lp::current_device(&dev);
   if (st != LP_OK) return st;
   return lp::launch_linear(dev, H, ld_h, W_shard, ld_w, targets, T, d, vocab_total, q_first, n_q,
-                           inv_tau, nullptr, nullptr, partials_out, workspace,
+                           tau, nullptr, nullptr, partials_out, workspace,
                            static_cast<cudaStream_t>(stream));
 }
 
@@ -389,14 +417,17 @@ size_t lp_linear_logprob_backward_workspace_size(int64_t T, int64_t d, int64_t V
   return lp::linear_backward_workspace_bytes(T, d, V);
 }
 
-lp_status lp_linear_logprob_backward(const void* H, int64_t ld_h, const void* W, int64_t ld_w,
-                                     const int64_t* targets, int64_t T, int64_t d, int64_t V,
-                                     float temperature, const float* saved_lse,
-                                     const float* saved_entropy, const float* grad_logp,
-                                     const float* grad_entropy, float* grad_H, float* grad_W,
-                                     void* workspace, size_t workspace_bytes, void* stream) {
-  float inv_tau;
-  if (!lp::inverse_temperature(temperature, &inv_tau)) return LP_ERR_INVALID_ARGUMENT;
+lp_status lp_linear_logprob_backward_ex(const void* H, int64_t ld_h, const void* W, int64_t ld_w,
+                                        const int64_t* targets, int64_t T, int64_t d, int64_t V,
+                                        float temperature, const float* saved_lse,
+                                        const float* saved_entropy, const float* grad_logp,
+                                        const float* grad_entropy, float* grad_H, void* grad_W,
+                                        int grad_W_dtype, void* workspace, size_t workspace_bytes,
+                                        void* stream) {
+  lp::TauArgs tau;
+  if (!lp::make_tau(temperature, &tau)) return LP_ERR_INVALID_ARGUMENT;
+  if (grad_W_dtype != LP_GRAD_W_FLOAT32 && grad_W_dtype != LP_GRAD_W_BFLOAT16)
+    return LP_ERR_INVALID_ARGUMENT;
   lp_status st = lp::check_fused_args(H, ld_h, W, ld_w, targets, T, d, V);
   if (st != LP_OK || T == 0) return st;
   if (grad_H == nullptr || workspace == nullptr) return LP_ERR_INVALID_ARGUMENT;
@@ -412,9 +443,21 @@ lp_status lp_linear_logprob_backward(const void* H, int64_t ld_h, const void* W,
   lp::Device dev;
   st = lp::current_device(&dev);
   if (st != LP_OK) return st;
-  return lp::launch_linear_backward(dev, H, ld_h, W, ld_w, targets, T, d, V, inv_tau, saved_lse,
+  return lp::launch_linear_backward(dev, H, ld_h, W, ld_w, targets, T, d, V, tau, saved_lse,
                                     saved_entropy, grad_logp, grad_entropy, grad_H, grad_W,
-                                    workspace, static_cast<cudaStream_t>(stream));
+                                    grad_W_dtype == LP_GRAD_W_BFLOAT16, workspace,
+                                    static_cast<cudaStream_t>(stream));
+}
+
+lp_status lp_linear_logprob_backward(const void* H, int64_t ld_h, const void* W, int64_t ld_w,
+                                     const int64_t* targets, int64_t T, int64_t d, int64_t V,
+                                     float temperature, const float* saved_lse,
+                                     const float* saved_entropy, const float* grad_logp,
+                                     const float* grad_entropy, float* grad_H, float* grad_W,
+                                     void* workspace, size_t workspace_bytes, void* stream) {
+  return lp_linear_logprob_backward_ex(H, ld_h, W, ld_w, targets, T, d, V, temperature, saved_lse,
+                                       saved_entropy, grad_logp, grad_entropy, grad_H, grad_W,
+                                       LP_GRAD_W_FLOAT32, workspace, workspace_bytes, stream);
 }
 
 lp_status lp_get_device_error(const void* workspace, size_t workspace_bytes, uint32_t* word_out,

@@ -32,6 +32,7 @@
 
 #include <mutex>
 
+#include "lp_check.cuh"
 #include "lp_device.cuh"
 #include "lp_internal.h"
 #include "lp_tcgen05.cuh"
@@ -111,7 +112,6 @@ struct GradEpilogue {
       const int64_t yl64 = y - c0;
       if (y_ok && yl64 >= 0 && yl64 < valid) yl = static_cast<int>(yl64);
     }
-    const float lzL = __fmul_rn(log_z, kLog2e);
     const float scale = a->inv_tau;
 #pragma unroll 1
     for (int p = 0; p < kBN / 64; ++p) {
@@ -127,7 +127,7 @@ struct GradEpilogue {
         for (int h = 0; h < 2; ++h) {
           const float zs = __fmul_rn(v[i + h], scale);                   // z / tau
           const float lp = __fsub_rn(zs, log_z);                         // log p
-          const float pr = exp2_approx(__fmaf_rn(zs, kLog2e, -lzL));     // p
+          const float pr = exp_fast(lp);                                 // p
           // -p (g_logp + g_ent (log p + entropy)) + g_logp [v == y], then / tau
           float g = -__fmul_rn(pr, __fmaf_rn(ge, __fadd_rn(lp, ent), gl));
           if (p * 64 + i + h == yl) g = __fadd_rn(g, gl);
@@ -138,6 +138,7 @@ struct GradEpilogue {
       }
       const int n = min(64, valid - p * 64);
       const int64_t col0 = c0 + p * 64;
+      if (!LP_CHECK(row < a->T && col0 >= 0 && col0 + n <= a->ld_g, kChkGStore)) continue;
       __nv_bfloat16* grow = a->G + row * a->ld_g + col0;
       if (n == 64 && ((reinterpret_cast<uintptr_t>(grow) & 15u) == 0)) {
 #pragma unroll
@@ -204,11 +205,14 @@ struct GemmArgs {
   CUtensorMap tmC;  // bulk-store map of C
   int64_t M;
   int64_t N;
+  int n_split;      // matrices of C (split products)
   uint32_t* err;
+  int out_bf16;     // C is bf16 (32 x 64 boxes) instead of fp32 (32 x 32 boxes)
 };
 
 // Epilogue of the products.  Each warp owns 32 rows of the tile and writes
-// them in 32 x 32 boxes: a box is staged in shared memory with the 128-byte
+// them in boxes of 32 rows x 128 bytes (32 fp32 columns, or 64 bf16 columns
+// rounded to nearest even): a box is staged in shared memory with the 128-byte
 // swizzle of C's store map (16-byte chunk c of row r at chunk c ^ (r % 8)), and
 // one lane issues its TMA bulk store.  The warp's two staging buffers
 // alternate, one per store, each reused once the store that last read it has
@@ -249,6 +253,31 @@ struct GemmEpilogue {
       float v[64];
       __syncwarp();
       tmem_load64(taddr + static_cast<uint32_t>(p * 64), v);
+      if (a->out_bf16) {
+        // the 64 columns of this piece as one box of 32 rows x 64 bf16
+        float* box = stg + next * kBoxFloats;
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kBoxes - 1) : "memory");
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t w[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * c + 2 * h], v[8 * c + 2 * h + 1]);
+            w[h] = *reinterpret_cast<const uint32_t*>(&b2);
+          }
+          *reinterpret_cast<uint4*>(box + lane * 32 + ((c ^ (lane & 7)) * 4)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0 && LP_CHECK(n0 + p * 64 < a->N && row0 < a->M && s >= 0 &&
+                                      s < a->n_split, kChkOutBox))
+          bulk_store_3d(&a->tmC, static_cast<int>(n0 + p * 64), static_cast<int>(row0), s,
+                        smem_u32(box));
+        if (++next == kBoxes) next = 0;
+        continue;
+      }
 #pragma unroll
       for (int b = 0; b < 2; ++b) {
         const int64_t col = n0 + p * 64 + b * 32;
@@ -265,7 +294,8 @@ struct GemmEpilogue {
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0)
+        if (lane == 0 && LP_CHECK(col < a->N && row0 < a->M && s >= 0 && s < a->n_split,
+                                  kChkOutBox))
           bulk_store_3d(&a->tmC, static_cast<int>(col), static_cast<int>(row0), s, smem_u32(box));
         if (++next == kBoxes) next = 0;
       }
@@ -300,7 +330,9 @@ __global__ void lp_split_sum_kernel(const float4* __restrict__ part, int64_t n4,
     float4 x[kSplitsDH];
 #pragma unroll
     for (int k = 0; k < kSplitsDH; ++k)
-      if (k < n_split) x[k] = part[k * n4 + i];
+      if (k < n_split)
+        x[k] = LP_CHECK(n_split <= kSplitsDH, kChkSplitIndex) ? part[k * n4 + i]
+                                                              : make_float4(0.f, 0.f, 0.f, 0.f);
     float4 s = x[0];
 #pragma unroll
     for (int k = 1; k < kSplitsDH; ++k) {
@@ -323,6 +355,15 @@ __global__ void lp_poison_kernel(const uint32_t* __restrict__ err, float* __rest
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
     out[i] = quiet_nan();
+}
+
+// The same for a bf16 output (NaN = 0x7fc0).
+__global__ void lp_poison_bf16_kernel(const uint32_t* __restrict__ err, uint16_t* __restrict__ out,
+                                      int64_t n) {
+  if ((err[0] | err[1] | err[2] | err[3]) == 0u) return;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    out[i] = 0x7fc0u;
 }
 
 struct BackwardLayout {
@@ -349,9 +390,9 @@ BackwardLayout backward_layout(int64_t T, int64_t d, int64_t V) {
 // with kAMn, [K, M] (M contiguous); B likewise with N.
 template <bool kAMn, bool kBMn>
 lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a, const void* B,
-                      int64_t N, int64_t ld_b, int64_t K, int n_split, float* C, int64_t ldc,
+                      int64_t N, int64_t ld_b, int64_t K, int n_split, void* C, int64_t ldc,
                       int64_t split_stride, uint32_t* err, cudaStream_t stream,
-                      int* n_split_out, bool nb_fastest) {
+                      int* n_split_out, bool nb_fastest, bool out_bf16 = false) {
   static PerContextOnce attr;
   if (attr.run(dev.ctx_id, [] {
         return set_pipeline_smem(reinterpret_cast<const void*>(lp_gemm_kernel<kAMn, kBMn>),
@@ -380,7 +421,11 @@ lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a,
   g.M = M;
   g.N = N;
   g.err = err;
-  if (!encode_f32_3d_store(&g.tmC, C, n_split, M, N, ldc, split_stride)) return LP_ERR_CUDA;
+  g.n_split = n_split;
+  g.out_bf16 = out_bf16 ? 1 : 0;
+  const bool ok_c = out_bf16 ? encode_bf16_3d_store(&g.tmC, C, n_split, M, N, ldc, split_stride)
+                             : encode_f32_3d_store(&g.tmC, C, n_split, M, N, ldc, split_stride);
+  if (!ok_c) return LP_ERR_CUDA;
   lp_gemm_kernel<kAMn, kBMn>
       <<<pair_grid(dev.sm_count, total), kThreads, kGemmSmemBytes, stream>>>(tmA, tmB, g);
   return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
@@ -431,7 +476,8 @@ __global__ void lp_pad_backward_kernel(const uint16_t* __restrict__ H, int64_t l
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t r = i / d16, c = i % d16;
-    H_out[i] = r < T ? load_row_chunk(H + r * ld_h, d, c) : make_uint4(0u, 0u, 0u, 0u);
+    if (LP_CHECK(c * 8 < ld_h, kChkCopyIndex))
+      H_out[i] = r < T ? load_row_chunk(H + r * ld_h, d, c) : make_uint4(0u, 0u, 0u, 0u);
   }
   if (blockIdx.x == 0 && threadIdx.x < kSmallRows) {
     const int r = threadIdx.x;
@@ -461,10 +507,10 @@ size_t linear_backward_workspace_bytes(int64_t T, int64_t d, int64_t V) {
 
 lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h, const void* W,
                                  int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
-                                 int64_t V, float inv_tau, const float* saved_lse,
+                                 int64_t V, const TauArgs& tau, const float* saved_lse,
                                  const float* saved_entropy, const float* g_logp,
-                                 const float* g_ent, float* grad_h, float* grad_w,
-                                 void* workspace, cudaStream_t stream) {
+                                 const float* g_ent, float* grad_h, void* grad_w,
+                                 bool grad_w_bf16, void* workspace, cudaStream_t stream) {
   if (T > 0 && T < kSmallRows) {
     const SmallLayout S = small_layout(d, V);
     uint8_t* base = static_cast<uint8_t*>(workspace);
@@ -482,8 +528,8 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
                                        ge16, lse16, ent16);
     if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
     const lp_status st =
-        launch_linear_backward(dev, h16, d8, W, ld_w, y16, kSmallRows, d, V, inv_tau, lse16,
-                               ent16, gl16, ge16, gh16, grad_w, workspace, stream);
+        launch_linear_backward(dev, h16, d8, W, ld_w, y16, kSmallRows, d, V, tau, lse16,
+                               ent16, gl16, ge16, gh16, grad_w, grad_w_bf16, workspace, stream);
     if (st != LP_OK) return st;
     lp_copy_rows_kernel<<<static_cast<unsigned>((T * d + 255) / 256), 256, 0, stream>>>(
         gh16, T * d, grad_h);
@@ -507,7 +553,7 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
   if (lse == nullptr || ent == nullptr) {
     float* lse_ws = reinterpret_cast<float*>(ws + L.off_lse);
     float* ent_ws = reinterpret_cast<float*>(ws + L.off_ent);
-    lp_status st0 = launch_linear_stats(dev, H, ld_h, W, ld_w, targets, T, d, V, 0, 4, inv_tau,
+    lp_status st0 = launch_linear_stats(dev, H, ld_h, W, ld_w, targets, T, d, V, 0, 4, tau,
                                         reinterpret_cast<float*>(ws + L.off_logp), ent_ws,
                                         nullptr, lse_ws, workspace, stream);
     if (st0 != LP_OK) return st0;
@@ -541,7 +587,7 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
     g.G = G;
     g.err = err + 1;
     g.ld_g = L.V8;
-    g.inv_tau = inv_tau;
+    g.inv_tau = tau.inv_hi;
     g.T = static_cast<int>(T);
     lp_grad_kernel<<<pair_grid(dev.sm_count, total), kThreads, kSmemBytes, stream>>>(tmA, tmB, g);
     if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
@@ -563,12 +609,19 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
   if (grad_w != nullptr) {
     // column blocks fastest: a block of G is used by 16 consecutive units
     st = launch_gemm<true, true>(dev, G, V, L.V8, H, d, ld_h, T, 1, grad_w, d, 0, err + 3, stream,
-                                 nullptr, true);
+                                 nullptr, true, grad_w_bf16);
     if (st != LP_OK) return st;
-    lp_poison_kernel<<<dev.sm_count * 4, 256, 0, stream>>>(err, grad_w, V * d);
+    if (grad_w_bf16)
+      lp_poison_bf16_kernel<<<dev.sm_count * 4, 256, 0, stream>>>(
+          err, static_cast<uint16_t*>(grad_w), V * d);
+    else
+      lp_poison_kernel<<<dev.sm_count * 4, 256, 0, stream>>>(err, static_cast<float*>(grad_w),
+                                                            V * d);
     if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
   }
   return LP_OK;
 }
+
+cudaError_t take_check_word_backward(uint32_t* out) { return take_check_word(out); }
 
 }  // namespace lp

@@ -1,18 +1,26 @@
 // lp_device.cuh: arithmetic shared by every kernel of liblp.
 //
-// The per-row state of a slice of the vocabulary is (m, s, u, t):
-//   m  the slice's maximum logit,
-//   s  sum over the slice of exp(z - m),
-//   u  sum over the slice of exp(z - m) * (z - m),
-//   t  the target logit z[y] when y lies in the slice, -inf when it does not,
-//      NaN when y is outside [0, V).
+// The per-row state of a slice of the vocabulary, for the distribution
+// softmax(z / tau), is (m, s, u, t):
+//   m  the slice's maximum RAW logit (before the temperature),
+//   s  sum over the slice of exp((z - m) / tau),
+//   u  sum over the slice of exp((z - m) / tau) * (z - m) / tau,
+//   t  the RAW target logit z[y] when y lies in the slice, -inf when it does
+//      not, NaN when y is outside [0, V).
 // From the states of the four vocabulary quarters the row's results follow:
-//   logp    = (t - M) - log S
+//   logp    = (t - M) / tau - log S
 //   entropy = log S - U / S
 // with M the largest m and S, U the quarter sums rebased to M.  This is
 // log-sum-exp of the selected-token log-probability of the RL-Kernel logprob
 // prior-art report (report.json, "candidates") split into slices; entropy uses
-// -sum p log p = log Z - sum p z.
+// -sum p log p = log Z - sum p z.  The temperature enters only through the
+// differences z - m (exact or nearly so for the terms that matter) and
+// (t - M) / tau, which is formed in float64: no logit is rounded after
+// scaling.
+//
+// A quarter state leaves a kernel as 8 floats (32 bytes, QuarterState):
+// m, s_hi, s_lo, u, t, tau, 0, 0, with s = s_hi + s_lo held as an unevaluated
+// float pair so that the sum keeps ~40 bits between kernels.
 //
 // Every kernel that forms or merges states goes through the functions below,
 // so a slice's state has one bit pattern whichever kernel or call produced it.
@@ -27,15 +35,11 @@
 namespace lp {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr double kLn2 = 0.6931471805599453;
 constexpr int kQuarters = 4;
 
 __host__ __device__ __forceinline__ int64_t quarter_begin(int64_t V, int q) {
   return (static_cast<int64_t>(q) * V) / kQuarters;
 }
-
-// exp(x) as exp2(x * log2 e) with CUDA's exp2f.
-__device__ __forceinline__ float exp_f(float x) { return exp2f(__fmul_rn(x, kLog2e)); }
 
 // 2^x with the hardware approximation (flushes subnormal results to zero).
 __device__ __forceinline__ float exp2_approx(float x) {
@@ -44,12 +48,25 @@ __device__ __forceinline__ float exp2_approx(float x) {
   return r;
 }
 
+// exp(x) through the hardware 2^x: e^x = 2^(x log2 e).  Used where the
+// results feed the bf16-tolerance fused path.
+__device__ __forceinline__ float exp_fast(float x) { return exp2_approx(__fmul_rn(x, kLog2e)); }
+
 // max that returns NaN when either operand is NaN.
 __device__ __forceinline__ float fmax_nan(float a, float b) {
   float r;
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
   return r;
 }
+
+// 1.0f when a >= b, else 0.0f (NaN compares false).
+__device__ __forceinline__ float ge_one_zero(float a, float b) {
+  float r;
+  asm("set.ge.f32.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000u); }
 
 // Chunk c (8 bf16 values, 16 bytes) of a row of d bf16 values starting at row
 // (16-byte aligned): read whole when it lies inside the row, value by value
@@ -67,11 +84,168 @@ __device__ __forceinline__ uint4 load_row_chunk(const uint16_t* __restrict__ row
   }
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
-
-__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000u); }
 __device__ __forceinline__ float quiet_nan() { return __int_as_float(0x7fffffffu); }
 
-// Online state of one thread over a sequence of logits.
+// ------------------------------------------------------------ packed f32 pairs
+// Two floats in one 64-bit register, for the f32x2 arithmetic of sm_100+.
+
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// ------------------------------------------------- exp for arguments x <= 0
+//
+// e^x by Cody and Waite's argument reduction and a polynomial (the textbook
+// method, e.g. J.-M. Muller, "Elementary Functions", ch. 11):
+//   n = round(x log2 e), r = x - n ln2 with ln2 = L1 + L2 split so that n L1
+//   is exact (L1 has 16 significant bits), |r| <= ln2 / 2, e^x = p(r) 2^n.
+// p(r) = 1 + r + r^2 (c2 + c3 r + ... + c6 r^4) is the minimax approximation
+// of e^r on [-ln2/2, ln2/2] in relative error with the first two coefficients
+// held at exactly 1 (so p(0) = 1: the maximal term of a sum is exactly 1),
+// computed with the Remez exchange algorithm: relative error 3.1e-9 before
+// float32 rounding.  The rounding to an integer uses the float addition of
+// 1.5 * 2^23 (+127, the exponent bias): the sum's low mantissa bits are then
+// n + 127, which shifted into the exponent field give 2^n directly.
+// Arguments are clamped to [-87, 0] first (2^n stays a normal float); below
+// -87 the result, ~1e-38, is negligible against the maximal term 1 of every
+// sum it enters.  NaN stays NaN.  With float32 fma Horner steps the relative
+// error is at most ~0.55 ulp and unbiased (mean ~2e-10); the hardware 2^x, by
+// comparison, measured -5e-8 (-0.4 ulp) biased on this GPU for |x| > 1.
+constexpr float kExpClampLo = -87.0f;
+constexpr float kExpMagic = 12583039.0f;     // 1.5 * 2^23 + 127
+constexpr float kExpMagicNeg = 12583295.0f;  // 1.5 * 2^23 + 127 + 256: also sets the sign bit
+constexpr float kLn2Hi = 0.693145751953125f;
+constexpr float kLn2Lo = 1.42860677e-06f;
+constexpr float kP2 = 0.49999993451708435f, kP3 = 0.1666652068983302f,
+                kP4 = 0.04166838736126115f, kP5 = 0.008368709824171195f,
+                kP6 = 0.0013814613260779772f;
+
+__device__ __forceinline__ float exp_neg(float x) {
+  const float xc = fmax_nan(x, kExpClampLo);
+  const float t = __fmaf_rn(xc, kLog2e, kExpMagic);
+  const float n = __fsub_rn(t, kExpMagic);
+  float r = __fmaf_rn(n, -kLn2Hi, xc);
+  r = __fmaf_rn(n, -kLn2Lo, r);
+  float p = __fmaf_rn(kP6, r, kP5);
+  p = __fmaf_rn(p, r, kP4);
+  p = __fmaf_rn(p, r, kP3);
+  p = __fmaf_rn(p, r, kP2);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  return __fmul_rn(p, __int_as_float(__float_as_int(t) << 23));
+}
+
+// Two lanes at once, for the sums of the logits path: for x <= 0 (or NaN)
+// returns f - e^xc, where xc = max(x, -87) (NaN stays) is also returned and
+// f = 1 where xc == 0 (the term of the running maximum, exactly e^0 = 1), else
+// 0, also returned.  So f - e^xc is 0 for the maximal term and -e^xc for the
+// others.  The negated exponential comes from the same fma that would scale
+// p(r) by 2^n: the magic constant kExpMagicNeg puts -2^n in the shifted bits.
+__device__ __forceinline__ uint64_t count_minus_exp2(uint64_t x2, uint64_t& xc2, uint64_t& f2) {
+  float a, b;
+  upk2(x2, a, b);
+  a = fmax_nan(a, kExpClampLo);
+  b = fmax_nan(b, kExpClampLo);
+  xc2 = pk2(a, b);
+  f2 = pk2(ge_one_zero(a, 0.f), ge_one_zero(b, 0.f));
+  const uint64_t t2 = fma2(xc2, pk2(kLog2e, kLog2e), pk2(kExpMagicNeg, kExpMagicNeg));
+  const uint64_t n2 = sub2(t2, pk2(kExpMagicNeg, kExpMagicNeg));
+  uint64_t r2 = fma2(n2, pk2(-kLn2Hi, -kLn2Hi), xc2);
+  r2 = fma2(n2, pk2(-kLn2Lo, -kLn2Lo), r2);
+  uint64_t p2 = fma2(pk2(kP6, kP6), r2, pk2(kP5, kP5));
+  p2 = fma2(p2, r2, pk2(kP4, kP4));
+  p2 = fma2(p2, r2, pk2(kP3, kP3));
+  p2 = fma2(p2, r2, pk2(kP2, kP2));
+  p2 = fma2(p2, r2, pk2(1.0f, 1.0f));
+  p2 = fma2(p2, r2, pk2(1.0f, 1.0f));
+  float ta, tb;
+  upk2(t2, ta, tb);
+  const uint64_t neg_scale2 = pk2(__int_as_float(__float_as_int(ta) << 23),
+                                  __int_as_float(__float_as_int(tb) << 23));
+  return fma2(p2, neg_scale2, f2);
+}
+
+// -------------------------------------------------- float pairs (hi + lo)
+
+// Error-free sum: hi + lo == a + b exactly, hi = fl(a + b) (Knuth's TwoSum).
+__device__ __forceinline__ void two_sum(float a, float b, float& hi, float& lo) {
+  hi = __fadd_rn(a, b);
+  const float bb = __fsub_rn(hi, a);
+  lo = __fadd_rn(__fsub_rn(a, __fsub_rn(hi, bb)), __fsub_rn(b, bb));
+}
+
+// (a_hi + a_lo) + (b_hi + b_lo) as a normalised pair.
+__device__ __forceinline__ void add_pair(float a_hi, float a_lo, float b_hi, float b_lo,
+                                         float& hi, float& lo) {
+  float s, e;
+  two_sum(a_hi, b_hi, s, e);
+  e = __fadd_rn(e, __fadd_rn(a_lo, b_lo));
+  hi = __fadd_rn(s, e);
+  lo = __fsub_rn(e, __fsub_rn(hi, s));
+}
+
+// a * (x_hi + x_lo) as a pair (the product's rounding error kept by an fma).
+__device__ __forceinline__ void mul_pair(float a, float x_hi, float x_lo, float& hi, float& lo) {
+  const float p = __fmul_rn(a, x_hi);
+  const float e = __fmaf_rn(a, x_hi, -p);
+  const float l = __fmaf_rn(a, x_lo, e);
+  hi = __fadd_rn(p, l);
+  lo = __fsub_rn(l, __fsub_rn(hi, p));
+}
+
+// d / tau for a difference d <= 0 of raw logits: d * (1/tau) with 1/tau given
+// as a float pair inv_hi + inv_lo, so that no rounding of 1/tau biases every
+// term the same way.  With inv_hi == 1, inv_lo == 0 this is d itself.
+__device__ __forceinline__ float scale_diff(float d, float inv_hi, float inv_lo) {
+  return __fmaf_rn(d, inv_lo, __fmul_rn(d, inv_hi));
+}
+
+// -------------------------------------------------------------- states
+
+struct QuarterState {
+  float m, s_hi, s_lo, u, t, tau, r0, r1;
+};
+static_assert(sizeof(QuarterState) == 32, "quarter states are 32 bytes");
+
+__device__ __forceinline__ void store_state(QuarterState* dst, const QuarterState& q) {
+  float4* p = reinterpret_cast<float4*>(dst);
+  p[0] = make_float4(q.m, q.s_hi, q.s_lo, q.u);
+  p[1] = make_float4(q.t, q.tau, 0.f, 0.f);
+}
+
+__device__ __forceinline__ QuarterState load_state(const QuarterState* src) {
+  const float4* p = reinterpret_cast<const float4*>(src);
+  const float4 a = p[0], b = p[1];
+  return QuarterState{a.x, a.y, a.z, a.w, b.x, b.y, 0.f, 0.f};
+}
+
+// Online state of one thread over a sequence of logits of the fused path
+// (bf16 tolerance): s includes the maximal term.
 struct Online {
   float m, s, u;
   __device__ __forceinline__ void reset() {
@@ -81,14 +255,14 @@ struct Online {
   }
   // Raise the running maximum to bm (a maximum over the next values, computed
   // with fmax_nan).  NaN in bm makes the state NaN from here on.
-  __device__ __forceinline__ void raise_to(float bm) {
+  __device__ __forceinline__ void raise_to(float bm, float inv_tau) {
     if (!(bm <= m)) {
       if (m == neg_inf()) {
         s = 0.f;
         u = 0.f;
       } else {
-        const float delta = __fsub_rn(m, bm);  // < 0
-        const float a = exp_f(delta);
+        const float delta = __fmul_rn(__fsub_rn(m, bm), inv_tau);  // < 0
+        const float a = exp_fast(delta);
         u = __fmul_rn(a, __fmaf_rn(delta, s, u));
         s = __fmul_rn(a, s);
       }
@@ -98,82 +272,63 @@ struct Online {
   __device__ __forceinline__ bool active() const { return m != neg_inf(); }
 };
 
-// One logit's terms relative to the running maximum m: e = exp(x - m) and the
-// clamped difference d = x - m, so that e * d is 0 for a -inf logit (never
-// 0 * inf) while NaN stays NaN.
-__device__ __forceinline__ void term(float x, float m, float& e, float& d) {
-  d = fmax_nan(__fsub_rn(x, m), -3.402823466e38f);
-  e = exp_f(d);
+// One logit's terms relative to the running maximum m on the fused path:
+// d = (x - m) / tau clamped so that e * d is 0 for a -inf logit (never
+// 0 * inf) while NaN stays NaN, and e = exp(d).
+__device__ __forceinline__ void term(float x, float m, float inv_tau, float& e, float& d) {
+  d = fmax_nan(__fmul_rn(__fsub_rn(x, m), inv_tau), -3.402823466e38f);
+  e = exp_fast(d);
 }
 
-// Rebase (m, s, u) to a common maximum M >= m: returns (s', u') with
-// s' = e^(m-M) s and u' = e^(m-M) (u + (m - M) s).  An empty state (m = -inf)
-// contributes nothing.
-__device__ __forceinline__ void rebase(float m, float s, float u, float M, float& s_out,
-                                       float& u_out) {
-  if (m == neg_inf()) {
-    s_out = 0.f;
-    u_out = 0.f;
-    return;
+// ------------------------------------------------------------- finalise
+//
+// The four quarter states of a row sit in four consecutive lanes of a warp
+// (lane & 3 == quarter); `mask` names every lane taking part (groups of four).
+// Each lane rebases its quarter to the row maximum in float64,
+//   a_q = exp((m_q - M) / tau),  S_q = a_q (s_hi + s_lo),
+//   U_q = a_q (u + (m_q - M) / tau (s_hi + s_lo)),
+// and the sums are formed as (Q0 + Q1) + (Q2 + Q3) with two xor-shuffles
+// (addition is commutative, so every lane of the group holds the same bits).
+// Every lane then has the row's logp, entropy and log Z = M / tau + log S.
+// States of different temperatures, NaN anywhere, or no finite logit give NaN.
+__device__ __forceinline__ void finalise_quad(const QuarterState& q, unsigned mask, float& logp,
+                                              float& entropy, float& log_z) {
+  float M = q.m;
+  M = fmax_nan(M, __shfl_xor_sync(mask, M, 1));
+  M = fmax_nan(M, __shfl_xor_sync(mask, M, 2));
+  float t = q.t;
+  t = fmax_nan(t, __shfl_xor_sync(mask, t, 1));
+  t = fmax_nan(t, __shfl_xor_sync(mask, t, 2));
+  int same_tau = q.tau == __shfl_xor_sync(mask, q.tau, 1);
+  same_tau &= q.tau == __shfl_xor_sync(mask, q.tau, 2);
+  same_tau &= __shfl_xor_sync(mask, same_tau, 1);
+  same_tau &= __shfl_xor_sync(mask, same_tau, 2);
+
+  const double tau = static_cast<double>(q.tau);
+  double S = 0.0, U = 0.0;
+  if (q.m != neg_inf() && M == M) {
+    const double delta = __ddiv_rn(__dsub_rn(static_cast<double>(q.m), static_cast<double>(M)), tau);
+    const double a = exp(delta);
+    const double sq = __dadd_rn(static_cast<double>(q.s_hi), static_cast<double>(q.s_lo));
+    S = __dmul_rn(a, sq);
+    U = __dmul_rn(a, __fma_rn(delta, sq, static_cast<double>(q.u)));
   }
-  const float delta = __fsub_rn(m, M);
-  const float a = exp_f(delta);
-  s_out = __fmul_rn(a, s);
-  u_out = __fmul_rn(a, __fmaf_rn(delta, s, u));
-}
+  S = __dadd_rn(S, __shfl_xor_sync(mask, S, 1));
+  U = __dadd_rn(U, __shfl_xor_sync(mask, U, 1));
+  S = __dadd_rn(S, __shfl_xor_sync(mask, S, 2));
+  U = __dadd_rn(U, __shfl_xor_sync(mask, U, 2));
 
-// exp(delta) for delta <= 0 given exactly in double, through float: the
-// relative error is that of rounding delta to float plus CUDA's expf, a few
-// times 1e-7 for the terms that matter (|delta| of order 1); terms with large
-// |delta| are negligible in the sums they enter.  Double-precision
-// transcendentals are slow on this GPU and the four quarters need only this.
-__device__ __forceinline__ double exp_nonpos(double delta) {
-  return static_cast<double>(expf(static_cast<float>(delta)));
-}
-
-// log(S) for finite S > 0: with S = m 2^e, m in [0.5, 1) (frexp),
-// log S = log m + e ln 2, log m taken with CUDA's logf (|log m| < 0.7, so its
-// absolute error is about 1e-7) and the rest in double.  log S itself can be
-// ~12 or more, where a float would carry an error of ~1e-6.
-__device__ __forceinline__ double log_pos(double S) {
-  int e;
-  const double m = frexp(S, &e);
-  return __dadd_rn(static_cast<double>(logf(static_cast<float>(m))),
-                   __dmul_rn(static_cast<double>(e), kLn2));
-}
-
-// Final merge of the four quarter states, fixed order (Q0 + Q1) + (Q2 + Q3),
-// in float64 (the exponentials and the logarithm through float, above), and
-// the row's results.
-__device__ __forceinline__ void finalise(const float4 (&q)[kQuarters], float& logp,
-                                         float& entropy) {
-  const float M = fmaxf(fmaxf(q[0].x, q[1].x), fmaxf(q[2].x, q[3].x));
-  double S_q[kQuarters], U_q[kQuarters];
-#pragma unroll
-  for (int i = 0; i < kQuarters; ++i) {
-    if (q[i].x == neg_inf()) {
-      S_q[i] = 0.0;
-      U_q[i] = 0.0;
-    } else {
-      const double delta = __dsub_rn(static_cast<double>(q[i].x), static_cast<double>(M));
-      const double a = exp_nonpos(delta);
-      S_q[i] = __dmul_rn(a, static_cast<double>(q[i].y));
-      U_q[i] = __dmul_rn(a, __fma_rn(delta, static_cast<double>(q[i].y),
-                                     static_cast<double>(q[i].z)));
-    }
-  }
-  const double S = __dadd_rn(__dadd_rn(S_q[0], S_q[1]), __dadd_rn(S_q[2], S_q[3]));
-  const double U = __dadd_rn(__dadd_rn(U_q[0], U_q[1]), __dadd_rn(U_q[2], U_q[3]));
-  const float t = fmax_nan(fmax_nan(q[0].w, q[1].w), fmax_nan(q[2].w, q[3].w));
-  if (!(M > neg_inf()) || !(S > 0.0)) {  // no distribution, or NaN somewhere
+  if (!same_tau || !(M > neg_inf()) || !(S > 0.0) || U != U) {  // NaN somewhere, or empty
     logp = quiet_nan();
     entropy = quiet_nan();
+    log_z = quiet_nan();
     return;
   }
-  const double log_s = log_pos(S);
-  logp = __double2float_rn(
-      __dsub_rn(__dsub_rn(static_cast<double>(t), static_cast<double>(M)), log_s));
+  const double log_s = log(S);
+  logp = __double2float_rn(__dsub_rn(
+      __ddiv_rn(__dsub_rn(static_cast<double>(t), static_cast<double>(M)), tau), log_s));
   entropy = __double2float_rn(__dsub_rn(log_s, __ddiv_rn(U, S)));
+  log_z = __double2float_rn(__dadd_rn(__ddiv_rn(static_cast<double>(M), tau), log_s));
 }
 
 }  // namespace lp

@@ -77,14 +77,22 @@ class PerContextOnce {
   int next_ = 0;
 };
 
+// Temperature of a call: tau itself (stored in every quarter state) and 1/tau
+// as a float pair inv_hi + inv_lo (inv_hi = fl(1/tau), inv_lo the rest); tau
+// == 1 gives (1, 1, 0), for which the kernels skip every multiplication.
+struct TauArgs {
+  float tau;
+  float inv_hi;
+  float inv_lo;
+};
+
 // logits path
-// inv_tau: every logit is multiplied by it first (1.0f: no temperature)
 lp_status launch_logits_final(const float* logits, int64_t ld, const int64_t* targets,
-                              int64_t T, int64_t V, float inv_tau, float* logp, float* entropy,
-                              cudaStream_t stream);
+                              int64_t T, int64_t V, const TauArgs& tau, float* logp,
+                              float* entropy, cudaStream_t stream);
 lp_status launch_logits_partials(const float* logits_shard, int64_t ld,
                                  const int64_t* targets, int64_t T, int64_t V_total,
-                                 int q_first, int n_q, float inv_tau, float* partials,
+                                 int q_first, int n_q, const TauArgs& tau, float* partials,
                                  cudaStream_t stream);
 lp_status launch_merge_partials(const float* const* shard_partials, int n_shards, int64_t T,
                                 float* logp, float* entropy, cudaStream_t stream);
@@ -93,7 +101,7 @@ lp_status launch_merge_partials(const float* const* shard_partials, int n_shards
 size_t linear_workspace_bytes(int64_t T, int64_t d, int64_t V_total, int n_q);
 lp_status launch_linear(const Device& dev, const void* H, int64_t ld_h, const void* W,
                         int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
-                        int64_t V_total, int q_first, int n_q, float inv_tau, float* logp,
+                        int64_t V_total, int q_first, int n_q, const TauArgs& tau, float* logp,
                         float* entropy, float* partials_out, void* workspace,
                         cudaStream_t stream);
 
@@ -106,7 +114,8 @@ lp_status static_scratch(void** out);
 // log-sum-exp log Z of the (tempered) logits.
 lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, const void* W,
                               int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
-                              int64_t V_total, int q_first, int n_q, float inv_tau, float* logp,
+                              int64_t V_total, int q_first, int n_q, const TauArgs& tau,
+                              float* logp,
                               float* entropy, float* partials_out, float* lse,
                               void* workspace, cudaStream_t stream);
 
@@ -114,10 +123,15 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
 size_t linear_backward_workspace_bytes(int64_t T, int64_t d, int64_t V);
 lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h, const void* W,
                                  int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
-                                 int64_t V, float inv_tau, const float* saved_lse,
+                                 int64_t V, const TauArgs& tau, const float* saved_lse,
                                  const float* saved_entropy, const float* g_logp,
-                                 const float* g_ent, float* grad_h, float* grad_w,
-                                 void* workspace, cudaStream_t stream);
+                                 const float* g_ent, float* grad_h, void* grad_w,
+                                 bool grad_w_bf16, void* workspace, cudaStream_t stream);
+
+// Read and clear the check word of each translation unit (lp_check.cuh).
+cudaError_t take_check_word_logits(uint32_t* out);
+cudaError_t take_check_word_linear(uint32_t* out);
+cudaError_t take_check_word_backward(uint32_t* out);
 
 int persistent_grid_limit();
 int fault_injection();

@@ -24,8 +24,9 @@
 // running maximum is raised once per 64 columns and the exponentials of a fully
 // valid piece are summed in packed f32x2 arithmetic.
 //
-// Temperature: with inv_tau != 1 every logit leaving tensor memory is first
-// multiplied by inv_tau; with inv_tau == 1 nothing changes.
+// Temperature: maxima are taken over raw logits and every difference z - m is
+// multiplied by fl(1/tau) before the exponential; with tau == 1 no
+// multiplication is made.
 //
 // A pipeline wait that gives up sets the workspace error word (see
 // lp_tcgen05.cuh); the merge kernel then writes NaN for every row.
@@ -34,6 +35,7 @@
 
 #include <mutex>
 
+#include "lp_check.cuh"
 #include "lp_device.cuh"
 #include "lp_internal.h"
 #include "lp_tcgen05.cuh"
@@ -93,6 +95,24 @@ bool encode_f32_3d_store(CUtensorMap* map, void* base, int64_t S, int64_t rows, 
   const cuuint32_t box[3] = {32, 32, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_bf16_3d_store(CUtensorMap* map, void* base, int64_t S, int64_t rows, int64_t cols,
+                          int64_t ld, int64_t split_stride) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  if (((ld * 2) % 16) != 0 || ((split_stride * 2) % 16) != 0 ||
+      (reinterpret_cast<uintptr_t>(base) % 16) != 0)
+    return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(S)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2,
+                                 static_cast<cuuint64_t>(S > 1 ? split_stride : rows * ld) * 2};
+  const cuuint32_t box[3] = {64, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -162,45 +182,42 @@ struct LinearArgs {
   const int64_t* targets;
   float4* chunks;  // [T][n_q][n_tiles_q]
   uint32_t* err;
-  float inv_tau;   // every logit is multiplied by it (1: no temperature)
+  float inv_tau;   // differences z - m are multiplied by it (1: no temperature)
+  float tau;       // stored in the quarter states
   int T;
   int n_q;
   int withhold_first_load;  // fault injection for tests of the bounded waits
 };
 
 // Add the 64 logits of a fully valid piece to the online state (whose maximum
-// already covers them): e = 2^(x log2e - m log2e) (one fma, one ex2.approx.ftz),
-// s += e, u += e (x - m), in packed f32x2 arithmetic with four lane sums.  Used
-// only when every logit of the piece is finite, which a product of finite bf16
+// already covers them): d = (x - m) / tau, e = 2^(d log2e) (ex2.approx.ftz),
+// s += e, u += e d, in packed f32x2 arithmetic with four lane sums.  Used only
+// when every logit of the piece is finite, which a product of finite bf16
 // inputs always is.
-__device__ __forceinline__ void accumulate_piece_packed(const float (&v)[64], Online& st) {
-  const float mL = __fmul_rn(st.m, kLog2e);
-  uint64_t mm, ll, nml, zero;
-  asm("mov.b64 %0, {%1, %1};" : "=l"(mm) : "f"(st.m));
-  asm("mov.b64 %0, {%1, %1};" : "=l"(ll) : "f"(kLog2e));
-  asm("mov.b64 %0, {%1, %1};" : "=l"(nml) : "f"(-mL));
-  asm("mov.b64 %0, {%1, %1};" : "=l"(zero) : "f"(0.f));
+template <bool kScaled>
+__device__ __forceinline__ void accumulate_piece_packed(const float (&v)[64], Online& st,
+                                                        float inv_tau) {
+  const uint64_t mm = pk2(st.m, st.m);
+  const uint64_t ll = pk2(kLog2e, kLog2e);
+  const uint64_t it = pk2(inv_tau, inv_tau);
+  const uint64_t zero = pk2(0.f, 0.f);
   uint64_t s2[2] = {zero, zero}, u2[2] = {zero, zero};
 #pragma unroll
   for (int i = 0; i < 64; i += 2) {
-    uint64_t x2, d2, a2, e2;
-    float a0, a1, e0, e1;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(x2) : "f"(v[i]), "f"(v[i + 1]));
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d2) : "l"(x2), "l"(mm));
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(a2) : "l"(x2), "l"(ll), "l"(nml));
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(a2));
-    e0 = exp2_approx(a0);
-    e1 = exp2_approx(a1);
-    asm("mov.b64 %0, {%1, %2};" : "=l"(e2) : "f"(e0), "f"(e1));
+    uint64_t d2 = sub2(pk2(v[i], v[i + 1]), mm);
+    if (kScaled) d2 = mul2(d2, it);
+    float a0, a1;
+    upk2(mul2(d2, ll), a0, a1);
+    const uint64_t e2 = pk2(exp2_approx(a0), exp2_approx(a1));
     const int k = (i >> 1) & 1;
-    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(s2[k]) : "l"(e2));
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(u2[k]) : "l"(e2), "l"(d2));
+    s2[k] = add2(s2[k], e2);
+    u2[k] = fma2(e2, d2, u2[k]);
   }
   float sa[4], ua[4];
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(sa[0]), "=f"(sa[1]) : "l"(s2[0]));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(sa[2]), "=f"(sa[3]) : "l"(s2[1]));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(ua[0]), "=f"(ua[1]) : "l"(u2[0]));
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(ua[2]), "=f"(ua[3]) : "l"(u2[1]));
+  upk2(s2[0], sa[0], sa[1]);
+  upk2(s2[1], sa[2], sa[3]);
+  upk2(u2[0], ua[0], ua[1]);
+  upk2(u2[1], ua[2], ua[3]);
   st.s = __fadd_rn(st.s, __fadd_rn(__fadd_rn(sa[0], sa[1]), __fadd_rn(sa[2], sa[3])));
   st.u = __fadd_rn(st.u, __fadd_rn(__fadd_rn(ua[0], ua[1]), __fadd_rn(ua[2], ua[3])));
 }
@@ -225,15 +242,12 @@ struct StateEpilogue {
 
     st.reset();
     t = neg_inf();
+    const float inv_tau = a->inv_tau;
 #pragma unroll 1
     for (int p = 0; p < kBN / 64; ++p) {
       float v[64];
       __syncwarp();
       tmem_load64(taddr + static_cast<uint32_t>(p * 64), v);
-      if (a->inv_tau != 1.f) {
-#pragma unroll
-        for (int i = 0; i < 64; ++i) v[i] = __fmul_rn(v[i], a->inv_tau);
-      }
       if (p * 64 + 64 > valid) {
 #pragma unroll
         for (int i = 0; i < 64; ++i)
@@ -248,16 +262,19 @@ struct StateEpilogue {
       float bm = v[0];
 #pragma unroll
       for (int i = 1; i < 64; ++i) bm = fmax_nan(bm, v[i]);
-      st.raise_to(bm);
+      st.raise_to(bm, inv_tau);
       if (p * 64 + 64 <= valid) {
-        accumulate_piece_packed(v, st);
+        if (inv_tau == 1.f)
+          accumulate_piece_packed<false>(v, st, inv_tau);
+        else
+          accumulate_piece_packed<true>(v, st, inv_tau);
       } else if (st.active()) {
         float sa[4] = {0.f, 0.f, 0.f, 0.f};
         float ua[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 64; ++i) {
           float e, d;
-          term(v[i], st.m, e, d);
+          term(v[i], st.m, inv_tau, e, d);
           sa[i & 3] = __fadd_rn(sa[i & 3], e);
           ua[i & 3] = __fmaf_rn(e, d, ua[i & 3]);
         }
@@ -273,8 +290,13 @@ struct StateEpilogue {
     int mb, ql, j;
     a->tiles.decode(u, mb, ql, j);
     const int64_t row = static_cast<int64_t>(mb) * (2 * kBM) + rank * kBM + lane_grp * 32 + lane;
-    if (row < a->T)
-      a->chunks[(row * a->n_q + ql) * a->tiles.n_tiles_q + j] = make_float4(st.m, st.s, st.u, t);
+    if (row < a->T) {
+      const int64_t idx = (row * a->n_q + ql) * a->tiles.n_tiles_q + j;
+      if (LP_CHECK(ql < a->n_q && j < a->tiles.n_tiles_q &&
+                       idx < int64_t(a->T) * a->n_q * a->tiles.n_tiles_q,
+                   kChkStateIndex))
+        a->chunks[idx] = make_float4(st.m, st.s, st.u, t);
+    }
   }
 };
 
@@ -294,16 +316,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // l rebases tiles l, l+32, l+64, ... to it and sums them, and the 32 lane sums
 // are combined by a fixed shuffle tree.  The result depends only on the
 // quarter's tile states.  When `lse` is given, the row's log-partition
-// log Z = M + log S (of the scaled logits) is also written there.
+// log Z = M / tau + log S is also written there.
 __global__ void __launch_bounds__(128)
     lp_tile_merge_kernel(const float4* __restrict__ chunks, const int64_t* __restrict__ targets,
                          const uint32_t* __restrict__ err, int n_q, int n_tiles_q, int64_t V,
-                         float* __restrict__ logp, float* __restrict__ entropy,
-                         float4* __restrict__ partials_out, float* __restrict__ lse) {
-  __shared__ float4 qs[kQuarters];
+                         float inv_tau, float tau, int64_t T, float* __restrict__ logp,
+                         float* __restrict__ entropy, QuarterState* __restrict__ partials_out,
+                         float* __restrict__ lse) {
+  __shared__ __align__(16) QuarterState qs[kQuarters];
   const int ql = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t row = blockIdx.x;
+  if (!LP_CHECK(row < T, kChkRowIndex)) return;
   if (ql < n_q) {
     const float4* c = chunks + (row * n_q + ql) * n_tiles_q;
     float M = neg_inf();
@@ -314,10 +338,12 @@ __global__ void __launch_bounds__(128)
     float t = neg_inf();
     for (int j = lane; j < n_tiles_q; j += 32) {
       const float4 x = c[j];
-      float s, u;
-      rebase(x.x, x.y, x.z, M, s, u);
-      S = __fadd_rn(S, s);
-      U = __fadd_rn(U, u);
+      if (x.x != neg_inf()) {
+        const float delta = __fmul_rn(__fsub_rn(x.x, M), inv_tau);
+        const float a = exp_neg(delta);
+        S = __fadd_rn(S, __fmul_rn(a, x.y));
+        U = __fadd_rn(U, __fmul_rn(a, __fmaf_rn(delta, x.y, x.z)));
+      }
       t = fmax_nan(t, x.w);
     }
 #pragma unroll
@@ -329,34 +355,26 @@ __global__ void __launch_bounds__(128)
     if (lane == 0) {
       const int64_t y = targets[row];
       if (y < 0 || y >= V) t = quiet_nan();
-      float4 st = make_float4(M, S, U, t);
-      if (*err != 0u) st.y = quiet_nan();  // a pipeline wait gave up: no result
-      if (partials_out != nullptr)
-        partials_out[row * n_q + ql] = st;
+      QuarterState st{M, S, 0.f, U, t, tau, 0.f, 0.f};
+      if (*err != 0u) st.s_hi = quiet_nan();  // a pipeline wait gave up: no result
+      if (partials_out != nullptr) {
+        if (LP_CHECK(row * n_q + ql < T * n_q, kChkStateIndex))
+          store_state(&partials_out[row * n_q + ql], st);
+      }
       else
-        qs[ql] = st;
+        store_state(&qs[ql], st);
     }
   }
   if (partials_out != nullptr) return;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    const float4 q4[kQuarters] = {qs[0], qs[1], qs[2], qs[3]};
-    float lp, ent;
-    finalise(q4, lp, ent);
-    logp[row] = lp;
-    if (entropy != nullptr) entropy[row] = ent;
-    if (lse != nullptr) {
-      // log Z from the same quarter states: M + log S, in float64
-      const float M = fmaxf(fmaxf(q4[0].x, q4[1].x), fmaxf(q4[2].x, q4[3].x));
-      double S = 0.0;
-#pragma unroll
-      for (int i = 0; i < kQuarters; ++i)
-        if (q4[i].x != neg_inf())
-          S = __dadd_rn(S, __dmul_rn(exp_nonpos(__dsub_rn(static_cast<double>(q4[i].x),
-                                                          static_cast<double>(M))),
-                                     static_cast<double>(q4[i].y)));
-      lse[row] = (*err != 0u) ? quiet_nan()
-                              : __double2float_rn(__dadd_rn(static_cast<double>(M), log_pos(S)));
+  if (threadIdx.x < 4) {
+    const QuarterState mine = load_state(&qs[threadIdx.x]);
+    float lp, ent, lz;
+    finalise_quad(mine, 0xfu, lp, ent, lz);
+    if (threadIdx.x == 0) {
+      logp[row] = lp;
+      if (entropy != nullptr) entropy[row] = ent;
+      if (lse != nullptr) lse[row] = lz;
     }
   }
 }
@@ -384,7 +402,8 @@ __global__ void lp_pad_rows_kernel(const uint16_t* __restrict__ H, int64_t ld_h,
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t r = i / d16, c = i % d16;
-    dst[i] = r < T ? load_row_chunk(H + r * ld_h, d, c) : make_uint4(0u, 0u, 0u, 0u);
+    if (LP_CHECK(i < rows_out * d16 && c * 8 < ld_h, kChkCopyIndex))
+      dst[i] = r < T ? load_row_chunk(H + r * ld_h, d, c) : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
@@ -399,8 +418,8 @@ size_t linear_workspace_bytes(int64_t T, int64_t d, int64_t V_total, int n_q) {
 
 lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, const void* W,
                               int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
-                              int64_t V_total, int q_first, int n_q, float inv_tau, float* logp,
-                              float* entropy, float* partials_out, float* lse,
+                              int64_t V_total, int q_first, int n_q, const TauArgs& tau,
+                              float* logp, float* entropy, float* partials_out, float* lse,
                               void* workspace, cudaStream_t stream) {
   static PerContextOnce attr;
   if (attr.run(dev.ctx_id, [] {
@@ -442,7 +461,8 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
   a.targets = targets;
   a.chunks = reinterpret_cast<float4*>(static_cast<uint8_t*>(workspace) + kWorkspaceHeader);
   a.err = static_cast<uint32_t*>(workspace);
-  a.inv_tau = inv_tau;
+  a.inv_tau = tau.inv_hi;
+  a.tau = tau.tau;
   a.T = static_cast<int>(T);
   a.n_q = n_q;
   a.withhold_first_load = fault_injection();
@@ -455,18 +475,18 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
   if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
   if (ev_stop != nullptr && cudaEventRecord(ev_stop, stream) != cudaSuccess) return LP_ERR_CUDA;
   lp_tile_merge_kernel<<<static_cast<unsigned>(T), 128, 0, stream>>>(
-      a.chunks, targets, a.err, n_q, a.tiles.n_tiles_q, V_total, logp, entropy,
-      reinterpret_cast<float4*>(partials_out), lse);
+      a.chunks, targets, a.err, n_q, a.tiles.n_tiles_q, V_total, a.inv_tau, a.tau, T, logp, entropy,
+      reinterpret_cast<QuarterState*>(partials_out), lse);
   return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }
 
 lp_status launch_linear(const Device& dev, const void* H, int64_t ld_h, const void* W,
                         int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
-                        int64_t V_total, int q_first, int n_q, float inv_tau, float* logp,
+                        int64_t V_total, int q_first, int n_q, const TauArgs& tau, float* logp,
                         float* entropy, float* partials_out, void* workspace,
                         cudaStream_t stream) {
   return launch_linear_stats(dev, H, ld_h, W, ld_w, targets, T, d, V_total, q_first, n_q,
-                             inv_tau, logp, entropy, partials_out, nullptr, workspace, stream);
+                             tau, logp, entropy, partials_out, nullptr, workspace, stream);
 }
 
 // --------------------------------------------- fixed scratch for the no-alloc call
@@ -522,5 +542,7 @@ lp_status static_scratch(void** out) {
   *out = p;
   return LP_OK;
 }
+
+cudaError_t take_check_word_linear(uint32_t* out) { return take_check_word(out); }
 
 }  // namespace lp

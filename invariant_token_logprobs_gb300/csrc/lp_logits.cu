@@ -9,25 +9,29 @@
 // owns the 4-column groups g = i, i + 256, i + 512, ... counted from the
 // quarter's first column; it reads them eight groups (128 bytes) at a time
 // with 128-bit non-caching loads, so a warp reads 512 contiguous bytes per
-// load.  A thread keeps an online (max, sum-exp, sum-exp*(z-max)) state,
-// raising its maximum once per batch of 32 values, and sums each batch in four
-// column-lane accumulators before adding it to the state.  The 256 thread
-// states are rebased to the CTA maximum and summed in a fixed tree (warp
-// shuffles, then 8 warp partials in a fixed pairing).  Which thread owns which
-// column depends only on the column's offset inside its quarter, so a row's
-// quarter state is the same whatever the row's position, batch or shard.
+// load.  A thread keeps an online state (max m, count of values equal to m,
+// sum of exp((z - m)/tau) over the others, and the entropy sum), raising its
+// maximum once per batch of 32 values; the exponentials are evaluated two at a
+// time in f32x2 arithmetic with the Cody-Waite + Taylor exp of lp_device.cuh
+// (unbiased, <= 0.64 ulp).  The 256 thread states are rebased to the CTA
+// maximum and summed as float pairs (hi + lo) in a fixed tree (warp shuffles,
+// then 8 warp partials in a fixed pairing).  Which thread owns which column
+// depends only on the column's offset inside its quarter, so a row's quarter
+// state is the same whatever the row's position, batch or shard.
 //
 // Finalising variant: the 4 CTAs of a row form a thread-block cluster; each
-// writes its quarter state into the shared memory of cluster rank 0 (DSMEM),
-// and after the cluster barrier rank 0 merges (Q0 + Q1) + (Q2 + Q3).  Partials
-// variant: each CTA writes its quarter state to global memory for
-// lp_merge_partials.
+// writes its 32-byte quarter state into the shared memory of cluster rank 0
+// (DSMEM), and after the cluster barrier four lanes of rank 0 merge
+// (Q0 + Q1) + (Q2 + Q3) in float64.  Partials variant: each CTA writes its
+// quarter state to global memory for lp_merge_partials.
 //
-// Temperature: with inv_tau != 1 every logit is first multiplied by inv_tau
-// (fl(z * fl(1/tau))); with inv_tau == 1 the results are exactly those of the
-// unscaled computation.
+// Temperature: the maximum is taken over raw logits and each difference
+// z - m is multiplied by 1/tau = inv_hi + inv_lo; with tau == 1 no
+// multiplication is made and the results are those of the unscaled entry
+// points.
 #include <cuda_runtime.h>
 
+#include "lp_check.cuh"
 #include "lp_device.cuh"
 #include "lp_internal.h"
 
@@ -36,20 +40,22 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kBatch = 8;  // 4-float groups per thread per batch
+constexpr int kBatch = 8;  // 4-float groups per thread per batch (32 values)
 
 __device__ __forceinline__ float4 load_stream(const float* p) {
   float4 v;
-  asm("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
-      : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-      : "l"(p));
+  asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p));
   return v;
 }
 
-// Group g (columns 4g .. 4g+3 of the quarter); columns >= w read as -inf.
-__device__ __forceinline__ void load_group(const float* __restrict__ q0, int64_t w, int64_t g,
-                                           bool vec, float (&v)[4]) {
-  const int64_t c = g * 4;
+// Group g (columns 4g .. 4g+3 of the quarter, w < 2^31 columns); columns >= w
+// read as -inf.  A whole group of a 16-byte aligned quarter is one 128-bit
+// load, others are scalar loads of the same values.
+__device__ __forceinline__ void load_group(const float* __restrict__ q0, int w, int g, bool vec,
+                                           float (&v)[4]) {
+  const int c = g * 4;
   if (vec && c + 3 < w) {
     const float4 x = load_stream(q0 + c);
     v[0] = x.x;
@@ -62,215 +68,310 @@ __device__ __forceinline__ void load_group(const float* __restrict__ q0, int64_t
   }
 }
 
-// State (M, S, U) of the w columns starting at q0, each logit multiplied by
-// inv_tau first when kScaled; valid in thread 0.
+// Per-thread online state of the logits path: the running maximum m, the
+// number c of values equal to it (each contributes exactly exp(0) = 1), the sum
+// s of exp((z - m) / tau) over the other values, and u.  Keeping the maximal
+// terms out of s keeps every rounding of the running sums relative to the
+// smaller terms: a row dominated by a few large logits (the peaked workload)
+// loses nothing to adding small terms onto a term of 1.
+struct LogitsOnline {
+  float m, c, s, u;
+  __device__ __forceinline__ void reset() {
+    m = neg_inf();
+    c = 0.f;
+    s = 0.f;
+    u = 0.f;
+  }
+  __device__ __forceinline__ void raise_to(float bm, float inv_hi, float inv_lo) {
+    if (!(bm <= m)) {
+      if (m == neg_inf()) {
+        c = 0.f;
+        s = 0.f;
+        u = 0.f;
+      } else {
+        const float delta = scale_diff(__fsub_rn(m, bm), inv_hi, inv_lo);  // < 0
+        const float a = exp_neg(delta);
+        const float tot = __fadd_rn(c, s);
+        u = __fmul_rn(a, __fmaf_rn(delta, tot, u));
+        s = __fmul_rn(a, tot);
+        c = 0.f;
+      }
+      m = bm;
+    }
+  }
+};
+
+// The quarter state (M, S = S_hi + S_lo, U) of the w columns starting at q0
+// for softmax(z / tau); valid in thread 0.
 template <bool kScaled>
 __device__ __forceinline__ void quarter_state(const float* __restrict__ q0, int64_t w,
-                                              float inv_tau, float& M_out, float& S_out,
-                                              float& U_out) {
-  __shared__ float red_m[kWarps], red_s[kWarps], red_u[kWarps];
+                                              float inv_hi, float inv_lo, QuarterState& out) {
+  __shared__ float red_m[kWarps], red_hi[kWarps], red_lo[kWarps], red_u[kWarps];
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const bool vec = (reinterpret_cast<uintptr_t>(q0) & 15u) == 0;
-  const int64_t n_groups = (w + 3) / 4;
+  const int wi = static_cast<int>(w);
+  const int n_groups = (wi + 3) / 4;
 
-  Online st;
+  LogitsOnline st;
   st.reset();
-  for (int64_t g0 = 0; g0 < n_groups; g0 += int64_t(kThreads) * kBatch) {
+  for (int g0 = 0; g0 < n_groups; g0 += kThreads * kBatch) {
     float v[kBatch][4];
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k) load_group(q0, w, g0 + k * kThreads + tid, vec, v[k]);
-    if (kScaled) {
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[k][i] = __fmul_rn(v[k][i], inv_tau);
-    }
+    for (int k = 0; k < kBatch; ++k) load_group(q0, wi, g0 + k * kThreads + tid, vec, v[k]);
     float bm = v[0][0];
 #pragma unroll
     for (int k = 0; k < kBatch; ++k)
 #pragma unroll
       for (int i = 0; i < 4; ++i) bm = fmax_nan(bm, v[k][i]);
-    st.raise_to(bm);
-    if (st.active()) {
-      float sa[4] = {0.f, 0.f, 0.f, 0.f};
-      float ua[4] = {0.f, 0.f, 0.f, 0.f};
-      // e = 2^(x log2e - m log2e): one fma and one ex2.approx.ftz per logit;
-      // d = x - m clamped so that a -inf logit adds e * d = 0, NaN stays NaN
-      const float mL = __fmul_rn(st.m, kLog2e);
+    st.raise_to(bm, inv_hi, inv_lo);
+    if (st.m != neg_inf()) {
+      // per value: d = (z - m) / tau, f = [d == 0] (the running maximum's
+      // term, exactly 1) to the count, e = exp(d) for the others to s, and
+      // e d to u.  The lanes hold f - e and (f - e) d (negated sums; f d = 0),
+      // two values per f32x2 operation, four lanes.
+      const uint64_t mm = pk2(st.m, st.m);
+      const uint64_t ih = pk2(inv_hi, inv_hi), il = pk2(inv_lo, inv_lo);
+      const uint64_t zero = pk2(0.f, 0.f);
+      uint64_t sn2[2] = {zero, zero}, c2[2] = {zero, zero}, un2[2] = {zero, zero};
 #pragma unroll
       for (int k = 0; k < kBatch; ++k)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float d = fmax_nan(__fsub_rn(v[k][i], st.m), -3.402823466e38f);
-          const float e = exp2_approx(__fmaf_rn(v[k][i], kLog2e, -mL));
-          sa[i] = __fadd_rn(sa[i], e);
-          ua[i] = __fmaf_rn(e, d, ua[i]);
+        for (int h = 0; h < 2; ++h) {
+          uint64_t d2 = sub2(pk2(v[k][2 * h], v[k][2 * h + 1]), mm);
+          if (kScaled) {
+            float da, db;
+            upk2(d2, da, db);  // finite before scaling: -inf * a negative 1/tau low part
+            d2 = pk2(fmax_nan(da, -3.402823466e38f), fmax_nan(db, -3.402823466e38f));
+            d2 = fma2(d2, il, mul2(d2, ih));
+          }
+          uint64_t dc2, f2;
+          const uint64_t fme2 = count_minus_exp2(d2, dc2, f2);
+          sn2[h] = add2(sn2[h], fme2);
+          c2[h] = add2(c2[h], f2);
+          un2[h] = fma2(fme2, dc2, un2[h]);
         }
-      st.s = __fadd_rn(st.s, __fadd_rn(__fadd_rn(sa[0], sa[1]), __fadd_rn(sa[2], sa[3])));
-      st.u = __fadd_rn(st.u, __fadd_rn(__fadd_rn(ua[0], ua[1]), __fadd_rn(ua[2], ua[3])));
+      float sa[4], ca[4], ua[4];
+      upk2(sn2[0], sa[0], sa[1]);
+      upk2(sn2[1], sa[2], sa[3]);
+      upk2(c2[0], ca[0], ca[1]);
+      upk2(c2[1], ca[2], ca[3]);
+      upk2(un2[0], ua[0], ua[1]);
+      upk2(un2[1], ua[2], ua[3]);
+      st.s = __fsub_rn(st.s, __fadd_rn(__fadd_rn(sa[0], sa[1]), __fadd_rn(sa[2], sa[3])));
+      st.c = __fadd_rn(st.c, __fadd_rn(__fadd_rn(ca[0], ca[1]), __fadd_rn(ca[2], ca[3])));
+      st.u = __fsub_rn(st.u, __fadd_rn(__fadd_rn(ua[0], ua[1]), __fadd_rn(ua[2], ua[3])));
     }
   }
 
-  // CTA maximum (order-free), then rebase and fixed-tree sums.
-  float m = st.m;
+  // CTA maximum (order-free), then every thread's sum rebased to it as a float
+  // pair and the pairs summed in a fixed tree (shuffles, then the 8 warp sums
+  // in a fixed pairing).
+  float M = st.m;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-  if (lane == 0) red_m[warp] = m;
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  if (lane == 0) red_m[warp] = M;
   __syncthreads();
-  float M = red_m[0];
+  M = red_m[0];
 #pragma unroll
   for (int i = 1; i < kWarps; ++i) M = fmaxf(M, red_m[i]);
 
-  float s, u;
-  if (M == neg_inf()) {
-    s = 0.f;
-    u = 0.f;
-  } else {
-    rebase(st.m, st.s, st.u, M, s, u);
+  float hi = 0.f, lo = 0.f, u = 0.f;
+  if (st.m != neg_inf()) {
+    const float delta = scale_diff(__fsub_rn(st.m, M), inv_hi, inv_lo);
+    const float a = exp_neg(delta);  // 1 for the thread(s) holding the maximum
+    float thi, tlo;
+    two_sum(st.c, st.s, thi, tlo);
+    mul_pair(a, thi, tlo, hi, lo);
+    u = __fmul_rn(a, __fmaf_rn(delta, thi, st.u));
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
-    s = __fadd_rn(s, __shfl_down_sync(0xffffffffu, s, off));
+    const float ohi = __shfl_down_sync(0xffffffffu, hi, off);
+    const float olo = __shfl_down_sync(0xffffffffu, lo, off);
     u = __fadd_rn(u, __shfl_down_sync(0xffffffffu, u, off));
+    add_pair(hi, lo, ohi, olo, hi, lo);
   }
   if (lane == 0) {
-    red_s[warp] = s;
+    red_hi[warp] = hi;
+    red_lo[warp] = lo;
     red_u[warp] = u;
   }
   __syncthreads();
   if (tid == 0) {
     static_assert(kWarps == 8, "fixed pairing below assumes 8 warps");
-    S_out = __fadd_rn(__fadd_rn(__fadd_rn(red_s[0], red_s[1]), __fadd_rn(red_s[2], red_s[3])),
-                      __fadd_rn(__fadd_rn(red_s[4], red_s[5]), __fadd_rn(red_s[6], red_s[7])));
-    U_out = __fadd_rn(__fadd_rn(__fadd_rn(red_u[0], red_u[1]), __fadd_rn(red_u[2], red_u[3])),
+    float h01, l01, h23, l23, h45, l45, h67, l67, h03, l03, h47, l47;
+    add_pair(red_hi[0], red_lo[0], red_hi[1], red_lo[1], h01, l01);
+    add_pair(red_hi[2], red_lo[2], red_hi[3], red_lo[3], h23, l23);
+    add_pair(red_hi[4], red_lo[4], red_hi[5], red_lo[5], h45, l45);
+    add_pair(red_hi[6], red_lo[6], red_hi[7], red_lo[7], h67, l67);
+    add_pair(h01, l01, h23, l23, h03, l03);
+    add_pair(h45, l45, h67, l67, h47, l47);
+    add_pair(h03, l03, h47, l47, out.s_hi, out.s_lo);
+    out.u = __fadd_rn(__fadd_rn(__fadd_rn(red_u[0], red_u[1]), __fadd_rn(red_u[2], red_u[3])),
                       __fadd_rn(__fadd_rn(red_u[4], red_u[5]), __fadd_rn(red_u[6], red_u[7])));
-    M_out = M;
+    out.m = M;
   }
 }
 
-// Target logit of a quarter: z[y] * inv_tau if y is in [c0, c1), -inf if y is
-// another valid column, NaN if y is outside [0, V).
+// RAW target logit of a quarter: z[y] if y is in [c0, c1), -inf if y is
+// another valid column, NaN if y is outside [0, V).  The load is issued before
+// the quarter's stream of loads (asm volatile keeps it there), so its latency
+// is hidden by the reduction.
 __device__ __forceinline__ float quarter_target(const float* __restrict__ q0, int64_t y,
-                                                int64_t c0, int64_t c1, int64_t V,
-                                                float inv_tau) {
+                                                int64_t c0, int64_t c1, int64_t V) {
   if (y < 0 || y >= V) return quiet_nan();
-  if (y >= c0 && y < c1) return __fmul_rn(__ldg(q0 + (y - c0)), inv_tau);
+  if (y >= c0 && y < c1) {
+    float t;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(t) : "l"(q0 + (y - c0)));
+    return t;
+  }
   return neg_inf();
 }
 
-__device__ __forceinline__ void quarter_state_any(const float* __restrict__ q0, int64_t w,
-                                                  float inv_tau, float& M, float& S, float& U) {
-  if (inv_tau == 1.f)
-    quarter_state<false>(q0, w, inv_tau, M, S, U);
+// Quarter state of the w columns at q0 (thread 0 holds it), the target taken
+// from targets[row]; temperature tau with 1/tau = inv_hi + inv_lo.
+__device__ __forceinline__ QuarterState quarter_state_any(const float* __restrict__ q0, int64_t w,
+                                                          const int64_t* __restrict__ targets,
+                                                          int64_t row, int64_t c0, int64_t V,
+                                                          const TauArgs& tau) {
+  float t = 0.f;
+  if (threadIdx.x == 0) t = quarter_target(q0, targets[row], c0, c0 + w, V);
+  QuarterState st{};
+  if (tau.inv_hi == 1.f && tau.inv_lo == 0.f)
+    quarter_state<false>(q0, w, tau.inv_hi, tau.inv_lo, st);
   else
-    quarter_state<true>(q0, w, inv_tau, M, S, U);
+    quarter_state<true>(q0, w, tau.inv_hi, tau.inv_lo, st);
+  if (threadIdx.x == 0) {
+    st.t = t;
+    st.tau = tau.tau;
+  }
+  return st;
 }
 
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads)
     lp_logits_final_kernel(const float* __restrict__ logits, int64_t ld,
-                           const int64_t* __restrict__ targets, int64_t V, float inv_tau,
+                           const int64_t* __restrict__ targets, int64_t T, int64_t V, TauArgs tau,
                            float* __restrict__ logp, float* __restrict__ entropy) {
-  __shared__ float4 qstates[kQuarters];
+  __shared__ __align__(16) QuarterState qstates[kQuarters];
   const int q = blockIdx.x & 3;
   const int64_t row = blockIdx.x >> 2;
   const int64_t c0 = quarter_begin(V, q);
-  const int64_t c1 = quarter_begin(V, q + 1);
-  const float* q0 = logits + row * ld + c0;
+  int64_t c1 = quarter_begin(V, q + 1);
+  // checked build: the row exists and its quarter lies inside the row stride
+  // (a failed test reads nothing: an empty quarter of row 0)
+  const bool geo_ok = LP_CHECK(row < T && c1 <= ld, row < T ? kChkLogitsLoad : kChkRowIndex);
+  const int64_t r = geo_ok ? row : 0;
+  if (!geo_ok) c1 = c0;
+  const float* q0 = logits + r * ld + c0;
 
-  float M, S, U;
-  quarter_state_any(q0, c1 - c0, inv_tau, M, S, U);
+  const QuarterState st = quarter_state_any(q0, c1 - c0, targets, r, c0, V, tau);
   if (threadIdx.x == 0) {
-    const float t = quarter_target(q0, targets[row], c0, c1, V, inv_tau);
     const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(&qstates[q]));
     uint32_t remote;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(0));
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(M),
-                 "f"(S), "f"(U), "f"(t)
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote), "f"(st.m),
+                 "f"(st.s_hi), "f"(st.s_lo), "f"(st.u)
+                 : "memory");
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(remote + 16u),
+                 "f"(st.t), "f"(st.tau), "f"(0.f), "f"(0.f)
                  : "memory");
   }
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-  if (q == 0 && threadIdx.x == 0) {
-    const float4 qs[kQuarters] = {qstates[0], qstates[1], qstates[2], qstates[3]};
-    float lp, ent;
-    finalise(qs, lp, ent);
-    logp[row] = lp;
-    if (entropy != nullptr) entropy[row] = ent;
+  if (q == 0 && threadIdx.x < 4) {
+    const QuarterState mine = load_state(&qstates[threadIdx.x]);
+    float lp, ent, lz;
+    finalise_quad(mine, 0xfu, lp, ent, lz);
+    if (threadIdx.x == 0 && geo_ok) {
+      logp[row] = lp;
+      if (entropy != nullptr) entropy[row] = ent;
+    }
   }
 }
 
 __global__ void __launch_bounds__(kThreads)
     lp_logits_partials_kernel(const float* __restrict__ logits_shard, int64_t ld,
-                              const int64_t* __restrict__ targets, int64_t V, int q_first,
-                              int n_q, float inv_tau, float4* __restrict__ partials) {
+                              const int64_t* __restrict__ targets, int64_t T, int64_t V,
+                              int q_first, int n_q, TauArgs tau,
+                              QuarterState* __restrict__ partials) {
   const int ql = blockIdx.x % n_q;
   const int64_t row = blockIdx.x / n_q;
   const int q = q_first + ql;
   const int64_t shard_c0 = quarter_begin(V, q_first);
   const int64_t c0 = quarter_begin(V, q);
-  const int64_t c1 = quarter_begin(V, q + 1);
-  const float* q0 = logits_shard + row * ld + (c0 - shard_c0);
+  int64_t c1 = quarter_begin(V, q + 1);
+  const bool geo_ok =
+      LP_CHECK(row < T && c1 - shard_c0 <= ld, row < T ? kChkLogitsLoad : kChkRowIndex);
+  const int64_t r = geo_ok ? row : 0;
+  if (!geo_ok) c1 = c0;
+  const float* q0 = logits_shard + r * ld + (c0 - shard_c0);
 
-  float M, S, U;
-  quarter_state_any(q0, c1 - c0, inv_tau, M, S, U);
-  if (threadIdx.x == 0) {
-    const float t = quarter_target(q0, targets[row], c0, c1, V, inv_tau);
-    partials[row * n_q + ql] = make_float4(M, S, U, t);
-  }
+  const QuarterState st = quarter_state_any(q0, c1 - c0, targets, r, c0, V, tau);
+  if (threadIdx.x == 0 && geo_ok && LP_CHECK(row * n_q + ql < T * n_q, kChkStateIndex))
+    store_state(&partials[row * n_q + ql], st);
 }
 
-__global__ void lp_merge_partials_kernel(const float4* __restrict__ p0,
-                                         const float4* __restrict__ p1,
-                                         const float4* __restrict__ p2,
-                                         const float4* __restrict__ p3, int n_shards,
-                                         int64_t T, float* __restrict__ logp,
-                                         float* __restrict__ entropy) {
-  const int64_t row = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (row >= T) return;
-  const float4* shard[4] = {p0, p1, p2, p3};
+// One thread per (row, quarter), four consecutive lanes per row.
+__global__ void __launch_bounds__(128)
+    lp_merge_partials_kernel(const QuarterState* __restrict__ p0,
+                             const QuarterState* __restrict__ p1,
+                             const QuarterState* __restrict__ p2,
+                             const QuarterState* __restrict__ p3, int n_shards, int64_t T,
+                             float* __restrict__ logp, float* __restrict__ entropy) {
+  const int64_t row = int64_t(blockIdx.x) * (blockDim.x / 4) + (threadIdx.x >> 2);
+  const int q = threadIdx.x & 3;
+  const QuarterState* shard[4] = {p0, p1, p2, p3};
   const int per = kQuarters / n_shards;
-  float4 qs[kQuarters];
-#pragma unroll
-  for (int q = 0; q < kQuarters; ++q) qs[q] = shard[q / per][row * per + (q % per)];
-  float lp, ent;
-  finalise(qs, lp, ent);
-  logp[row] = lp;
-  if (entropy != nullptr) entropy[row] = ent;
+  QuarterState st{neg_inf(), 0.f, 0.f, 0.f, neg_inf(), 1.f, 0.f, 0.f};
+  if (row < T &&
+      LP_CHECK(q / per < n_shards && row * per + (q % per) < T * per, kChkStateIndex))
+    st = load_state(&shard[q / per][row * per + (q % per)]);
+  float lp, ent, lz;
+  finalise_quad(st, 0xffffffffu, lp, ent, lz);
+  if (row < T && q == 0) {
+    logp[row] = lp;
+    if (entropy != nullptr) entropy[row] = ent;
+  }
 }
 
 }  // namespace
 
 lp_status launch_logits_final(const float* logits, int64_t ld, const int64_t* targets,
-                              int64_t T, int64_t V, float inv_tau, float* logp, float* entropy,
-                              cudaStream_t stream) {
+                              int64_t T, int64_t V, const TauArgs& tau, float* logp,
+                              float* entropy, cudaStream_t stream) {
   const int64_t blocks = T * kQuarters;
   lp_logits_final_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-      logits, ld, targets, V, inv_tau, logp, entropy);
+      logits, ld, targets, T, V, tau, logp, entropy);
   return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }
 
 lp_status launch_logits_partials(const float* logits_shard, int64_t ld,
                                  const int64_t* targets, int64_t T, int64_t V_total,
-                                 int q_first, int n_q, float inv_tau, float* partials,
+                                 int q_first, int n_q, const TauArgs& tau, float* partials,
                                  cudaStream_t stream) {
   const int64_t blocks = T * n_q;
   lp_logits_partials_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-      logits_shard, ld, targets, V_total, q_first, n_q, inv_tau,
-      reinterpret_cast<float4*>(partials));
+      logits_shard, ld, targets, T, V_total, q_first, n_q, tau,
+      reinterpret_cast<QuarterState*>(partials));
   return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }
 
 lp_status launch_merge_partials(const float* const* shard_partials, int n_shards, int64_t T,
                                 float* logp, float* entropy, cudaStream_t stream) {
-  const float4* p[4] = {nullptr, nullptr, nullptr, nullptr};
-  for (int i = 0; i < n_shards; ++i) p[i] = reinterpret_cast<const float4*>(shard_partials[i]);
-  const int threads = 128;
-  const int64_t blocks = (T + threads - 1) / threads;
+  const QuarterState* p[4] = {nullptr, nullptr, nullptr, nullptr};
+  for (int i = 0; i < n_shards; ++i)
+    p[i] = reinterpret_cast<const QuarterState*>(shard_partials[i]);
+  const int threads = 128;  // 32 rows per block, one thread per quarter
+  const int64_t blocks = (T + threads / 4 - 1) / (threads / 4);
   lp_merge_partials_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
       p[0], p[1], p[2], p[3], n_shards, T, logp, entropy);
   return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }
 
+}  // namespace lp
+
+namespace lp {
+cudaError_t take_check_word_logits(uint32_t* out) { return take_check_word(out); }
 }  // namespace lp

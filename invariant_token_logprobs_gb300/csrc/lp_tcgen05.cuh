@@ -38,6 +38,7 @@
 
 #include <cstdint>
 
+#include "lp_check.cuh"
 #include "lp_internal.h"
 
 namespace lp {
@@ -369,8 +370,11 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
             pending |= 1u << stage;
             pending_parity = (pending_parity & ~(1u << stage)) | (phase << stage);
           }
-          const bool withheld = withhold_first_load != 0 && pair == 0 && rank == 0 &&
-                                u == pair && kb == kb0;
+          // checked build: a negative coordinate is recorded and its copy
+          // withheld (the stage's bounded waits then give up: no fault)
+          const bool withheld = (withhold_first_load != 0 && pair == 0 && rank == 0 &&
+                                 u == pair && kb == kb0) ||
+                                !LP_CHECK(a_row >= 0 && b_row >= 0 && kb >= 0, kChkTmaCoord);
           if (!withheld) {
             if (kAMn) {
               tma_load_2d(sa, tmA, a_row, kb * kBK, leader_full);
@@ -494,6 +498,10 @@ bool encode_bf16_2d(CUtensorMap* map, const void* base, int64_t rows, int64_t co
 // stride that is not a multiple of 16 bytes).
 bool encode_f32_3d_store(CUtensorMap* map, void* base, int64_t S, int64_t rows, int64_t cols,
                          int64_t ld, int64_t split_stride);
+
+// The same over bf16 [S, rows, cols] with 64 x 32 x 1 boxes (128-byte rows).
+bool encode_bf16_3d_store(CUtensorMap* map, void* base, int64_t S, int64_t rows, int64_t cols,
+                          int64_t ld, int64_t split_stride);
 
 // Persistent grid (in CTAs, even) for `units` units on `sm_count` SMs under the
 // process-wide CTA limit: one CTA pair per two SMs, never more pairs than units.

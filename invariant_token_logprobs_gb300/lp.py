@@ -24,6 +24,7 @@ from . import _build_lib
 __all__ = [
     "LpError",
     "STATUS",
+    "STATE_FLOATS",
     "load",
     "declared_symbols",
     "lp_logprob_from_logits",
@@ -42,12 +43,16 @@ __all__ = [
     "lp_linear_logprob_backward_workspace_size",
     "lp_linear_logprob_lse",
     "lp_linear_logprob_backward",
+    "lp_linear_logprob_backward_ex",
+    "GRAD_W_FLOAT32",
+    "GRAD_W_BFLOAT16",
     "linear_logprob_lse",
     "linear_logprob_backward",
     "lp_get_device_error",
     "lp_set_persistent_grid_limit",
     "lp_set_kernel_timing_events",
     "lp_set_fault_injection",
+    "lp_get_check_word",
     "lp_status_string",
     "lp_backend_id",
     "logprob_from_logits",
@@ -57,6 +62,9 @@ __all__ = [
     "linear_logprob_partials",
     "vocab_shard_range",
 ]
+
+# floats per quarter state in the partials layout [T][quarters][STATE_FLOATS]
+STATE_FLOATS = 8
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "lp.h")
 
@@ -111,10 +119,14 @@ _SIGNATURES = {
     "lp_linear_logprob_backward": (
         _int, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, ctypes.c_float, _vp, _vp, _vp, _vp,
                _vp, _vp, _vp, _sz, _vp]),
+    "lp_linear_logprob_backward_ex": (
+        _int, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, ctypes.c_float, _vp, _vp, _vp, _vp,
+               _vp, _vp, _int, _vp, _sz, _vp]),
     "lp_get_device_error": (_int, [_vp, _sz, ctypes.POINTER(ctypes.c_uint32), _vp]),
     "lp_set_persistent_grid_limit": (_int, [_int]),
     "lp_set_kernel_timing_events": (_int, [_vp, _vp]),
     "lp_set_fault_injection": (_int, [_int]),
+    "lp_get_check_word": (_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "lp_status_string": (ctypes.c_char_p, [_int]),
     "lp_backend_id": (ctypes.c_char_p, []),
 }
@@ -320,6 +332,30 @@ def lp_linear_logprob_backward(H, W, targets, temperature, saved_lse, saved_entr
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
+GRAD_W_FLOAT32 = 0
+GRAD_W_BFLOAT16 = 1
+
+
+def lp_linear_logprob_backward_ex(H, W, targets, temperature, saved_lse, saved_entropy,
+                                  grad_logp, grad_entropy, grad_H, grad_W, workspace,
+                                  stream=None) -> None:
+    """The backward with grad_W float32 or bfloat16 (taken from grad_W's dtype)."""
+    _check_bf16(H, W, targets)
+    T, d = H.shape
+    V = W.shape[0]
+    dtype = GRAD_W_FLOAT32
+    if grad_W is not None:
+        if grad_W.dtype == torch.bfloat16:
+            dtype = GRAD_W_BFLOAT16
+        elif grad_W.dtype != torch.float32:
+            raise TypeError("grad_W must be float32 or bfloat16")
+    _check("lp_linear_logprob_backward_ex", load().lp_linear_logprob_backward_ex(
+        _ptr(H), _row_stride(H), _ptr(W), _row_stride(W), _ptr(targets), T, d, V,
+        float(temperature), _ptr(saved_lse), _ptr(saved_entropy), _ptr(grad_logp),
+        _ptr(grad_entropy), _ptr(grad_H), _ptr(grad_W), dtype, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
 def linear_logprob_lse(H, W, y, temperature: float = 1.0, workspace=None, stream=None):
     """(logp, entropy, lse) [T] fp32 of the fused path; keep entropy and lse for the backward."""
     T, d = H.shape
@@ -333,16 +369,20 @@ def linear_logprob_lse(H, W, y, temperature: float = 1.0, workspace=None, stream
 
 def linear_logprob_backward(H, W, y, grad_logp=None, grad_entropy=None, temperature: float = 1.0,
                             with_grad_W: bool = True, saved_lse=None, saved_entropy=None,
-                            workspace=None, stream=None):
-    """(grad_H [T, d] fp32, grad_W [V, d] fp32 or None) of the fused path."""
+                            workspace=None, stream=None, grad_W_dtype=torch.float32):
+    """(grad_H [T, d] fp32, grad_W [V, d] fp32 / bf16 or None) of the fused path."""
     T, d = H.shape
     V = W.shape[0]
     if workspace is None:
         workspace = _workspace(lp_linear_logprob_backward_workspace_size(T, d, V), H.device)
     gH = torch.empty((T, d), dtype=torch.float32, device=H.device)
-    gW = torch.empty((V, d), dtype=torch.float32, device=H.device) if with_grad_W else None
-    lp_linear_logprob_backward(H, W, y, temperature, saved_lse, saved_entropy, grad_logp,
-                               grad_entropy, gH, gW, workspace, stream)
+    gW = torch.empty((V, d), dtype=grad_W_dtype, device=H.device) if with_grad_W else None
+    if grad_W_dtype == torch.float32:
+        lp_linear_logprob_backward(H, W, y, temperature, saved_lse, saved_entropy, grad_logp,
+                                   grad_entropy, gH, gW, workspace, stream)
+    else:
+        lp_linear_logprob_backward_ex(H, W, y, temperature, saved_lse, saved_entropy, grad_logp,
+                                      grad_entropy, gH, gW, workspace, stream)
     return gH, gW
 
 
@@ -369,6 +409,14 @@ def lp_set_kernel_timing_events(start_event=None, stop_event=None) -> None:
 
 def lp_set_fault_injection(mode: int) -> None:
     _check("lp_set_fault_injection", load().lp_set_fault_injection(mode))
+
+
+def lp_get_check_word() -> int:
+    """The OR of the check words of the checked build since the last read (0 in
+    the normal build); synchronises the device."""
+    word = ctypes.c_uint32(0)
+    _check("lp_get_check_word", load().lp_get_check_word(ctypes.byref(word)))
+    return int(word.value)
 
 
 def lp_status_string(status: int) -> str:
@@ -405,7 +453,8 @@ def vocab_shard_range(vocab_total: int, shard_index: int, n_shards: int) -> tupl
 def logprob_partials_from_logits(z_shard, y, vocab_total, shard_index, n_shards, stream=None,
                                  temperature: Optional[float] = None):
     T = z_shard.shape[0]
-    partials = torch.empty((T, 4 // n_shards, 4), dtype=torch.float32, device=z_shard.device)
+    partials = torch.empty((T, 4 // n_shards, STATE_FLOATS), dtype=torch.float32,
+                           device=z_shard.device)
     if temperature is None:
         lp_logprob_partials_from_logits(z_shard, y, vocab_total, shard_index, n_shards, partials,
                                         stream)
@@ -445,7 +494,7 @@ def linear_logprob_partials(H, W_shard, y, vocab_total, shard_index, n_shards, w
     if workspace is None:
         workspace = _workspace(
             lp_linear_logprob_partials_workspace_size(T, d, vocab_total, n_shards), H.device)
-    partials = torch.empty((T, 4 // n_shards, 4), dtype=torch.float32, device=H.device)
+    partials = torch.empty((T, 4 // n_shards, STATE_FLOATS), dtype=torch.float32, device=H.device)
     if temperature is None:
         lp_linear_logprob_partials(H, W_shard, y, vocab_total, shard_index, n_shards, partials,
                                    workspace, stream)

@@ -38,3 +38,15 @@ def max_err(gpu: torch.Tensor, ref: np.ndarray) -> float:
 
 def bits(t: torch.Tensor) -> torch.Tensor:
     return t.contiguous().view(torch.int32).cpu()
+
+
+def excess_over_rounding(gpu: torch.Tensor, ref: np.ndarray) -> float:
+    """Largest |gpu - ref| beyond half an ulp of the float32 nearest ref, over
+    the finite entries: what an output that is ref correctly rounded to float32
+    would show as 0."""
+    g = gpu.double().cpu().numpy()
+    ok = np.isfinite(ref) & np.isfinite(g)
+    r = ref[ok]
+    half_ulp = np.spacing(np.abs(r).astype(np.float32)).astype(np.float64) / 2
+    ex = np.abs(g[ok] - r) - half_ulp
+    return float(max(ex.max(), 0.0)) if ex.size else 0.0

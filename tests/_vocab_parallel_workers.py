@@ -1,0 +1,63 @@
+"""Rank processes of the vocabulary-parallel tests (spawned by
+tests/test_vocab_parallel_host.py and tests/test_gpu_vocab_parallel.py)."""
+
+from __future__ import annotations
+
+import os
+
+import torch
+import torch.distributed as dist
+
+
+def _init(rank: int, world: int, init_file: str) -> None:
+    # a file rendezvous: no TCP port to pick or to collide on
+    dist.init_process_group("gloo", init_method=f"file://{init_file}", rank=rank,
+                            world_size=world)
+
+
+def host_gather(rank: int, world: int, init_file: str, out_dir: str) -> None:
+    """Each rank contributes a [T, 4 / world, 8] state tensor whose bytes name
+    the rank (with -inf and NaN payloads among them); the gathered tensors are
+    saved for the parent to check."""
+    from invariant_token_logprobs_gb300 import vocab_parallel as vp
+    _init(rank, world, init_file)
+    try:
+        T, nq = 5, 4 // world
+        bits = torch.arange(T * nq * 8, dtype=torch.int32).view(T, nq, 8) + (rank << 20)
+        bits[0, 0, 0] = 0x7FC00000 + rank  # NaN with a payload
+        bits[1, 0, 4] = -8388608            # -inf (0xff800000)
+        part = bits.view(torch.float32)
+        got = vp.gather_partials(part)
+        shard = vp.shard_of_rank(151936)
+        torch.save({"got": [g.view(torch.int32).clone() for g in got], "shard": shard},
+                   os.path.join(out_dir, f"rank{rank}.pt"))
+    finally:
+        dist.destroy_process_group()
+
+
+def gpu_vocab_parallel(rank: int, world: int, init_file: str, out_dir: str, path: str) -> None:
+    """Every rank on cuda:0: its shard's partial states, an all-gather over
+    gloo (host-staged), the fixed merge.  Saves logp and entropy."""
+    from invariant_token_logprobs_gb300 import lp, synth
+    from invariant_token_logprobs_gb300 import vocab_parallel as vp
+    _init(rank, world, init_file)
+    try:
+        torch.cuda.set_device(0)
+        lp.load(build_if_needed=False)
+        if path == "fused":
+            x = synth.fused_inputs("fused_qwen3_next", device="cuda:0")
+            V = x.W.shape[0]
+            _, n, b, e = vp.shard_of_rank(V)
+            w_shard = x.W[b:e]
+            del x.W
+            logp, ent = vp.vocab_parallel_linear_logprob(x.H, w_shard, x.y, V)
+        else:
+            x = synth.logits_inputs("logits_peaked", device="cuda:0")
+            V = x.z.shape[1]
+            _, n, b, e = vp.shard_of_rank(V)
+            logp, ent = vp.vocab_parallel_logprob_from_logits(x.z[:, b:e], x.y, V,
+                                                              temperature=0.7)
+        torch.cuda.synchronize()
+        torch.save({"logp": logp.cpu(), "ent": ent.cpu()}, os.path.join(out_dir, f"rank{rank}.pt"))
+    finally:
+        dist.destroy_process_group()

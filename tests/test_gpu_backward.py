@@ -2,11 +2,17 @@
 oracle, determinism, and row invariance of grad_H.
 
 Tolerance (from the arithmetic): the kernel forms G = dL/dz in fp32 and rounds
-it to bf16 (relative error <= 2^-9) before two tensor-core products with fp32
-accumulation (whose error over K <= 151936 terms is far below that), so an
-element of grad_H = G W may be off by at most about 2^-9 sum_v |G[t,v] W[v,k]|
-and one of grad_W = G^T H by 2^-9 sum_t |G[t,v] H[t,k]|.  The tests allow
-2^-8 times those sums (computed in fp64 from the oracle's G) plus 1e-6.
+it to bf16 before two tensor-core products with fp32 accumulation.  bf16 keeps
+8 significant bits, so its round-to-nearest error is at most 2^-8 relative
+(the unit roundoff of an 8-bit significand); a product term G[t,v] X[.,k] then
+carries at most 2^-8 |G X| of error.  The products add at most about
+n 2^-24 sum |terms| for n terms summed in one fp32 chain: grad_H = G W sums
+V terms in 16 fixed ranges (n = V/16 + 16), grad_W = G^T H sums T terms
+(n = T).  So the tests allow (2^-8 + n 2^-24) sum |G X| + 1e-6 per element,
+the sums taken in fp64 from the oracle's G.  These are absolute-sum bounds:
+they hold also where the terms cancel (the entropy-only gradient, whose rows
+of G sum to zero).  A bf16 grad_W must be the fp32 grad_W of the same call
+rounded to nearest even, bit for bit.
 """
 
 import numpy as np
@@ -39,7 +45,7 @@ def _np(t):
     return None if t is None else t.double().cpu().numpy()
 
 
-def _check_against_oracle(x, gl, ge, tau, gH, gW, rows=None):
+def _check_against_oracle(x, gl, ge, tau, gH, gW, rows=None, w_cols=97):
     h = x.H.float().cpu().numpy().astype(np.float64)
     w = x.W.float().cpu().numpy().astype(np.float64)
     y = x.y.cpu().numpy()
@@ -53,20 +59,23 @@ def _check_against_oracle(x, gl, ge, tau, gH, gW, rows=None):
     del z
     r = np.arange(T) if rows is None else np.asarray(rows)
     ref_h = G[r] @ w
-    bound_h = 2.0 ** -8 * (np.abs(G[r]) @ np.abs(w)) + 1e-6
+    bound_h = (2.0 ** -8 + (w.shape[0] / 16 + 16) * 2.0 ** -24) * (np.abs(G[r]) @ np.abs(w)) + 1e-6
     got_h = gH[torch.as_tensor(r)].double().cpu().numpy()
     err_h = np.abs(got_h - ref_h)
     assert np.all(err_h <= bound_h), (float(err_h.max()), float((err_h / bound_h).max()))
     out = {"grad_H_max_err": float(err_h.max()), "grad_H_max_ratio": float((err_h / bound_h).max())}
     if gW is not None:
-        vs = np.unique(np.concatenate([np.arange(0, w.shape[0], max(1, w.shape[0] // 97)),
-                                       y[y < w.shape[0]][:16]]))
+        spread = np.arange(0, w.shape[0], max(1, w.shape[0] // w_cols))
+        targets = y[(y >= 0) & (y < w.shape[0])]
+        vs = np.unique(np.concatenate([spread, targets if w_cols > 97 else targets[:16]]))
         ref_w = G[:, vs].T @ h
-        bound_w = 2.0 ** -8 * (np.abs(G[:, vs]).T @ np.abs(h)) + 1e-6
+        bound_w = (2.0 ** -8 + T * 2.0 ** -24) * (np.abs(G[:, vs]).T @ np.abs(h)) + 1e-6
         got_w = gW[torch.as_tensor(vs)].double().cpu().numpy()
         err_w = np.abs(got_w - ref_w)
         assert np.all(err_w <= bound_w), (float(err_w.max()), float((err_w / bound_w).max()))
         out["grad_W_max_err"] = float(err_w.max())
+        out["grad_W_max_ratio"] = float((err_w / bound_w).max())
+        out["grad_W_columns"] = int(vs.size)
     return out
 
 
@@ -111,13 +120,41 @@ def test_backward_one_upstream_and_bad_targets():
     assert none is None and torch.isfinite(gH).all()
 
 
-def test_backward_qwen3_8b_head_sampled():
+def test_backward_qwen3_8b_head_all_rows():
+    """The headline shape: every row of grad_H, and 1024 spread columns of
+    grad_W plus every target column."""
     x = synth.fused_inputs("fused_qwen3_8b", device=DEV)
     gl, ge = _upstream(512, seed=2)
     gH, gW = lp.linear_logprob_backward(x.H, x.W, x.y, gl, ge)
     torch.cuda.synchronize()
-    out = _check_against_oracle(x, gl, ge, 1.0, gH, gW, rows=[0, 255, 256, 511])
+    out = _check_against_oracle(x, gl, ge, 1.0, gH, gW, w_cols=1024)
     print(f"qwen3-8b head backward: {out}")
+
+
+def test_backward_qwen3_8b_head_entropy_only():
+    """Entropy gradient alone: every row of G sums to zero (heavy cancellation
+    in both products); the absolute-sum bound must still hold."""
+    x = synth.fused_inputs("fused_qwen3_8b", device=DEV)
+    _, ge = _upstream(512, seed=3, with_logp=False)
+    gH, gW = lp.linear_logprob_backward(x.H, x.W, x.y, None, ge)
+    torch.cuda.synchronize()
+    out = _check_against_oracle(x, None, ge, 1.0, gH, gW, w_cols=1024)
+    print(f"qwen3-8b head backward, entropy only: {out}")
+
+
+@pytest.mark.parametrize("T,d,V", [(300, 128, 20003), (5, 64, 3001), (512, 4096, 151936)])
+def test_backward_bf16_grad_W_is_rounded_fp32(T, d, V):
+    """grad_W in bf16 holds the fp32 results of the same products rounded to
+    nearest even; grad_H is unchanged."""
+    spec = "fused_qwen3_8b" if d == 4096 else "fused_tiny"
+    x = synth.fused_inputs(spec, device=DEV, T=T, d=d, V=V, seed=T + 1)
+    gl, ge = _upstream(T, seed=11)
+    h32, w32 = lp.linear_logprob_backward(x.H, x.W, x.y, gl, ge)
+    h16, w16 = lp.linear_logprob_backward(x.H, x.W, x.y, gl, ge, grad_W_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert w16.dtype == torch.bfloat16
+    assert torch.equal(bits(h16.reshape(-1)), bits(h32.reshape(-1)))
+    assert torch.equal(w16.view(torch.int16), w32.to(torch.bfloat16).view(torch.int16))
 
 
 def test_backward_with_saved_forward_statistics():

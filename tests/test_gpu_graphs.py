@@ -103,7 +103,7 @@ def test_sharded_merge_graph_replay_bytes_equal_eager():
     d, V, T = 512, 151936, 8
     x = synth.fused_inputs("fused_qwen3_next", device=DEV, T=T, d=d, V=V, seed=3)
     ranges = [lp.vocab_shard_range(V, i, 4) for i in range(4)]
-    parts = [torch.empty((T, 1, 4), device=DEV) for _ in range(4)]
+    parts = [torch.empty((T, 1, lp.STATE_FLOATS), device=DEV) for _ in range(4)]
     wss = [torch.empty(lp.lp_linear_logprob_partials_workspace_size(T, d, V, 4), dtype=torch.uint8,
                        device=DEV) for _ in range(4)]
     logp = torch.empty(T, device=DEV)
