@@ -59,6 +59,13 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
   return r;
 }
 
+// Three-operand max that returns NaN when any operand is NaN.
+__device__ __forceinline__ float fmax3_nan(float a, float b, float c) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // 1.0f when a >= b, else 0.0f (NaN compares false).
 __device__ __forceinline__ float ge_one_zero(float a, float b) {
   float r;
@@ -280,16 +287,90 @@ __device__ __forceinline__ void term(float x, float m, float inv_tau, float& e, 
   e = exp_fast(d);
 }
 
+// ------------------------------------------------ float-pair exp and log
+//
+// Values held as an unevaluated pair hi + lo of floats (|lo| <= ulp(hi) / 2),
+// about 44 significant bits, for the once-per-row finalisation.  Float64
+// transcendentals are slow on this GPU; these use only float operations.
+
+struct F2 {
+  float hi, lo;
+};
+
+__device__ __forceinline__ F2 f2_norm(float hi, float lo) {  // |hi| >= |lo|
+  const float s = __fadd_rn(hi, lo);
+  return F2{s, __fsub_rn(lo, __fsub_rn(s, hi))};
+}
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+  float s, e;
+  two_sum(a.hi, b.hi, s, e);
+  return f2_norm(s, __fadd_rn(e, __fadd_rn(a.lo, b.lo)));
+}
+__device__ __forceinline__ F2 f2_mul(F2 a, F2 b) {
+  const float p = __fmul_rn(a.hi, b.hi);
+  const float e = __fmaf_rn(a.hi, b.hi, -p);
+  return f2_norm(p, __fmaf_rn(a.hi, b.lo, __fmaf_rn(a.lo, b.hi, e)));
+}
+
+// e^x for x = x.hi + x.lo with -87 <= x.hi <= 0: n = round(x log2 e),
+// r = x - n ln2 (ln2 split in three, n L1 exact), e^r = 1 + r + r^2 P(r) with
+// P(r) = 1/2 + r (1/3! + r/4! + ... + r^6/9!) (Taylor, truncation < 1e-11 for
+// |r| <= ln2/2), the leading terms carried as pairs; e^x = e^r 2^n.
+// Relative error about 1e-10.
+constexpr float kLn2A = 0.693145751953125f;       // 16 significant bits
+constexpr float kLn2B = 1.4286068203094172e-06f;  // next 24 bits
+constexpr float kLn2C = 5.497923e-14f;            // remainder (ln2 - A - B)
+__device__ __forceinline__ F2 exp_f2(F2 x) {
+  const float t = __fmaf_rn(x.hi, kLog2e, kExpMagic);
+  const float n = __fsub_rn(t, kExpMagic);
+  const float r1 = __fmaf_rn(n, -kLn2A, x.hi);  // exact
+  const float pb = __fmul_rn(n, kLn2B);
+  const float pbe = __fmaf_rn(n, kLn2B, -pb);
+  F2 r;
+  two_sum(r1, -pb, r.hi, r.lo);
+  r = f2_norm(r.hi, __fadd_rn(r.lo, __fsub_rn(x.lo, __fmaf_rn(n, kLn2C, pbe))));
+  float q = 1.0f / 362880.0f;  // 1/9!
+  q = __fmaf_rn(q, r.hi, 1.0f / 40320.0f);
+  q = __fmaf_rn(q, r.hi, 1.0f / 5040.0f);
+  q = __fmaf_rn(q, r.hi, 1.0f / 720.0f);
+  q = __fmaf_rn(q, r.hi, 1.0f / 120.0f);
+  q = __fmaf_rn(q, r.hi, 1.0f / 24.0f);
+  q = __fmaf_rn(q, r.hi, 1.0f / 6.0f);
+  F2 P;
+  two_sum(0.5f, __fmul_rn(r.hi, q), P.hi, P.lo);
+  P.lo = __fadd_rn(P.lo, __fmaf_rn(r.hi, q, -__fmul_rn(r.hi, q)));
+  F2 r2;  // r^2 including 2 r.hi r.lo
+  r2.hi = __fmul_rn(r.hi, r.hi);
+  r2.lo = __fmaf_rn(r.hi, r.hi, -r2.hi);
+  r2.lo = __fmaf_rn(__fmul_rn(2.0f, r.hi), r.lo, r2.lo);
+  const F2 tail = f2_mul(r2, P);
+  F2 e = f2_add(F2{1.0f, 0.0f}, r);
+  e = f2_add(e, tail);
+  const float scale = __int_as_float(__float_as_int(t) << 23);  // 2^n
+  return F2{__fmul_rn(e.hi, scale), __fmul_rn(e.lo, scale)};
+}
+
+// log S for S = S.hi + S.lo >= 1 (finite): y = logf(S.hi) (CUDA's logf), then
+// one Newton step on e^y = S in pairs, log S = y + (S e^-y - 1) (the next
+// term, -(S e^-y - 1)^2 / 2, is below 1e-14).  Absolute error about 1e-10.
+__device__ __forceinline__ F2 log_f2(F2 S) {
+  const float y = logf(S.hi);
+  const F2 E = exp_f2(F2{-y, 0.0f});
+  const F2 w = f2_add(f2_mul(S, E), F2{-1.0f, 0.0f});
+  return f2_add(F2{y, 0.0f}, w);
+}
+
 // ------------------------------------------------------------- finalise
 //
 // The four quarter states of a row sit in four consecutive lanes of a warp
 // (lane & 3 == quarter); `mask` names every lane taking part (groups of four).
-// Each lane rebases its quarter to the row maximum in float64,
-//   a_q = exp((m_q - M) / tau),  S_q = a_q (s_hi + s_lo),
-//   U_q = a_q (u + (m_q - M) / tau (s_hi + s_lo)),
+// Each lane rebases its quarter to the row maximum with float pairs,
+//   delta_q = (m_q - M) / tau,  a_q = exp(delta_q),  S_q = a_q (s_hi + s_lo),
+//   U_q = a_q (u + delta_q (s_hi + s_lo)),
 // and the sums are formed as (Q0 + Q1) + (Q2 + Q3) with two xor-shuffles
-// (addition is commutative, so every lane of the group holds the same bits).
-// Every lane then has the row's logp, entropy and log Z = M / tau + log S.
+// (pair addition is commutative, so every lane of the group holds the same
+// bits).  Every lane then has the row's logp = (t - M) / tau - log S, entropy
+// = log S - U / S and log Z = M / tau + log S, each rounded to float once.
 // States of different temperatures, NaN anywhere, or no finite logit give NaN.
 __device__ __forceinline__ void finalise_quad(const QuarterState& q, unsigned mask, float& logp,
                                               float& entropy, float& log_z) {
@@ -304,31 +385,46 @@ __device__ __forceinline__ void finalise_quad(const QuarterState& q, unsigned ma
   same_tau &= __shfl_xor_sync(mask, same_tau, 1);
   same_tau &= __shfl_xor_sync(mask, same_tau, 2);
 
-  const double tau = static_cast<double>(q.tau);
-  double S = 0.0, U = 0.0;
-  if (q.m != neg_inf() && M == M) {
-    const double delta = __ddiv_rn(__dsub_rn(static_cast<double>(q.m), static_cast<double>(M)), tau);
-    const double a = exp(delta);
-    const double sq = __dadd_rn(static_cast<double>(q.s_hi), static_cast<double>(q.s_lo));
-    S = __dmul_rn(a, sq);
-    U = __dmul_rn(a, __fma_rn(delta, sq, static_cast<double>(q.u)));
-  }
-  S = __dadd_rn(S, __shfl_xor_sync(mask, S, 1));
-  U = __dadd_rn(U, __shfl_xor_sync(mask, U, 1));
-  S = __dadd_rn(S, __shfl_xor_sync(mask, S, 2));
-  U = __dadd_rn(U, __shfl_xor_sync(mask, U, 2));
+  // 1/tau as a pair (tau == 1: exactly 1, 0)
+  const float inv_hi = __frcp_rn(q.tau);
+  const float inv_lo = __fdiv_rn(__fmaf_rn(-inv_hi, q.tau, 1.0f), q.tau);
+  const F2 inv{inv_hi, inv_lo};
 
-  if (!same_tau || !(M > neg_inf()) || !(S > 0.0) || U != U) {  // NaN somewhere, or empty
+  F2 S{0.0f, 0.0f};
+  float U = 0.0f;
+  if (q.m != neg_inf() && M == M) {
+    F2 d;
+    two_sum(q.m, -M, d.hi, d.lo);  // exact
+    d = f2_mul(d, inv);
+    const F2 a = d.hi < kExpClampLo ? F2{0.0f, 0.0f} : exp_f2(d);
+    S = f2_mul(a, F2{q.s_hi, q.s_lo});
+    U = __fmul_rn(a.hi, __fmaf_rn(d.hi, q.s_hi, q.u));
+  }
+  F2 o;
+  o.hi = __shfl_xor_sync(mask, S.hi, 1);
+  o.lo = __shfl_xor_sync(mask, S.lo, 1);
+  S = f2_add(S, o);
+  U = __fadd_rn(U, __shfl_xor_sync(mask, U, 1));
+  o.hi = __shfl_xor_sync(mask, S.hi, 2);
+  o.lo = __shfl_xor_sync(mask, S.lo, 2);
+  S = f2_add(S, o);
+  U = __fadd_rn(U, __shfl_xor_sync(mask, U, 2));
+
+  if (!same_tau || !(M > neg_inf()) || !(S.hi > 0.0f) || U != U || S.hi != S.hi ||
+      S.hi > 3.402823466e38f) {  // NaN somewhere, or empty
     logp = quiet_nan();
     entropy = quiet_nan();
     log_z = quiet_nan();
     return;
   }
-  const double log_s = log(S);
-  logp = __double2float_rn(__dsub_rn(
-      __ddiv_rn(__dsub_rn(static_cast<double>(t), static_cast<double>(M)), tau), log_s));
-  entropy = __double2float_rn(__dsub_rn(log_s, __ddiv_rn(U, S)));
-  log_z = __double2float_rn(__dadd_rn(__ddiv_rn(static_cast<double>(M), tau), log_s));
+  const F2 log_s = log_f2(S);
+  F2 tm;
+  two_sum(t, -M, tm.hi, tm.lo);
+  const F2 lp = f2_add(f2_mul(tm, inv), F2{-log_s.hi, -log_s.lo});
+  logp = t == neg_inf() ? neg_inf() : t != t ? quiet_nan() : __fadd_rn(lp.hi, lp.lo);
+  entropy = __fadd_rn(log_s.hi, __fsub_rn(log_s.lo, __fdiv_rn(U, S.hi)));
+  const F2 lz = f2_add(f2_mul(F2{M, 0.0f}, inv), log_s);
+  log_z = __fadd_rn(lz.hi, lz.lo);
 }
 
 }  // namespace lp

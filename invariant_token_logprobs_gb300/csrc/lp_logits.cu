@@ -12,8 +12,8 @@
 // load.  A thread keeps an online state (max m, count of values equal to m,
 // sum of exp((z - m)/tau) over the others, and the entropy sum), raising its
 // maximum once per batch of 32 values; the exponentials are evaluated two at a
-// time in f32x2 arithmetic with the Cody-Waite + Taylor exp of lp_device.cuh
-// (unbiased, <= 0.64 ulp).  The 256 thread states are rebased to the CTA
+// time in f32x2 arithmetic with the Cody-Waite + minimax exp of lp_device.cuh
+// (unbiased, <= 0.55 ulp).  The 256 thread states are rebased to the CTA
 // maximum and summed as float pairs (hi + lo) in a fixed tree (warp shuffles,
 // then 8 warp partials in a fixed pairing).  Which thread owns which column
 // depends only on the column's offset inside its quarter, so a row's quarter
@@ -22,8 +22,8 @@
 // Finalising variant: the 4 CTAs of a row form a thread-block cluster; each
 // writes its 32-byte quarter state into the shared memory of cluster rank 0
 // (DSMEM), and after the cluster barrier four lanes of rank 0 merge
-// (Q0 + Q1) + (Q2 + Q3) in float64.  Partials variant: each CTA writes its
-// quarter state to global memory for lp_merge_partials.
+// (Q0 + Q1) + (Q2 + Q3) with float pairs.  Partials variant: each CTA writes
+// its quarter state to global memory for lp_merge_partials.
 //
 // Temperature: the maximum is taken over raw logits and each difference
 // z - m is multiplied by 1/tau = inv_hi + inv_lo; with tau == 1 no
@@ -101,6 +101,47 @@ struct LogitsOnline {
   }
 };
 
+// Add one batch of values (all <= st.m) to the online state: per value
+// d = (z - m) / tau, f = [d == 0] (the running maximum's term, exactly 1) to
+// the count, e = exp(d) for the others to s, and e d to u.  The lanes hold
+// f - e and (f - e) d (negated sums; f d = 0), two values per f32x2
+// operation, four lanes.
+template <bool kScaled>
+__device__ __forceinline__ void accumulate_batch(const float (&v)[kBatch][4], LogitsOnline& st,
+                                                 float inv_hi, float inv_lo) {
+  const uint64_t mm = pk2(st.m, st.m);
+  const uint64_t ih = pk2(inv_hi, inv_hi), il = pk2(inv_lo, inv_lo);
+  const uint64_t zero = pk2(0.f, 0.f);
+  uint64_t sn2[2] = {zero, zero}, c2[2] = {zero, zero}, un2[2] = {zero, zero};
+#pragma unroll
+  for (int k = 0; k < kBatch; ++k)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint64_t d2 = sub2(pk2(v[k][2 * h], v[k][2 * h + 1]), mm);
+      if (kScaled) {  // finite before scaling: -inf * a negative 1/tau low part
+        float da, db;
+        upk2(d2, da, db);
+        d2 = pk2(fmax_nan(da, -3.402823466e38f), fmax_nan(db, -3.402823466e38f));
+        d2 = fma2(d2, il, mul2(d2, ih));
+      }
+      uint64_t dc2, f2;
+      const uint64_t fme2 = count_minus_exp2(d2, dc2, f2);
+      sn2[h] = add2(sn2[h], fme2);
+      c2[h] = add2(c2[h], f2);
+      un2[h] = fma2(fme2, dc2, un2[h]);
+    }
+  float sa[4], ca[4], ua[4];
+  upk2(sn2[0], sa[0], sa[1]);
+  upk2(sn2[1], sa[2], sa[3]);
+  upk2(c2[0], ca[0], ca[1]);
+  upk2(c2[1], ca[2], ca[3]);
+  upk2(un2[0], ua[0], ua[1]);
+  upk2(un2[1], ua[2], ua[3]);
+  st.s = __fsub_rn(st.s, __fadd_rn(__fadd_rn(sa[0], sa[1]), __fadd_rn(sa[2], sa[3])));
+  st.c = __fadd_rn(st.c, __fadd_rn(__fadd_rn(ca[0], ca[1]), __fadd_rn(ca[2], ca[3])));
+  st.u = __fsub_rn(st.u, __fadd_rn(__fadd_rn(ua[0], ua[1]), __fadd_rn(ua[2], ua[3])));
+}
+
 // The quarter state (M, S = S_hi + S_lo, U) of the w columns starting at q0
 // for softmax(z / tau); valid in thread 0.
 template <bool kScaled>
@@ -118,51 +159,29 @@ __device__ __forceinline__ void quarter_state(const float* __restrict__ q0, int6
   st.reset();
   for (int g0 = 0; g0 < n_groups; g0 += kThreads * kBatch) {
     float v[kBatch][4];
+    if (vec && (g0 + kThreads * kBatch) * 4 <= wi) {  // every group of the batch is whole
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k) load_group(q0, wi, g0 + k * kThreads + tid, vec, v[k]);
-    float bm = v[0][0];
+      for (int k = 0; k < kBatch; ++k) {
+        const float4 x = load_stream(q0 + (g0 + k * kThreads + tid) * 4);
+        v[k][0] = x.x;
+        v[k][1] = x.y;
+        v[k][2] = x.z;
+        v[k][3] = x.w;
+      }
+    } else {
 #pragma unroll
-    for (int k = 0; k < kBatch; ++k)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) bm = fmax_nan(bm, v[k][i]);
-    st.raise_to(bm, inv_hi, inv_lo);
-    if (st.m != neg_inf()) {
-      // per value: d = (z - m) / tau, f = [d == 0] (the running maximum's
-      // term, exactly 1) to the count, e = exp(d) for the others to s, and
-      // e d to u.  The lanes hold f - e and (f - e) d (negated sums; f d = 0),
-      // two values per f32x2 operation, four lanes.
-      const uint64_t mm = pk2(st.m, st.m);
-      const uint64_t ih = pk2(inv_hi, inv_hi), il = pk2(inv_lo, inv_lo);
-      const uint64_t zero = pk2(0.f, 0.f);
-      uint64_t sn2[2] = {zero, zero}, c2[2] = {zero, zero}, un2[2] = {zero, zero};
-#pragma unroll
-      for (int k = 0; k < kBatch; ++k)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint64_t d2 = sub2(pk2(v[k][2 * h], v[k][2 * h + 1]), mm);
-          if (kScaled) {
-            float da, db;
-            upk2(d2, da, db);  // finite before scaling: -inf * a negative 1/tau low part
-            d2 = pk2(fmax_nan(da, -3.402823466e38f), fmax_nan(db, -3.402823466e38f));
-            d2 = fma2(d2, il, mul2(d2, ih));
-          }
-          uint64_t dc2, f2;
-          const uint64_t fme2 = count_minus_exp2(d2, dc2, f2);
-          sn2[h] = add2(sn2[h], fme2);
-          c2[h] = add2(c2[h], f2);
-          un2[h] = fma2(fme2, dc2, un2[h]);
-        }
-      float sa[4], ca[4], ua[4];
-      upk2(sn2[0], sa[0], sa[1]);
-      upk2(sn2[1], sa[2], sa[3]);
-      upk2(c2[0], ca[0], ca[1]);
-      upk2(c2[1], ca[2], ca[3]);
-      upk2(un2[0], ua[0], ua[1]);
-      upk2(un2[1], ua[2], ua[3]);
-      st.s = __fsub_rn(st.s, __fadd_rn(__fadd_rn(sa[0], sa[1]), __fadd_rn(sa[2], sa[3])));
-      st.c = __fadd_rn(st.c, __fadd_rn(__fadd_rn(ca[0], ca[1]), __fadd_rn(ca[2], ca[3])));
-      st.u = __fsub_rn(st.u, __fadd_rn(__fadd_rn(ua[0], ua[1]), __fadd_rn(ua[2], ua[3])));
+      for (int k = 0; k < kBatch; ++k) load_group(q0, wi, g0 + k * kThreads + tid, vec, v[k]);
     }
+    // batch maximum, three operands per instruction
+    float bm = fmax3_nan(v[0][0], v[0][1], v[0][2]);
+    bm = fmax_nan(bm, v[0][3]);
+#pragma unroll
+    for (int k = 1; k < kBatch; ++k) {
+      bm = fmax3_nan(bm, v[k][0], v[k][1]);
+      bm = fmax3_nan(bm, v[k][2], v[k][3]);
+    }
+    st.raise_to(bm, inv_hi, inv_lo);
+    if (st.m != neg_inf()) accumulate_batch<kScaled>(v, st, inv_hi, inv_lo);
   }
 
   // CTA maximum (order-free), then every thread's sum rebased to it as a float
