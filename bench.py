@@ -56,6 +56,9 @@ LINEAR_SOURCES = [os.path.join(ROOT, "invariant_token_logprobs_gb300", "csrc", f
                   for f in ("lp_linear.cu", "lp_tcgen05.cuh", "lp_device.cuh")]
 LOGITS_SOURCES = [os.path.join(ROOT, "invariant_token_logprobs_gb300", "csrc", f)
                   for f in ("lp_logits.cu", "lp_device.cuh")]
+BACKWARD_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "backward.fused_qwen3_8b.txt")
+BACKWARD_SOURCES = [os.path.join(ROOT, "invariant_token_logprobs_gb300", "csrc", f)
+                    for f in ("lp_backward.cu", "lp_linear.cu", "lp_tcgen05.cuh", "lp_device.cuh")]
 
 
 def parse_args(argv=None):
@@ -128,9 +131,11 @@ def sha256_files(paths) -> str:
     return h.hexdigest()
 
 
-def profile_traffic(summary=PROFILE_SUMMARY, sources=LINEAR_SOURCES):
-    """DRAM bytes per launch of a kernel from its committed ncu summary, or None
-    when the summary is absent or was taken on different kernel sources."""
+def profile_traffic(summary=PROFILE_SUMMARY, sources=LINEAR_SOURCES,
+                    field="dram_bytes_per_launch_full_size"):
+    """DRAM bytes per launch of a kernel (or per call, for `field`) from its
+    committed ncu summary, or None when the summary is absent or was taken on
+    different kernel sources."""
     if not os.path.exists(summary):
         return None
     fields = {}
@@ -142,7 +147,7 @@ def profile_traffic(summary=PROFILE_SUMMARY, sources=LINEAR_SOURCES):
     if fields.get("source_sha256") != sha256_files(sources):
         return None
     try:
-        return float(fields["dram_bytes_per_launch_full_size"])
+        return float(fields[field])
     except (KeyError, ValueError):
         return None
 
@@ -568,7 +573,10 @@ def bench_backward(lp, torch, x, dev, stream, peaks, peaks_kind, max_over, world
                             "note": "grad_W written in bf16 (lp_linear_logprob_backward_ex)"},
             "gpu_launches_per_call": 5,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
-                         "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"], "traffic": None,
+                         "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
+                         "traffic": profile_traffic(BACKWARD_PROFILE_SUMMARY, BACKWARD_SOURCES,
+                                                    "dram_bytes_per_call_full_size"),
+                         "algorithmic_bytes_per_call": 5.72e9,
                          "kernel": "whole backward call (3 tensor-core kernels + 2 small ones)",
                          "algorithmic_flops_per_call": flops,
                          "note": "log-sum-exp and entropy saved from the forward (lp_linear_logprob_lse); one memset + 5 kernels per call",
