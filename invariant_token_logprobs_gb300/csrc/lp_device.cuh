@@ -269,9 +269,14 @@ struct Online {
         u = 0.f;
       } else {
         const float delta = __fmul_rn(__fsub_rn(m, bm), inv_tau);  // < 0
-        const float a = exp_fast(delta);
-        u = __fmul_rn(a, __fmaf_rn(delta, s, u));
-        s = __fmul_rn(a, s);
+        if (delta < kExpClampLo) {  // the old terms vanish (delta may be -inf); NaN goes on
+          s = 0.f;
+          u = 0.f;
+        } else {
+          const float a = exp_fast(delta);
+          u = __fmul_rn(a, __fmaf_rn(delta, s, u));
+          s = __fmul_rn(a, s);
+        }
       }
       m = bm;
     }
@@ -395,10 +400,14 @@ __device__ __forceinline__ void finalise_quad(const QuarterState& q, unsigned ma
   if (q.m != neg_inf() && M == M) {
     F2 d;
     two_sum(q.m, -M, d.hi, d.lo);  // exact
-    d = f2_mul(d, inv);
-    const F2 a = d.hi < kExpClampLo ? F2{0.0f, 0.0f} : exp_f2(d);
-    S = f2_mul(a, F2{q.s_hi, q.s_lo});
-    U = __fmul_rn(a.hi, __fmaf_rn(d.hi, q.s_hi, q.u));
+    // a quarter more than 87 below the row maximum after scaling adds nothing
+    // (the scaled difference may even overflow); NaN goes on
+    if (!(__fmul_rn(d.hi, inv_hi) < kExpClampLo)) {
+      d = f2_mul(d, inv);
+      const F2 a = exp_f2(d);
+      S = f2_mul(a, F2{q.s_hi, q.s_lo});
+      U = __fmul_rn(a.hi, __fmaf_rn(d.hi, q.s_hi, q.u));
+    }
   }
   F2 o;
   o.hi = __shfl_xor_sync(mask, S.hi, 1);

@@ -338,8 +338,8 @@ __global__ void __launch_bounds__(128)
     float t = neg_inf();
     for (int j = lane; j < n_tiles_q; j += 32) {
       const float4 x = c[j];
-      if (x.x != neg_inf()) {
-        const float delta = __fmul_rn(__fsub_rn(x.x, M), inv_tau);
+      const float delta = __fmul_rn(__fsub_rn(x.x, M), inv_tau);
+      if (x.x != neg_inf() && !(delta < kExpClampLo)) {  // NaN goes on
         const float a = exp_neg(delta);
         S = __fadd_rn(S, __fmul_rn(a, x.y));
         U = __fadd_rn(U, __fmul_rn(a, __fmaf_rn(delta, x.y, x.z)));

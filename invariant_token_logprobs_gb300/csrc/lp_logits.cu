@@ -90,10 +90,15 @@ struct LogitsOnline {
         u = 0.f;
       } else {
         const float delta = scale_diff(__fsub_rn(m, bm), inv_hi, inv_lo);  // < 0
-        const float a = exp_neg(delta);
-        const float tot = __fadd_rn(c, s);
-        u = __fmul_rn(a, __fmaf_rn(delta, tot, u));
-        s = __fmul_rn(a, tot);
+        if (delta < kExpClampLo) {  // the old terms vanish (delta may be -inf); NaN goes on
+          s = 0.f;
+          u = 0.f;
+        } else {
+          const float a = exp_neg(delta);
+          const float tot = __fadd_rn(c, s);
+          u = __fmul_rn(a, __fmaf_rn(delta, tot, u));
+          s = __fmul_rn(a, tot);
+        }
         c = 0.f;
       }
       m = bm;
@@ -197,8 +202,10 @@ __device__ __forceinline__ void quarter_state(const float* __restrict__ q0, int6
   for (int i = 1; i < kWarps; ++i) M = fmaxf(M, red_m[i]);
 
   float hi = 0.f, lo = 0.f, u = 0.f;
-  if (st.m != neg_inf()) {
-    const float delta = scale_diff(__fsub_rn(st.m, M), inv_hi, inv_lo);
+  const float delta = scale_diff(__fsub_rn(st.m, M), inv_hi, inv_lo);
+  // a thread whose maximum lies more than 87 below the CTA's (after scaling;
+  // possibly -inf) adds nothing; NaN goes on
+  if (st.m != neg_inf() && !(delta < kExpClampLo)) {
     const float a = exp_neg(delta);  // 1 for the thread(s) holding the maximum
     float thi, tlo;
     two_sum(st.c, st.s, thi, tlo);

@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from invariant_token_logprobs_gb300 import lp, synth
 from _gpu_helpers import (LOGITS_ENT_TOL, LOGITS_LOGP_TOL, bits, excess_over_rounding, max_err,
                           oracle_logits)
@@ -147,6 +148,37 @@ def test_special_values():
     assert math.isnan(float(logp[2])) and math.isfinite(float(ent[2]))  # bad target
     assert math.isnan(float(logp[3])) and math.isnan(float(ent[3]))
     assert math.isnan(float(logp[4])) and math.isnan(float(ent[4]))
+
+
+def test_row_maximum_near_float_max():
+    """Logits near the top (and bottom) of the float range: the maximum is never
+    scaled by log2 e before the subtraction, so every difference z - max is
+    finite and the results are those of the closed forms, also at tau = 0.7.
+    (The fp64 oracle cannot serve here: at |z| ~ 3e38 a double holds log Z =
+    M + log S only to ~4e22, so z[y] - log Z loses the log S term.)"""
+    V = 3001
+    g = torch.Generator(device=DEV)
+    g.manual_seed(5)
+    z = torch.randn((4, V), generator=g, device=DEV)
+    z[0, 17] = 3.0e38            # one dominant logit: logp 0, entropy 0
+    z[1] = 3.0e38 + z[1]         # a whole row at 3e38 (the small terms are absorbed): uniform
+    z[2, 100] = 3.3e38
+    z[2, 200] = 3.3e38 - 1.0e32  # two huge logits; the target is the smaller one
+    z[3] = -3.0e38 + z[3]        # a whole row at -3e38: uniform
+    y = torch.tensor([17, 5, 200, 9], device=DEV)
+    gap = float(z[2, 200].double() - z[2, 100].double())  # exact difference of two floats
+    for tau in (1.0, 0.7):
+        inv = 1.0 / float(np.float32(tau))
+        logp, ent = lp.logprob_from_logits(z, y, temperature=tau)
+        got_lp = logp.double().cpu().numpy()
+        got_ent = ent.double().cpu().numpy()
+        assert np.isfinite(got_lp).all() and np.isfinite(got_ent).all(), (tau, got_lp, got_ent)
+        assert abs(got_lp[0]) <= LOGITS_LOGP_TOL and abs(got_ent[0]) <= LOGITS_ENT_TOL
+        for r in (1, 3):
+            assert abs(got_lp[r] + math.log(V)) <= LOGITS_LOGP_TOL, (tau, r, got_lp[r])
+            assert abs(got_ent[r] - math.log(V)) <= LOGITS_ENT_TOL, (tau, r, got_ent[r])
+        assert abs(got_lp[2] - gap * inv) <= 1e-6 * abs(gap * inv), (tau, got_lp[2], gap * inv)
+        assert abs(got_ent[2]) <= LOGITS_ENT_TOL
 
 
 def test_uniform_closed_form():
