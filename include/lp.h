@@ -309,7 +309,7 @@ LP_API lp_status lp_linear_logprob_partials_temperature(
  * ------------------------------------------------------------------------ */
 
 /* Workspace bytes of lp_linear_logprob_backward: the forward's workspace, the
- * bf16 G [T, V] (2 T V bytes) and 16 fp32 partial grad_H (64 T d bytes);
+ * bf16 G [T, V] (2 T V bytes) and 19 fp32 partial grad_H (76 T d bytes);
  * 0 for invalid sizes. */
 LP_API size_t lp_linear_logprob_backward_workspace_size(int64_t T, int64_t d, int64_t V);
 

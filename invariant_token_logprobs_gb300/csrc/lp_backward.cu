@@ -17,7 +17,7 @@
 //   2. lp_grad_kernel: z tiles recomputed in tensor memory; the epilogue forms
 //      G in fp32 and stores it in bf16 as G [T, V];
 //   3. lp_gemm_kernel<K-major A, N-major B>: dH = G W, reading W [V, d] as an
-//      N-major operand, over 16 fixed vocabulary ranges (partial products in
+//      N-major operand, over 19 fixed vocabulary ranges (partial products in
 //      fp32), then lp_split_sum_kernel adds the ranges in order;
 //   4. lp_gemm_kernel<M-major A, N-major B>: dW = G^T H, reading G [T, V] as an
 //      M-major operand and H [T, d] as an N-major one.
@@ -42,7 +42,10 @@ namespace {
 
 using namespace tc;
 
-constexpr int kSplitsDH = 16;  // fixed vocabulary ranges of the dH product
+// Fixed vocabulary ranges of the dH product (split K), summed in order.  A
+// constant, so the bits never depend on the GPU; 19 makes the 32 output tiles
+// of T = 512, d = 4096 exactly 8 waves of 76 CTA pairs (608 units).
+constexpr int kSplitsDH = 19;
 
 inline int64_t round8(int64_t x) { return (x + 7) / 8 * 8; }
 
@@ -593,7 +596,7 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
     if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
   }
 
-  // 3. dH = G W (W read N-major) over 16 fixed vocabulary ranges, summed in order
+  // 3. dH = G W (W read N-major) over 19 fixed vocabulary ranges, summed in order
   int n_split = kSplitsDH;
   // row blocks fastest: the pairs of one W range run together
   st = launch_gemm<false, true>(dev, G, T, L.V8, W, d, ld_w, V, kSplitsDH, dh_part, d, T * d,

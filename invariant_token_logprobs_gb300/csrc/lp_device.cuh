@@ -142,10 +142,10 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
 // -87 the result, ~1e-38, is negligible against the maximal term 1 of every
 // sum it enters.  NaN stays NaN.  With float32 fma Horner steps the relative
 // error is at most ~0.55 ulp and unbiased (mean ~2e-10); the hardware 2^x, by
-// comparison, measured -5e-8 (-0.4 ulp) biased on this GPU for |x| > 1.
+// comparison, measured -5e-8 (-0.4 ulp) biased on this GPU for |x| > 1.  Used
+// for every rescaling of a sum (raised maxima, rebases to a common maximum).
 constexpr float kExpClampLo = -87.0f;
 constexpr float kExpMagic = 12583039.0f;     // 1.5 * 2^23 + 127
-constexpr float kExpMagicNeg = 12583295.0f;  // 1.5 * 2^23 + 127 + 256: also sets the sign bit
 constexpr float kLn2Hi = 0.693145751953125f;
 constexpr float kLn2Lo = 1.42860677e-06f;
 constexpr float kP2 = 0.49999993451708435f, kP3 = 0.1666652068983302f,
@@ -165,36 +165,6 @@ __device__ __forceinline__ float exp_neg(float x) {
   p = __fmaf_rn(p, r, 1.0f);
   p = __fmaf_rn(p, r, 1.0f);
   return __fmul_rn(p, __int_as_float(__float_as_int(t) << 23));
-}
-
-// Two lanes at once, for the sums of the logits path: for x <= 0 (or NaN)
-// returns f - e^xc, where xc = max(x, -87) (NaN stays) is also returned and
-// f = 1 where xc == 0 (the term of the running maximum, exactly e^0 = 1), else
-// 0, also returned.  So f - e^xc is 0 for the maximal term and -e^xc for the
-// others.  The negated exponential comes from the same fma that would scale
-// p(r) by 2^n: the magic constant kExpMagicNeg puts -2^n in the shifted bits.
-__device__ __forceinline__ uint64_t count_minus_exp2(uint64_t x2, uint64_t& xc2, uint64_t& f2) {
-  float a, b;
-  upk2(x2, a, b);
-  a = fmax_nan(a, kExpClampLo);
-  b = fmax_nan(b, kExpClampLo);
-  xc2 = pk2(a, b);
-  f2 = pk2(ge_one_zero(a, 0.f), ge_one_zero(b, 0.f));
-  const uint64_t t2 = fma2(xc2, pk2(kLog2e, kLog2e), pk2(kExpMagicNeg, kExpMagicNeg));
-  const uint64_t n2 = sub2(t2, pk2(kExpMagicNeg, kExpMagicNeg));
-  uint64_t r2 = fma2(n2, pk2(-kLn2Hi, -kLn2Hi), xc2);
-  r2 = fma2(n2, pk2(-kLn2Lo, -kLn2Lo), r2);
-  uint64_t p2 = fma2(pk2(kP6, kP6), r2, pk2(kP5, kP5));
-  p2 = fma2(p2, r2, pk2(kP4, kP4));
-  p2 = fma2(p2, r2, pk2(kP3, kP3));
-  p2 = fma2(p2, r2, pk2(kP2, kP2));
-  p2 = fma2(p2, r2, pk2(1.0f, 1.0f));
-  p2 = fma2(p2, r2, pk2(1.0f, 1.0f));
-  float ta, tb;
-  upk2(t2, ta, tb);
-  const uint64_t neg_scale2 = pk2(__int_as_float(__float_as_int(ta) << 23),
-                                  __int_as_float(__float_as_int(tb) << 23));
-  return fma2(p2, neg_scale2, f2);
 }
 
 // -------------------------------------------------- float pairs (hi + lo)
