@@ -143,9 +143,10 @@ LP_API lp_status lp_logprob_partials_from_logits(const float* logits_shard, int6
  *                   float32, 16-byte aligned) from either partials entry point.
  *   n_shards        1, 2 or 4.
  *   logp_out        [T] float32; entropy_out [T] float32 or NULL.
- * The four states of a row are rebased to the row's largest m in float64,
- * summed as (Q0 + Q1) + (Q2 + Q3), and logp = (t - M) / tau - log S,
- * entropy = log S - U / S formed in float64 and rounded once.  A row whose
+ * The four states of a row are rebased to the row's largest m and summed as
+ * (Q0 + Q1) + (Q2 + Q3), and logp = (t - M) / tau - log S,
+ * entropy = log S - U / S are formed with float pairs (hi + lo, ~44 bits)
+ * and rounded once.  A row whose
  * states carry different tau gives NaN.
  */
 LP_API lp_status lp_merge_partials(const float* const* shard_partials, int n_shards,
@@ -260,7 +261,7 @@ LP_API lp_status lp_linear_logprob_partials(const void* H, int64_t ld_h, const v
  * each difference z - m is multiplied by 1/tau (on the logits path as the
  * float pair fl(1/tau) + fl(1/tau - fl(1/tau)); on the fused path by
  * fl(1/tau)) before its exponential, and the target enters as (t - M) / tau
- * formed in float64.  Every invariance above holds for a fixed tau, and
+ * formed with float pairs (~44 bits).  Every invariance above holds for a fixed tau, and
  * tau == 1 gives exactly the bits of the unscaled entry points.  temperature
  * must be finite and > 0 with 1/tau a finite positive float, else
  * LP_ERR_INVALID_ARGUMENT.  All other arguments are those of the unscaled
@@ -316,7 +317,7 @@ LP_API size_t lp_linear_logprob_backward_workspace_size(int64_t T, int64_t d, in
 /*
  * lp_linear_logprob_lse: lp_linear_logprob_temperature that also writes, per
  * row, lse_out[t] = log sum_v exp(z[t, v] / tau) (float32 [T], formed as
- * M / tau + log S in float64 and rounded once).  Keep lse_out
+ * M / tau + log S with float pairs and rounded once).  Keep lse_out
  * and entropy_out from the forward pass and hand them to the backward to skip
  * its forward recomputation.  All three outputs are required.
  */

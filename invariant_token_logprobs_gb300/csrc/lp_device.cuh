@@ -15,8 +15,8 @@
 // prior-art report (report.json, "candidates") split into slices; entropy uses
 // -sum p log p = log Z - sum p z.  The temperature enters only through the
 // differences z - m (exact or nearly so for the terms that matter) and
-// (t - M) / tau, which is formed in float64: no logit is rounded after
-// scaling.
+// (t - M) / tau, which is formed with float pairs (~44 bits): no logit is
+// rounded after scaling.
 //
 // A quarter state leaves a kernel as 8 floats (32 bytes, QuarterState):
 // m, s_hi, s_lo, u, t, tau, 0, 0, with s = s_hi + s_lo held as an unevaluated
