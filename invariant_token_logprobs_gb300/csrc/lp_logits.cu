@@ -242,17 +242,25 @@ __device__ __forceinline__ void quarter_state(const float* __restrict__ q0, int6
   }
   __syncthreads();
   if (tid == 0) {
-    static_assert(kWarps == 8, "fixed pairing below assumes 8 warps");
-    float h01, l01, h23, l23, h45, l45, h67, l67, h03, l03, h47, l47;
-    add_pair(red_hi[0], red_lo[0], red_hi[1], red_lo[1], h01, l01);
-    add_pair(red_hi[2], red_lo[2], red_hi[3], red_lo[3], h23, l23);
-    add_pair(red_hi[4], red_lo[4], red_hi[5], red_lo[5], h45, l45);
-    add_pair(red_hi[6], red_lo[6], red_hi[7], red_lo[7], h67, l67);
-    add_pair(h01, l01, h23, l23, h03, l03);
-    add_pair(h45, l45, h67, l67, h47, l47);
-    add_pair(h03, l03, h47, l47, out.s_hi, out.s_lo);
-    out.u = __fadd_rn(__fadd_rn(__fadd_rn(red_u[0], red_u[1]), __fadd_rn(red_u[2], red_u[3])),
-                      __fadd_rn(__fadd_rn(red_u[4], red_u[5]), __fadd_rn(red_u[6], red_u[7])));
+    // fixed pairwise tree over the warp sums: ((0+1)+(2+3))+((4+5)+(6+7)) for 8
+    static_assert((kWarps & (kWarps - 1)) == 0, "a power of two of warps");
+    float h[kWarps], l[kWarps], uu[kWarps];
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) {
+      h[i] = red_hi[i];
+      l[i] = red_lo[i];
+      uu[i] = red_u[i];
+    }
+#pragma unroll
+    for (int width = kWarps / 2; width >= 1; width /= 2)
+#pragma unroll
+      for (int i = 0; i < width; ++i) {
+        add_pair(h[2 * i], l[2 * i], h[2 * i + 1], l[2 * i + 1], h[i], l[i]);
+        uu[i] = __fadd_rn(uu[2 * i], uu[2 * i + 1]);
+      }
+    out.s_hi = h[0];
+    out.s_lo = l[0];
+    out.u = uu[0];
     out.m = M;
   }
 }

@@ -76,3 +76,20 @@ def test_committed_summaries_parse():
 def test_whole_job_throughput():
     # 512 rows per rank, 10 steps, 2 ranks, slowest rank 5 ms -> 2048 rows/ms
     assert bench.whole_job_throughput(512, 10, 2, 5.0) == pytest.approx(2048e3)
+
+
+def test_profile_traffic_per_call_field(tmp_path):
+    src = tmp_path / "b.cu"
+    src.write_text("backward v1\n")
+    summary = tmp_path / "b.txt"
+    h = bench.sha256_files([str(src)])
+    summary.write_text(f"source_sha256: {h}\ndram_bytes_per_call_full_size: 5.73e9\n")
+    assert bench.profile_traffic(str(summary), [str(src)], "dram_bytes_per_call_full_size") == \
+        pytest.approx(5.73e9)
+    # a field the summary does not hold reads as unknown
+    assert bench.profile_traffic(str(summary), [str(src)]) is None
+
+
+def test_tp_option_parses_and_defaults_to_replicas():
+    assert bench.parse_args([]).tp == 0
+    assert bench.parse_args(["--tp", "4", "--gpus", "4"]).tp == 4
