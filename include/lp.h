@@ -418,9 +418,10 @@ LP_API lp_status lp_set_kernel_timing_events(void* start_event, void* stop_event
  * every later fused forward call withholds one TMA load of its first CTA pair,
  * so that pair's pipeline waits give up after their time bound (about a second
  * each); the call still returns LP_OK, its outputs are NaN and
- * lp_get_device_error returns LP_ERR_TIMEOUT.  No fault is raised on the
- * device and the context stays usable.  Mode 0 (the default) turns it off.
- * Process-wide setting; not for production use.
+ * lp_get_device_error returns LP_ERR_TIMEOUT.  Mode 2: the same in the grad_W
+ * product of every later backward call (grad_W is NaN, grad_H exact).  No
+ * fault is raised on the device and the context stays usable.  Mode 0 (the
+ * default) turns it off.  Process-wide setting; not for production use.
  */
 LP_API lp_status lp_set_fault_injection(int mode);
 

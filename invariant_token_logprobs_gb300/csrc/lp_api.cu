@@ -180,7 +180,7 @@ lp_status lp_set_persistent_grid_limit(int max_ctas) {
 }
 
 lp_status lp_set_fault_injection(int mode) {
-  if (mode != 0 && mode != 1) return LP_ERR_INVALID_ARGUMENT;
+  if (mode < 0 || mode > 2) return LP_ERR_INVALID_ARGUMENT;
   lp::g_fault_injection.store(mode, std::memory_order_relaxed);
   return LP_OK;
 }

@@ -18,11 +18,14 @@
 //      G in fp32 and stores it in bf16 as G [T, V];
 //   3. lp_gemm_kernel<K-major A, N-major B>: dH = G W, reading W [V, d] as an
 //      N-major operand, over 19 fixed vocabulary ranges (partial products in
-//      fp32), then lp_split_sum_kernel adds the ranges in order;
+//      fp32);
 //   4. lp_gemm_kernel<M-major A, N-major B>: dW = G^T H, reading G [T, V] as an
-//      M-major operand and H [T, d] as an N-major one.
-// Both products write their fp32 output through TMA bulk stores from a
-// swizzled staging area.  No operand is transposed in memory.  Every output
+//      M-major operand and H [T, d] as an N-major one.  A seventh warp per CTA
+//      adds the 19 ranges of dH in order meanwhile (lp_split_sum_kernel does
+//      it on its own when dW is not asked for), and the last CTA to finish
+//      fills dW with NaN if a wait of the call gave up.
+// Both products write their output through TMA bulk stores from a swizzled
+// staging area.  No operand is transposed in memory.  Every output
 // element is produced by one CTA pair with a fixed K order and split sums are
 // added in a fixed order: the results are deterministic, and a row of dH
 // depends only on that row's inputs (not on T or its offset).
@@ -84,6 +87,7 @@ struct GradArgs {
   const float* ent;       // [T] entropy
   __nv_bfloat16* G;       // [T][ld_g]
   uint32_t* err;
+  uint32_t* ticket;       // finish counter of the dW product, zeroed here
   int64_t ld_g;
   float inv_tau;
   int T;
@@ -165,6 +169,7 @@ struct GradEpilogue {
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     lp_grad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ GradArgs a) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) *a.ticket = 0u;
   GradEpilogue epi{&a};
   run_pair_pipeline(&tmA, &tmB, a.tiles, epi, a.err);
 }
@@ -203,6 +208,68 @@ struct GemmTiles {
   }
 };
 
+// A 16-byte load that skips L1 and leaves L2 first in line for eviction: the
+// split sum reads each partial once, and in the dW product it must not push
+// out the operand blocks that consecutive units re-read from L2.
+__device__ __forceinline__ float4 load_once(const float4* p) {
+  float4 v;
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
+
+// out[i] = sum_s part[s][i] for s = 0 .. n_split-1 in order (n_split <=
+// kSplitsDH), for i = i0, i0 + stride, ... < n4 (float4 elements: n4 = n / 4,
+// part and out 16-byte aligned); NaN when an error word of the kernels that
+// made the partials (words 0..2 of the call) is set.
+__device__ __forceinline__ void split_sum(const float4* __restrict__ part, int64_t n4, int n_split,
+                                          const uint32_t* __restrict__ err,
+                                          float4* __restrict__ out, int64_t i0, int64_t stride) {
+  const bool failed = (err[0] | err[1] | err[2]) != 0u;
+  for (int64_t i = i0; i < n4; i += stride) {
+    float4 x[kSplitsDH];
+#pragma unroll
+    for (int k = 0; k < kSplitsDH; ++k)
+      if (k < n_split)
+        x[k] = LP_CHECK(n_split <= kSplitsDH, kChkSplitIndex) ? load_once(part + k * n4 + i)
+                                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 s = x[0];
+#pragma unroll
+    for (int k = 1; k < kSplitsDH; ++k) {
+      if (k < n_split) {
+        s.x = __fadd_rn(s.x, x[k].x);
+        s.y = __fadd_rn(s.y, x[k].y);
+        s.z = __fadd_rn(s.z, x[k].z);
+        s.w = __fadd_rn(s.w, x[k].w);
+      }
+    }
+    const float q = quiet_nan();
+    out[i] = failed ? make_float4(q, q, q, q) : s;
+  }
+}
+
+// The split sum of dH as the side warp of the dW product: the product is
+// bound by its tensor work and stores, the sum by HBM reads, so the two
+// overlap.  part == nullptr: nothing to do.
+struct SplitSumSide {
+  const float4* part;
+  int64_t n4;
+  int n_split;
+  const uint32_t* err;
+  float4* out;
+  __device__ __forceinline__ void operator()(int lane) const {
+    if (part == nullptr) return;
+    split_sum(part, n4, n_split, err, out, static_cast<int64_t>(blockIdx.x) * 32 + lane,
+              static_cast<int64_t>(gridDim.x) * 32);
+  }
+};
+
+// Threads of a product CTA: the pipeline's six warps and the side warp.
+constexpr int kGemmThreads = kThreads + 32;
+
 struct GemmArgs {
   GemmTiles tiles;
   CUtensorMap tmC;  // bulk-store map of C
@@ -211,6 +278,15 @@ struct GemmArgs {
   int n_split;      // matrices of C (split products)
   uint32_t* err;
   int out_bf16;     // C is bf16 (32 x 64 boxes) instead of fp32 (32 x 32 boxes)
+  SplitSumSide side;
+  // NaN fill of poison_out[0, poison_n) (C's type) by the last CTA to finish
+  // when any of the call's four error words is set (ticket == nullptr: none);
+  // the ticket is zero at launch and counts finished CTAs.
+  uint32_t* ticket;
+  const uint32_t* err_all;
+  void* poison_out;
+  int64_t poison_n;
+  int withhold_first_load;  // fault injection for tests of the bounded waits
 };
 
 // Epilogue of the products.  Each warp owns 32 rows of the tile and writes
@@ -241,6 +317,7 @@ __device__ __forceinline__ void bulk_store_3d(const CUtensorMap* map, int c0, in
 struct GemmEpilogue {
   const GemmArgs* a;
   int next = 0;  // staging buffer of this warp's next store
+
   __device__ __forceinline__ void consume(int u, uint32_t taddr, uint32_t rank, int lane_grp,
                                           int lane) {
     int mb, nb, s;
@@ -312,61 +389,48 @@ struct GemmEpilogue {
   }
 };
 
+// The last CTA of the grid to get here fills poison_out with NaN if a wait of
+// the call gave up: every CTA counts itself in after its own work, so the last
+// one sees every error word of the launch (and of the kernels before it).
+__device__ __forceinline__ void poison_if_failed(const GemmArgs& a) {
+  uint32_t* flag = reinterpret_cast<uint32_t*>(pipeline_smem_base());  // the ring is idle now
+  if (threadIdx.x == 0) {
+    uint32_t failed = 0u;
+    __threadfence();
+    if (atomicAdd(a.ticket, 1u) == gridDim.x - 1) {
+      __threadfence();
+      const volatile uint32_t* e = a.err_all;
+      failed = (e[0] | e[1] | e[2] | e[3]) != 0u ? 1u : 0u;
+    }
+    *flag = failed;
+  }
+  __syncthreads();
+  if (*flag == 0u) return;
+  for (int64_t i = threadIdx.x; i < a.poison_n; i += blockDim.x) {
+    if (a.out_bf16)
+      reinterpret_cast<uint16_t*>(a.poison_out)[i] = 0x7fc0u;  // bf16 NaN
+    else
+      reinterpret_cast<float*>(a.poison_out)[i] = quiet_nan();
+  }
+}
+
 template <bool kAMn, bool kBMn>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     lp_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ GemmArgs a) {
   GemmEpilogue epi{&a};
-  run_pair_pipeline<GemmTiles, GemmEpilogue, kAMn, kBMn>(&tmA, &tmB, a.tiles, epi, a.err);
+  run_pair_pipeline<GemmTiles, GemmEpilogue, kAMn, kBMn, SplitSumSide>(
+      &tmA, &tmB, a.tiles, epi, a.err, a.withhold_first_load, a.side);
+  if (a.ticket != nullptr) poison_if_failed(a);
 }
 
 // ------------------------------------------------------------- plain kernels
 
-// out[i] = sum_s part[s][i] for s = 0 .. n_split-1 in order (n_split <=
-// kSplitsDH); NaN when any error word of the call is set.  Four elements per
-// thread and step (n4 = n / 4; part and out 16-byte aligned).
+// dH's split sum on its own (when dW is not asked for).
 __global__ void lp_split_sum_kernel(const float4* __restrict__ part, int64_t n4, int n_split,
                                     const uint32_t* __restrict__ err, float4* __restrict__ out) {
-  const bool failed = (err[0] | err[1] | err[2] | err[3]) != 0u;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    float4 x[kSplitsDH];
-#pragma unroll
-    for (int k = 0; k < kSplitsDH; ++k)
-      if (k < n_split)
-        x[k] = LP_CHECK(n_split <= kSplitsDH, kChkSplitIndex) ? part[k * n4 + i]
-                                                              : make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 s = x[0];
-#pragma unroll
-    for (int k = 1; k < kSplitsDH; ++k) {
-      if (k < n_split) {
-        s.x = __fadd_rn(s.x, x[k].x);
-        s.y = __fadd_rn(s.y, x[k].y);
-        s.z = __fadd_rn(s.z, x[k].z);
-        s.w = __fadd_rn(s.w, x[k].w);
-      }
-    }
-    const float q = quiet_nan();
-    out[i] = failed ? make_float4(q, q, q, q) : s;
-  }
-}
-
-// Fill out[0..n) with NaN when any error word of the call is set.
-__global__ void lp_poison_kernel(const uint32_t* __restrict__ err, float* __restrict__ out,
-                                 int64_t n) {
-  if ((err[0] | err[1] | err[2] | err[3]) == 0u) return;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-    out[i] = quiet_nan();
-}
-
-// The same for a bf16 output (NaN = 0x7fc0).
-__global__ void lp_poison_bf16_kernel(const uint32_t* __restrict__ err, uint16_t* __restrict__ out,
-                                      int64_t n) {
-  if ((err[0] | err[1] | err[2] | err[3]) == 0u) return;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-    out[i] = 0x7fc0u;
+  split_sum(part, n4, n_split, err, out, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x,
+            static_cast<int64_t>(gridDim.x) * blockDim.x);
 }
 
 struct BackwardLayout {
@@ -391,11 +455,23 @@ BackwardLayout backward_layout(int64_t T, int64_t d, int64_t V) {
 
 // C = A B^T over the pipeline.  A is [M, K] (K-major, row stride ld_a) or,
 // with kAMn, [K, M] (M contiguous); B likewise with N.
+// What a product launch does besides C = A B^T: the side warps' split sum and
+// the last CTA's NaN fill (both off by default).
+struct GemmExtras {
+  SplitSumSide side{nullptr, 0, 0, nullptr, nullptr};
+  uint32_t* ticket = nullptr;
+  const uint32_t* err_all = nullptr;
+  void* poison_out = nullptr;
+  int64_t poison_n = 0;
+  int withhold_first_load = 0;
+};
+
 template <bool kAMn, bool kBMn>
 lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a, const void* B,
                       int64_t N, int64_t ld_b, int64_t K, int n_split, void* C, int64_t ldc,
                       int64_t split_stride, uint32_t* err, cudaStream_t stream,
-                      int* n_split_out, bool nb_fastest, bool out_bf16 = false) {
+                      int* n_split_out, bool nb_fastest, bool out_bf16 = false,
+                      const GemmExtras& x = GemmExtras()) {
   static PerContextOnce attr;
   if (attr.run(dev.ctx_id, [] {
         return set_pipeline_smem(reinterpret_cast<const void*>(lp_gemm_kernel<kAMn, kBMn>),
@@ -426,11 +502,17 @@ lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a,
   g.err = err;
   g.n_split = n_split;
   g.out_bf16 = out_bf16 ? 1 : 0;
+  g.side = x.side;
+  g.ticket = x.ticket;
+  g.err_all = x.err_all;
+  g.poison_out = x.poison_out;
+  g.poison_n = x.poison_n;
+  g.withhold_first_load = x.withhold_first_load;
   const bool ok_c = out_bf16 ? encode_bf16_3d_store(&g.tmC, C, n_split, M, N, ldc, split_stride)
                              : encode_f32_3d_store(&g.tmC, C, n_split, M, N, ldc, split_stride);
   if (!ok_c) return LP_ERR_CUDA;
   lp_gemm_kernel<kAMn, kBMn>
-      <<<pair_grid(dev.sm_count, total), kThreads, kGemmSmemBytes, stream>>>(tmA, tmB, g);
+      <<<pair_grid(dev.sm_count, total), kGemmThreads, kGemmSmemBytes, stream>>>(tmA, tmB, g);
   return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }
 
@@ -589,6 +671,7 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
     g.ent = ent;
     g.G = G;
     g.err = err + 1;
+    g.ticket = err + 4;
     g.ld_g = L.V8;
     g.inv_tau = tau.inv_hi;
     g.T = static_cast<int>(T);
@@ -603,26 +686,26 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
                                 err + 2, stream, &n_split, false);
   if (st != LP_OK) return st;
   // T * d is a multiple of 4 (d % 8 == 0); dh_part and grad_h are 16-byte aligned
-  lp_split_sum_kernel<<<dev.sm_count * 4, 256, 0, stream>>>(
-      reinterpret_cast<const float4*>(dh_part), T * d / 4, n_split, err,
-      reinterpret_cast<float4*>(grad_h));
-  if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
-
-  // 4. dW = G^T H (G read M-major, H read N-major)
-  if (grad_w != nullptr) {
-    // column blocks fastest: a block of G is used by 16 consecutive units
-    st = launch_gemm<true, true>(dev, G, V, L.V8, H, d, ld_h, T, 1, grad_w, d, 0, err + 3, stream,
-                                 nullptr, true, grad_w_bf16);
-    if (st != LP_OK) return st;
-    if (grad_w_bf16)
-      lp_poison_bf16_kernel<<<dev.sm_count * 4, 256, 0, stream>>>(
-          err, static_cast<uint16_t*>(grad_w), V * d);
-    else
-      lp_poison_kernel<<<dev.sm_count * 4, 256, 0, stream>>>(err, static_cast<float*>(grad_w),
-                                                            V * d);
-    if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
+  const SplitSumSide sum{reinterpret_cast<const float4*>(dh_part), T * d / 4, n_split, err,
+                         reinterpret_cast<float4*>(grad_h)};
+  if (grad_w == nullptr) {
+    lp_split_sum_kernel<<<dev.sm_count * 4, 256, 0, stream>>>(sum.part, sum.n4, sum.n_split, err,
+                                                              sum.out);
+    return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
   }
-  return LP_OK;
+
+  // 4. dW = G^T H (G read M-major, H read N-major), dH's split sum alongside;
+  // NaN in dW if any wait of the call gave up
+  GemmExtras x;
+  x.side = sum;
+  x.ticket = err + 4;  // zeroed by lp_grad_kernel
+  x.err_all = err;
+  x.poison_out = grad_w;
+  x.poison_n = V * d;
+  x.withhold_first_load = fault_injection() == 2 ? 1 : 0;
+  // column blocks fastest: a block of G is used by 16 consecutive units
+  return launch_gemm<true, true>(dev, G, V, L.V8, H, d, ld_h, T, 1, grad_w, d, 0, err + 3, stream,
+                                 nullptr, true, grad_w_bf16, x);
 }
 
 cudaError_t take_check_word_backward(uint32_t* out) { return take_check_word(out); }

@@ -465,7 +465,7 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
   a.tau = tau.tau;
   a.T = static_cast<int>(T);
   a.n_q = n_q;
-  a.withhold_first_load = fault_injection();
+  a.withhold_first_load = fault_injection() == 1 ? 1 : 0;
 
   const int grid = pair_grid(dev.sm_count, total);
   cudaEvent_t ev_start, ev_stop;

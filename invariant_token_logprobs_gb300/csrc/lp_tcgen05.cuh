@@ -280,9 +280,12 @@ __device__ __forceinline__ uint8_t* pipeline_smem_base() {
 //     work that no longer needs tensor memory (after the accumulator is freed);
 //   void finish(int lane_grp, int lane);
 //     once after the last unit (e.g. wait for asynchronous stores).
+// Side (optional): a kernel launched with more than kThreads threads gives
+//   each warp past the epilogue warps side(lane) to run once, alongside the
+//   pipeline (work that needs neither shared nor tensor memory).
 //
 // Called by every thread of a CTA of a 2-CTA cluster launched with kThreads
-// threads and kSmemBytes of dynamic shared memory.  `withhold_first_load`
+// threads (or more, for a Side) and kSmemBytes of dynamic shared memory.  `withhold_first_load`
 // (tests of the bounded waits only): the leader CTA of pair 0 announces but
 // never issues its first TMA load, so that stage never fills and the waits
 // on it give up after their time bound.
@@ -292,10 +295,15 @@ __device__ __forceinline__ uint8_t* pipeline_smem_base() {
 // box_rows 128); M- or N-major operands (true) are [K, rows] with the rows
 // contiguous and their tensor maps have 64 x 64 boxes (box_rows 64), two per
 // stage.
-template <class Sched, class Epi, bool kAMn = false, bool kBMn = false>
+struct NoSide {
+  __device__ __forceinline__ void operator()(int) const {}
+};
+
+template <class Sched, class Epi, bool kAMn = false, bool kBMn = false, class Side = NoSide>
 __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const CUtensorMap* tmB,
                                                   const Sched& sch, Epi& epi, uint32_t* err,
-                                                  int withhold_first_load = 0) {
+                                                  int withhold_first_load = 0,
+                                                  const Side& side = Side()) {
   uint8_t* smem = pipeline_smem_base();
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
@@ -447,7 +455,7 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
       }
       drain_wait(drain_bar, 0);
     }
-  } else {
+  } else if (warp < 2 + kEpilogueThreads / 32) {
     // -------------------------------------------------------------- epilogue
     const int lane_grp = warp & 3;  // tensor-memory lanes 32*lane_grp .. +31
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(lane_grp * 32) << 16);
@@ -468,6 +476,8 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
       if (acc == 0) acc_phase ^= 1u;
     }
     epi.finish(lane_grp, lane);
+  } else {
+    side(lane);
   }
 
   tc_fence_before();

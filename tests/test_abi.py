@@ -167,5 +167,7 @@ def test_valid_call_without_gb300_fails_loudly(lib):
     assert lib.lp_merge_partials(arr, 1, 8, A, A, None) == UNSUPPORTED
     assert lib.lp_set_persistent_grid_limit(-1) == INVALID
     assert lib.lp_set_persistent_grid_limit(0) == OK
-    assert lib.lp_set_fault_injection(2) == INVALID
+    assert lib.lp_set_fault_injection(3) == INVALID
+    assert lib.lp_set_fault_injection(-1) == INVALID
+    assert lib.lp_set_fault_injection(2) == OK
     assert lib.lp_set_fault_injection(0) == OK

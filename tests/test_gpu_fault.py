@@ -6,6 +6,8 @@ issues; its pipeline waits give up after their time bound (about a second),
 set the workspace error word, drain and free tensor memory, and the kernel
 returns.  The call's outputs are NaN, lp_get_device_error reports
 LP_ERR_TIMEOUT, and the next call on the same context gives correct results.
+The same holds for the grad_W product of the backward (its last CTA fills
+grad_W with NaN).
 """
 
 import math
@@ -45,3 +47,37 @@ def test_withheld_load_times_out_cleanly():
     torch.cuda.synchronize()
     assert lp.lp_get_device_error(ws) == 0
     assert torch.equal(bits(logp), bits(ref[0])) and torch.equal(bits(ent), bits(ref[1]))
+
+
+def _bits16(t):
+    return t.contiguous().view(torch.int16 if t.element_size() == 2 else torch.int32).cpu()
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_backward_withheld_load_poisons_grad_W(dtype):
+    lp.load()
+    x = synth.fused_inputs("fused_tiny", device=DEV)
+    T, d = x.H.shape
+    V = x.W.shape[0]
+    g = torch.Generator().manual_seed(5)
+    gl = torch.randn(T, generator=g).to(DEV)
+    ge = torch.randn(T, generator=g).to(DEV)
+    ref_h, ref_w = lp.linear_logprob_backward(x.H, x.W, x.y, gl, ge, grad_W_dtype=dtype)
+    ws = torch.empty(lp.lp_linear_logprob_backward_workspace_size(T, d, V), dtype=torch.uint8,
+                     device=DEV)
+    lp.lp_set_fault_injection(2)
+    try:
+        gh, gw = lp.linear_logprob_backward(x.H, x.W, x.y, gl, ge, workspace=ws,
+                                            grad_W_dtype=dtype)
+        torch.cuda.synchronize()
+    finally:
+        lp.lp_set_fault_injection(0)
+    assert lp.lp_get_device_error(ws) != 0
+    assert torch.isnan(gw.float()).all()
+    # grad_H comes from the kernels before the product that gave up
+    assert torch.equal(bits(gh), bits(ref_h))
+    # the context is still usable and the next call is exact
+    gh, gw = lp.linear_logprob_backward(x.H, x.W, x.y, gl, ge, workspace=ws, grad_W_dtype=dtype)
+    torch.cuda.synchronize()
+    assert lp.lp_get_device_error(ws) == 0
+    assert torch.equal(bits(gh), bits(ref_h)) and torch.equal(_bits16(gw), _bits16(ref_w))
