@@ -479,9 +479,9 @@ lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a,
       }) != cudaSuccess)
     return LP_ERR_CUDA;
   CUtensorMap tmA, tmB;
-  const bool okA = kAMn ? encode_bf16_2d(&tmA, A, K, M, ld_a, 64)
+  const bool okA = kAMn ? encode_bf16_2d(&tmA, A, K, M, ld_a, kBK)
                         : encode_bf16_2d(&tmA, A, M, K, ld_a, kBM);
-  const bool okB = kBMn ? encode_bf16_2d(&tmB, B, K, N, ld_b, 64)
+  const bool okB = kBMn ? encode_bf16_2d(&tmB, B, K, N, ld_b, kBK)
                         : encode_bf16_2d(&tmB, B, N, K, ld_b, kBNHalf);
   if (!okA || !okB) return LP_ERR_CUDA;
   GemmArgs g;

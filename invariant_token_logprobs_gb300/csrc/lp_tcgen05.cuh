@@ -6,14 +6,15 @@
 // and hands every finished tile to an epilogue.  CTA r of a pair holds rows
 // 128r..128r+127 of the A box and rows 128r..128r+127 of the B box in its own
 // shared memory and receives rows 128r.. of D in its own tensor memory, so an
-// SM stages 32 KB per 64-wide K block (a single-CTA 128 x 256 tile needs 48 KB,
-// and with the tensor core reading what TMA writes, shared-memory bandwidth is
+// SM stages 32 KB per 64 of K (a single-CTA 128 x 256 tile needs 48 KB, and
+// with the tensor core reading what TMA writes, shared-memory bandwidth is
 // what bounds it).
 //
 // Roles (6 warps per CTA):
-//   warp 0     TMA loader (both CTAs): this CTA's halves of the A and B boxes
-//              (64 x 128 each, 128-byte swizzle) into a 6-stage ring; the bytes
-//              of both CTAs complete one barrier in the leader CTA;
+//   warp 0     TMA loader (both CTAs): this CTA's halves of the A and B blocks
+//              (128 rows x 128 of K each, as two 64-wide boxes with 128-byte
+//              swizzle) into a 3-stage ring; the bytes of both CTAs complete
+//              one barrier in the leader CTA;
 //   warp 1     tensor memory: 512 columns (two 128 x 256 fp32 accumulators)
 //              allocated by both CTAs; one lane of the leader issues the MMAs
 //              and commits them to barriers in both CTAs (multicast);
@@ -47,11 +48,17 @@ namespace tc {
 constexpr int kBM = 128;       // rows of A per CTA (tensor-memory lanes); 256 per pair
 constexpr int kBN = 256;       // columns of D per tile; 128 rows of B per CTA
 constexpr int kBNHalf = kBN / 2;
-constexpr int kBK = 64;        // K per pipeline stage: 64 bf16 = one 128-byte swizzle row
+// K per pipeline stage: 128 bf16, two 128-byte swizzle atoms side by side.
+// With 64 (one atom) and a 6-deep ring the fused kernel ran 4-5% slower: each
+// W row was fetched 128 bytes at a time; two adjacent 128-byte pieces
+// requested together read HBM better (ring depth alone changed nothing).
+constexpr int kBK = 128;
+constexpr int kAtomK = 64;                   // bf16 per 128-byte swizzle row
+constexpr int kAtoms = kBK / kAtomK;
 constexpr int kUmmaK = 16;
-constexpr int kStages = 6;
-constexpr int kABytes = kBM * kBK * 2;       // 16 KB
-constexpr int kBBytes = kBNHalf * kBK * 2;   // 16 KB
+constexpr int kStages = 3;
+constexpr int kABytes = kBM * kBK * 2;       // 32 KB
+constexpr int kBBytes = kBNHalf * kBK * 2;   // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 192;
 constexpr int kEpilogueThreads = 128;
@@ -197,12 +204,14 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
 }
 
 // Shared-memory matrix descriptor of a K-major bf16 tile written by TMA with
-// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
-// Start address >> 4 in bits 0-13, leading-dimension offset (unused for this
-// layout, set to 16 bytes) in bits 16-29, stride offset 1024 >> 4 in bits
-// 32-45, descriptor version 1 in bits 46-47, swizzle mode 2 (128-byte) in
-// bits 61-63.  The tile base is 1024-byte aligned, so the K offset of each
-// 16-element MMA step is added to the start address.
+// 128-byte swizzle: rows of 128 bytes (64 K elements), 8-row groups 1024 bytes
+// apart; a stage holds kAtoms such boxes along K, each (rows x 128 bytes)
+// after the previous.  Start address >> 4 in bits 0-13, leading-dimension
+// offset (unused for this layout, set to 16 bytes) in bits 16-29, stride
+// offset 1024 >> 4 in bits 32-45, descriptor version 1 in bits 46-47, swizzle
+// mode 2 (128-byte) in bits 61-63.  The box base is 1024-byte aligned, so the
+// K offset of each 16-element MMA step within a box is added to the start
+// address.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
@@ -214,17 +223,18 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 }
 
 // Shared-memory matrix descriptor of an M- or N-major bf16 tile of 128 (MN) x
-// 64 (K) written by TMA with 128-byte swizzle as two boxes of 64 (MN) x 64 (K):
-// in each box, K row r sits at r * 128 bytes (64 contiguous MN elements), so a
-// swizzle atom is 64 MN elements x 8 K rows (1024 bytes).  The leading-
-// dimension offset (bits 16-29) is the distance between atoms along MN (the
-// second box, 8192 bytes); the stride offset (bits 32-45) the distance between
-// 8-row groups along K (1024 bytes).  Each 16-element MMA step along K adds
-// 2048 bytes to the start address.
+// kBK (K) written by TMA with 128-byte swizzle as two boxes of 64 (MN) x kBK
+// (K): in each box, K row r sits at r * 128 bytes (64 contiguous MN
+// elements), so a swizzle atom is 64 MN elements x 8 K rows (1024 bytes).  The
+// leading-dimension offset (bits 16-29) is the distance between atoms along
+// MN (the second box, kBK * 128 bytes); the stride offset (bits 32-45) the
+// distance between 8-row groups along K (1024 bytes).  Each 16-element MMA
+// step along K adds 2048 bytes to the start address.
+constexpr uint32_t kMnBoxBytes = kBK * 128;
 __device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(8192 >> 4) << 16;
+  d |= static_cast<uint64_t>(kMnBoxBytes >> 4) << 16;
   d |= static_cast<uint64_t>(1024 >> 4) << 32;
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
@@ -291,10 +301,10 @@ __device__ __forceinline__ uint8_t* pipeline_smem_base() {
 // on it give up after their time bound.
 //
 // Operand layouts: K-major (kAMn / kBMn false) operands are [rows, K] with K
-// contiguous and their tensor maps have 64 x 128 boxes (encode_bf16_2d with
-// box_rows 128); M- or N-major operands (true) are [K, rows] with the rows
-// contiguous and their tensor maps have 64 x 64 boxes (box_rows 64), two per
-// stage.
+// contiguous and their tensor maps have boxes of 64 K x 128 rows
+// (encode_bf16_2d with box_rows 128), kAtoms per stage along K; M- or N-major
+// operands (true) are [K, rows] with the rows contiguous and their tensor maps
+// have boxes of 64 rows x kBK K (box_rows kBK), two per stage along the rows.
 struct NoSide {
   __device__ __forceinline__ void operator()(int) const {}
 };
@@ -388,13 +398,19 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
               tma_load_2d(sa, tmA, a_row, kb * kBK, leader_full);
               tma_load_2d(sa + kABytes / 2, tmA, a_row + 64, kb * kBK, leader_full);
             } else {
-              tma_load_2d(sa, tmA, kb * kBK, a_row, leader_full);
+#pragma unroll
+              for (int i = 0; i < kAtoms; ++i)
+                tma_load_2d(sa + i * (kABytes / kAtoms), tmA, kb * kBK + i * kAtomK, a_row,
+                            leader_full);
             }
             if (kBMn) {
               tma_load_2d(sa + kABytes, tmB, b_row, kb * kBK, leader_full);
               tma_load_2d(sa + kABytes + kBBytes / 2, tmB, b_row + 64, kb * kBK, leader_full);
             } else {
-              tma_load_2d(sa + kABytes, tmB, kb * kBK, b_row, leader_full);
+#pragma unroll
+              for (int i = 0; i < kAtoms; ++i)
+                tma_load_2d(sa + kABytes + i * (kBBytes / kAtoms), tmB, kb * kBK + i * kAtomK,
+                            b_row, leader_full);
             }
           }
           if (++stage == kStages) {
@@ -436,8 +452,14 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
             const uint32_t sb = sa + kABytes;
 #pragma unroll
             for (int k = 0; k < kBK / kUmmaK; ++k) {
-              const uint64_t ad = kAMn ? sw128_mn_desc(sa + k * 2048) : sw128_desc(sa + k * kUmmaK * 2);
-              const uint64_t bd = kBMn ? sw128_mn_desc(sb + k * 2048) : sw128_desc(sb + k * kUmmaK * 2);
+              // K-major: box k / 4 of the stage, 32 bytes per step within it
+              constexpr int kSteps = kAtomK / kUmmaK;
+              const uint64_t ad = kAMn ? sw128_mn_desc(sa + k * 2048)
+                                       : sw128_desc(sa + (k / kSteps) * (kABytes / kAtoms) +
+                                                    (k % kSteps) * kUmmaK * 2);
+              const uint64_t bd = kBMn ? sw128_mn_desc(sb + k * 2048)
+                                       : sw128_desc(sb + (k / kSteps) * (kBBytes / kAtoms) +
+                                                    (k % kSteps) * kUmmaK * 2);
               tc_mma(d_tmem, ad, bd, (kb != kb0 || k != 0) ? 1u : 0u, idesc(kAMn, kBMn));
             }
             tc_commit_pair(empty_bar(stage));  // frees the stage in both CTAs
