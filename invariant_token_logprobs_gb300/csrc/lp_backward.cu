@@ -45,6 +45,11 @@ namespace {
 
 using namespace tc;
 
+// Ring geometry of the gradient kernel (both operands K-major, like the fused
+// forward) and of the two products (M/N-major operands).
+using GradRing = WideRing;
+using GemmRing = NarrowRing;
+
 // Fixed vocabulary ranges of the dH product (split K), summed in order.  A
 // constant, so the bits never depend on the GPU; 19 makes the 32 output tiles
 // of T = 512, d = 4096 exactly 8 waves of 76 CTA pairs (608 units).
@@ -171,7 +176,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                    const __grid_constant__ GradArgs a) {
   if (blockIdx.x == 0 && threadIdx.x == 0) *a.ticket = 0u;
   GradEpilogue epi{&a};
-  run_pair_pipeline(&tmA, &tmB, a.tiles, epi, a.err);
+  run_pair_pipeline<GradRing>(&tmA, &tmB, a.tiles, epi, a.err);
 }
 
 // ---------------------------------------------------------------------- GEMM
@@ -301,7 +306,7 @@ constexpr int kBoxFloats = 32 * 32;
 constexpr int kBoxes = 2;  // staging buffers per epilogue warp
 // dynamic shared memory of the product kernels: alignment slack, the
 // pipeline, then 4 warps' staging buffers
-constexpr int kGemmSmemBytes = 1024 + kPipelineSmemEnd + 4 * kBoxes * kBoxFloats * 4;
+constexpr int kGemmSmemBytes = 1024 + GemmRing::kSmemEnd + 4 * kBoxes * kBoxFloats * 4;
 static_assert(kGemmSmemBytes <= 232448, "fits the 227 KB per-CTA limit");
 
 __device__ __forceinline__ void bulk_store_3d(const CUtensorMap* map, int c0, int c1, int c2,
@@ -324,7 +329,7 @@ struct GemmEpilogue {
     a->tiles.decode(u, mb, nb, s);
     const int64_t row0 = static_cast<int64_t>(mb) * (2 * kBM) + rank * kBM + lane_grp * 32;
     const int64_t n0 = static_cast<int64_t>(nb) * kBN;
-    float* stg = reinterpret_cast<float*>(pipeline_smem_base() + kPipelineSmemEnd) +
+    float* stg = reinterpret_cast<float*>(pipeline_smem_base() + GemmRing::kSmemEnd) +
                  lane_grp * kBoxes * kBoxFloats;
     if (row0 >= a->M) return;
 #pragma unroll 1
@@ -419,7 +424,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     lp_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ GemmArgs a) {
   GemmEpilogue epi{&a};
-  run_pair_pipeline<GemmTiles, GemmEpilogue, kAMn, kBMn, SplitSumSide>(
+  run_pair_pipeline<GemmRing, GemmTiles, GemmEpilogue, kAMn, kBMn, SplitSumSide>(
       &tmA, &tmB, a.tiles, epi, a.err, a.withhold_first_load, a.side);
   if (a.ticket != nullptr) poison_if_failed(a);
 }
@@ -474,20 +479,20 @@ lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a,
                       const GemmExtras& x = GemmExtras()) {
   static PerContextOnce attr;
   if (attr.run(dev.ctx_id, [] {
-        return set_pipeline_smem(reinterpret_cast<const void*>(lp_gemm_kernel<kAMn, kBMn>),
-                                 kGemmSmemBytes - kSmemBytes);
+        return set_smem_limit(reinterpret_cast<const void*>(lp_gemm_kernel<kAMn, kBMn>),
+                              kGemmSmemBytes);
       }) != cudaSuccess)
     return LP_ERR_CUDA;
   CUtensorMap tmA, tmB;
-  const bool okA = kAMn ? encode_bf16_2d(&tmA, A, K, M, ld_a, kBK)
+  const bool okA = kAMn ? encode_bf16_2d(&tmA, A, K, M, ld_a, GemmRing::kBK)
                         : encode_bf16_2d(&tmA, A, M, K, ld_a, kBM);
-  const bool okB = kBMn ? encode_bf16_2d(&tmB, B, K, N, ld_b, kBK)
+  const bool okB = kBMn ? encode_bf16_2d(&tmB, B, K, N, ld_b, GemmRing::kBK)
                         : encode_bf16_2d(&tmB, B, N, K, ld_b, kBNHalf);
   if (!okA || !okB) return LP_ERR_CUDA;
   GemmArgs g;
   g.tiles.n_mb = static_cast<int>((M + 2 * kBM - 1) / (2 * kBM));
   g.tiles.n_nb = static_cast<int>((N + kBN - 1) / kBN);
-  g.tiles.n_kb = static_cast<int>((K + kBK - 1) / kBK);
+  g.tiles.n_kb = static_cast<int>((K + GemmRing::kBK - 1) / GemmRing::kBK);
   g.tiles.kb_per_split = (g.tiles.n_kb + n_split - 1) / n_split;
   // every split gets at least one K block (the count depends on K alone)
   n_split = (g.tiles.n_kb + g.tiles.kb_per_split - 1) / g.tiles.kb_per_split;
@@ -622,7 +627,7 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
   }
   static PerContextOnce attr;
   if (attr.run(dev.ctx_id, [] {
-        return set_pipeline_smem(reinterpret_cast<const void*>(lp_grad_kernel));
+        return set_smem_limit(reinterpret_cast<const void*>(lp_grad_kernel), GradRing::kSmemBytes);
       }) != cudaSuccess)
     return LP_ERR_CUDA;
 
@@ -659,7 +664,7 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
     GradArgs g;
     g.tiles.V = V;
     g.tiles.n_mb = static_cast<int>((T + 2 * kBM - 1) / (2 * kBM));
-    g.tiles.n_kb = static_cast<int>((d + kBK - 1) / kBK);
+    g.tiles.n_kb = static_cast<int>((d + GradRing::kBK - 1) / GradRing::kBK);
     g.tiles.n_tiles_q = static_cast<int>(tiles_per_quarter(V));
     const int64_t total = int64_t(g.tiles.n_mb) * 4 * g.tiles.n_tiles_q;
     if (total >= (int64_t(1) << 31)) return LP_ERR_INVALID_ARGUMENT;
@@ -675,7 +680,8 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
     g.ld_g = L.V8;
     g.inv_tau = tau.inv_hi;
     g.T = static_cast<int>(T);
-    lp_grad_kernel<<<pair_grid(dev.sm_count, total), kThreads, kSmemBytes, stream>>>(tmA, tmB, g);
+    lp_grad_kernel<<<pair_grid(dev.sm_count, total), kThreads, GradRing::kSmemBytes, stream>>>(
+        tmA, tmB, g);
     if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
   }
 

@@ -126,9 +126,8 @@ int pair_grid(int sm_count, int64_t units) {
   return 2 * pairs;
 }
 
-cudaError_t set_pipeline_smem(const void* kernel, int extra) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSmemBytes + extra);
+cudaError_t set_smem_limit(const void* kernel, int bytes) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
 }  // namespace tc
@@ -300,6 +299,8 @@ struct StateEpilogue {
   }
 };
 
+using LinearRing = WideRing;
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     lp_linear_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const __grid_constant__ LinearArgs a) {
@@ -307,7 +308,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // of this kernel starts them at zero too
   if (blockIdx.x == 0 && threadIdx.x == 0) a.err[1] = a.err[2] = a.err[3] = 0u;
   StateEpilogue epi{&a};
-  run_pair_pipeline(&tmA, &tmB, a.tiles, epi, a.err, a.withhold_first_load);
+  run_pair_pipeline<LinearRing>(&tmA, &tmB, a.tiles, epi, a.err, a.withhold_first_load);
 }
 
 // Merge the tile states of each quarter and then either finalise the row from
@@ -423,7 +424,8 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
                               void* workspace, cudaStream_t stream) {
   static PerContextOnce attr;
   if (attr.run(dev.ctx_id, [] {
-        return set_pipeline_smem(reinterpret_cast<const void*>(lp_linear_kernel));
+        return set_smem_limit(reinterpret_cast<const void*>(lp_linear_kernel),
+                              LinearRing::kSmemBytes);
       }) != cudaSuccess)
     return LP_ERR_CUDA;
 
@@ -452,7 +454,7 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
   a.tiles.V = V_total;
   a.tiles.w_row0 = w_row0;
   a.tiles.n_mb = static_cast<int>((T + 2 * kBM - 1) / (2 * kBM));
-  a.tiles.n_kb = static_cast<int>((d + kBK - 1) / kBK);
+  a.tiles.n_kb = static_cast<int>((d + LinearRing::kBK - 1) / LinearRing::kBK);
   a.tiles.q_first = q_first;
   a.tiles.n_tiles_q = static_cast<int>(tiles_per_quarter(V_total));
   const int64_t total = int64_t(a.tiles.n_mb) * n_q * a.tiles.n_tiles_q;
@@ -471,7 +473,7 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
   cudaEvent_t ev_start, ev_stop;
   timing_events(&ev_start, &ev_stop);
   if (ev_start != nullptr && cudaEventRecord(ev_start, stream) != cudaSuccess) return LP_ERR_CUDA;
-  lp_linear_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, a);
+  lp_linear_kernel<<<grid, kThreads, LinearRing::kSmemBytes, stream>>>(tmA, tmB, a);
   if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
   if (ev_stop != nullptr && cudaEventRecord(ev_stop, stream) != cudaSuccess) return LP_ERR_CUDA;
   lp_tile_merge_kernel<<<static_cast<unsigned>(T), 128, 0, stream>>>(

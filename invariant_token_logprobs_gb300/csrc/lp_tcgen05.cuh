@@ -48,30 +48,46 @@ namespace tc {
 constexpr int kBM = 128;       // rows of A per CTA (tensor-memory lanes); 256 per pair
 constexpr int kBN = 256;       // columns of D per tile; 128 rows of B per CTA
 constexpr int kBNHalf = kBN / 2;
-// K per pipeline stage: 128 bf16, two 128-byte swizzle atoms side by side.
-// With 64 (one atom) and a 6-deep ring the fused kernel ran 4-5% slower: each
-// W row was fetched 128 bytes at a time; two adjacent 128-byte pieces
-// requested together read HBM better (ring depth alone changed nothing).
-constexpr int kBK = 128;
-constexpr int kAtomK = 64;                   // bf16 per 128-byte swizzle row
-constexpr int kAtoms = kBK / kAtomK;
+constexpr int kAtomK = 64;     // bf16 per 128-byte swizzle row
 constexpr int kUmmaK = 16;
-constexpr int kStages = 3;
-constexpr int kABytes = kBM * kBK * 2;       // 32 KB
-constexpr int kBBytes = kBNHalf * kBK * 2;   // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kThreads = 192;
 constexpr int kEpilogueThreads = 128;
 constexpr uint32_t kTmemCols = 2 * kBN;
-constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;
-constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kNumBars * 8 + 16;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
-// Bytes past the 1024-aligned dynamic shared-memory base the pipeline uses
-// (ring, barriers, tensor-memory slot); an epilogue may use what follows.
-constexpr int kPipelineSmemEnd = kStages * kStageBytes + 1024;
 
 static_assert(kBN == kTileN, "the vocabulary tile of the fused path is one MMA tile");
-static_assert(kNumBars * 8 + 16 <= 1024, "barriers fit below kPipelineSmemEnd");
+
+// Geometry of the operand ring: BK of K per stage (BK / 64 boxes of 128-byte
+// swizzle rows side by side for a K-major operand), Stages stages.
+template <int BK, int Stages>
+struct Ring {
+  static constexpr int kBK = BK;
+  static constexpr int kAtoms = BK / kAtomK;
+  static constexpr int kStages = Stages;
+  static constexpr int kABytes = kBM * BK * 2;
+  static constexpr int kBBytes = kBNHalf * BK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kNumBars = 2 * Stages + 2 + 2 + 1;
+  // bytes past the 1024-aligned dynamic shared-memory base the pipeline uses
+  // (ring, barriers, tensor-memory slot); an epilogue may use what follows
+  static constexpr int kSmemEnd = Stages * kStageBytes + 1024;
+  // dynamic shared memory of a kernel whose epilogue uses none
+  static constexpr int kSmemBytes = 1024 + Stages * kStageBytes + kNumBars * 8 + 16;
+  // distance between the two 64-row boxes of an M- or N-major operand
+  static constexpr uint32_t kMnBoxBytes = BK * 128;
+  static_assert(BK % kAtomK == 0, "whole swizzle rows per stage");
+  static_assert(kNumBars * 8 + 16 <= 1024, "barriers fit below kSmemEnd");
+};
+
+// 128 of K per stage, 3 stages: the fused forward and gradient kernels (both
+// operands K-major).  With 64 and a 6-deep ring the fused kernel ran 4-5%
+// slower: each W row was fetched 128 bytes at a time, while two adjacent
+// 128-byte pieces requested together read HBM better (ring depth alone, 5 to
+// 7 stages, changed nothing).
+using WideRing = Ring<128, 3>;
+// 64 of K per stage, 6 stages: the backward's products (M/N-major operands,
+// 8 K blocks per grad_W unit), which ran ~1% faster this way.
+using NarrowRing = Ring<64, 6>;
 
 // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B bf16
 // (bits 7-9 = 1, bits 10-12 = 1), A / B major-ness in bits 15 / 16 (0: K-major,
@@ -223,18 +239,17 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 }
 
 // Shared-memory matrix descriptor of an M- or N-major bf16 tile of 128 (MN) x
-// kBK (K) written by TMA with 128-byte swizzle as two boxes of 64 (MN) x kBK
+// BK (K) written by TMA with 128-byte swizzle as two boxes of 64 (MN) x BK
 // (K): in each box, K row r sits at r * 128 bytes (64 contiguous MN
 // elements), so a swizzle atom is 64 MN elements x 8 K rows (1024 bytes).  The
 // leading-dimension offset (bits 16-29) is the distance between atoms along
-// MN (the second box, kBK * 128 bytes); the stride offset (bits 32-45) the
-// distance between 8-row groups along K (1024 bytes).  Each 16-element MMA
+// MN (the second box, box_bytes = BK * 128); the stride offset (bits 32-45)
+// the distance between 8-row groups along K (1024 bytes).  Each 16-element MMA
 // step along K adds 2048 bytes to the start address.
-constexpr uint32_t kMnBoxBytes = kBK * 128;
-__device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr) {
+__device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr, uint32_t box_bytes) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(kMnBoxBytes >> 4) << 16;
+  d |= static_cast<uint64_t>(box_bytes >> 4) << 16;
   d |= static_cast<uint64_t>(1024 >> 4) << 32;
   d |= static_cast<uint64_t>(1) << 46;
   d |= static_cast<uint64_t>(2) << 61;
@@ -295,7 +310,8 @@ __device__ __forceinline__ uint8_t* pipeline_smem_base() {
 //   pipeline (work that needs neither shared nor tensor memory).
 //
 // Called by every thread of a CTA of a 2-CTA cluster launched with kThreads
-// threads (or more, for a Side) and kSmemBytes of dynamic shared memory.  `withhold_first_load`
+// threads (or more, for a Side) and at least R::kSmemBytes of dynamic shared
+// memory; R is the ring geometry (WideRing or NarrowRing).  `withhold_first_load`
 // (tests of the bounded waits only): the leader CTA of pair 0 announces but
 // never issues its first TMA load, so that stage never fills and the waits
 // on it give up after their time bound.
@@ -304,16 +320,25 @@ __device__ __forceinline__ uint8_t* pipeline_smem_base() {
 // contiguous and their tensor maps have boxes of 64 K x 128 rows
 // (encode_bf16_2d with box_rows 128), kAtoms per stage along K; M- or N-major
 // operands (true) are [K, rows] with the rows contiguous and their tensor maps
-// have boxes of 64 rows x kBK K (box_rows kBK), two per stage along the rows.
+// have boxes of 64 rows x R::kBK K (box_rows R::kBK), two per stage along the
+// rows.
 struct NoSide {
   __device__ __forceinline__ void operator()(int) const {}
 };
 
-template <class Sched, class Epi, bool kAMn = false, bool kBMn = false, class Side = NoSide>
+template <class R, class Sched, class Epi, bool kAMn = false, bool kBMn = false,
+          class Side = NoSide>
 __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const CUtensorMap* tmB,
                                                   const Sched& sch, Epi& epi, uint32_t* err,
                                                   int withhold_first_load = 0,
                                                   const Side& side = Side()) {
+  constexpr int kBK = R::kBK;
+  constexpr int kAtoms = R::kAtoms;
+  constexpr int kStages = R::kStages;
+  constexpr int kABytes = R::kABytes;
+  constexpr int kBBytes = R::kBBytes;
+  constexpr int kStageBytes = R::kStageBytes;
+  constexpr int kNumBars = R::kNumBars;
   uint8_t* smem = pipeline_smem_base();
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
@@ -454,10 +479,10 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
             for (int k = 0; k < kBK / kUmmaK; ++k) {
               // K-major: box k / 4 of the stage, 32 bytes per step within it
               constexpr int kSteps = kAtomK / kUmmaK;
-              const uint64_t ad = kAMn ? sw128_mn_desc(sa + k * 2048)
+              const uint64_t ad = kAMn ? sw128_mn_desc(sa + k * 2048, R::kMnBoxBytes)
                                        : sw128_desc(sa + (k / kSteps) * (kABytes / kAtoms) +
                                                     (k % kSteps) * kUmmaK * 2);
-              const uint64_t bd = kBMn ? sw128_mn_desc(sb + k * 2048)
+              const uint64_t bd = kBMn ? sw128_mn_desc(sb + k * 2048, R::kMnBoxBytes)
                                        : sw128_desc(sb + (k / kSteps) * (kBBytes / kAtoms) +
                                                     (k % kSteps) * kUmmaK * 2);
               tc_mma(d_tmem, ad, bd, (kb != kb0 || k != 0) ? 1u : 0u, idesc(kAMn, kBMn));
@@ -539,9 +564,9 @@ bool encode_bf16_3d_store(CUtensorMap* map, void* base, int64_t S, int64_t rows,
 // process-wide CTA limit: one CTA pair per two SMs, never more pairs than units.
 int pair_grid(int sm_count, int64_t units);
 
-// Give `kernel` the dynamic shared memory of the pipeline plus `extra` bytes
-// for its epilogue (once per kernel).
-cudaError_t set_pipeline_smem(const void* kernel, int extra = 0);
+// Let `kernel` launch with `bytes` of dynamic shared memory (once per kernel
+// and context).
+cudaError_t set_smem_limit(const void* kernel, int bytes);
 
 }  // namespace tc
 }  // namespace lp
