@@ -44,6 +44,12 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBatch = 8;  // 4-float groups per thread per batch (32 values)
+// Resident CTAs per SM the kernels are compiled for: 5 caps them at 51
+// registers a thread (48 used, a 16-byte spill) where they took 58 and fitted
+// 4 per SM.  The fifth CTA keeps more loads in flight: 98.6 us against
+// 101.3 us for the 1024 x 151936 logits; 6 (40 registers) spilled and ran
+// 126 us.
+constexpr int kCtasPerSm = 5;
 
 __device__ __forceinline__ float4 load_stream(const float* p) {
   float4 v;
@@ -300,7 +306,7 @@ __device__ __forceinline__ QuarterState quarter_state_any(const float* __restric
   return st;
 }
 
-__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads)
+__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, kCtasPerSm)
     lp_logits_final_kernel(const float* __restrict__ logits, int64_t ld,
                            const int64_t* __restrict__ targets, int64_t T, int64_t V, TauArgs tau,
                            float* __restrict__ logp, float* __restrict__ entropy) {
@@ -341,7 +347,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads)
   }
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     lp_logits_partials_kernel(const float* __restrict__ logits_shard, int64_t ld,
                               const int64_t* __restrict__ targets, int64_t T, int64_t V,
                               int q_first, int n_q, TauArgs tau,
