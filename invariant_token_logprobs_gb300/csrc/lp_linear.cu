@@ -299,8 +299,12 @@ struct StateEpilogue {
   }
 };
 
-using LinearRing = WideRing;
-
+// The ring follows the batch: with one 256-row block (T <= 256) the kernel
+// streams W from HBM and the 6 x 64 ring ran ~2% faster (T = 1: 205 against
+// 209 us); from two blocks on it is tensor-bound and the 3 x 128 ring is 4-12%
+// faster (T = 512: 370 against 386 us; T = 2048: 1365 against 1540 us).  The
+// K order of the MMAs is the same in both, and so are the bits.
+template <class R>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     lp_linear_kernel(const __grid_constant__ CUtensorMap tmA,
                      const __grid_constant__ CUtensorMap tmB, const __grid_constant__ LinearArgs a) {
@@ -308,7 +312,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // of this kernel starts them at zero too
   if (blockIdx.x == 0 && threadIdx.x == 0) a.err[1] = a.err[2] = a.err[3] = 0u;
   StateEpilogue epi{&a};
-  run_pair_pipeline<LinearRing>(&tmA, &tmB, a.tiles, epi, a.err, a.withhold_first_load);
+  run_pair_pipeline<R>(&tmA, &tmB, a.tiles, epi, a.err, a.withhold_first_load);
 }
 
 // Merge the tile states of each quarter and then either finalise the row from
@@ -424,8 +428,12 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
                               void* workspace, cudaStream_t stream) {
   static PerContextOnce attr;
   if (attr.run(dev.ctx_id, [] {
-        return set_smem_limit(reinterpret_cast<const void*>(lp_linear_kernel),
-                              LinearRing::kSmemBytes);
+        cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(lp_linear_kernel<WideRing>),
+                                       WideRing::kSmemBytes);
+        if (e == cudaSuccess)
+          e = set_smem_limit(reinterpret_cast<const void*>(lp_linear_kernel<NarrowRing>),
+                             NarrowRing::kSmemBytes);
+        return e;
       }) != cudaSuccess)
     return LP_ERR_CUDA;
 
@@ -454,7 +462,9 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
   a.tiles.V = V_total;
   a.tiles.w_row0 = w_row0;
   a.tiles.n_mb = static_cast<int>((T + 2 * kBM - 1) / (2 * kBM));
-  a.tiles.n_kb = static_cast<int>((d + LinearRing::kBK - 1) / LinearRing::kBK);
+  const bool wide = a.tiles.n_mb > 1;
+  const int bk = wide ? WideRing::kBK : NarrowRing::kBK;
+  a.tiles.n_kb = static_cast<int>((d + bk - 1) / bk);
   a.tiles.q_first = q_first;
   a.tiles.n_tiles_q = static_cast<int>(tiles_per_quarter(V_total));
   const int64_t total = int64_t(a.tiles.n_mb) * n_q * a.tiles.n_tiles_q;
@@ -473,7 +483,10 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
   cudaEvent_t ev_start, ev_stop;
   timing_events(&ev_start, &ev_stop);
   if (ev_start != nullptr && cudaEventRecord(ev_start, stream) != cudaSuccess) return LP_ERR_CUDA;
-  lp_linear_kernel<<<grid, kThreads, LinearRing::kSmemBytes, stream>>>(tmA, tmB, a);
+  if (wide)
+    lp_linear_kernel<WideRing><<<grid, kThreads, WideRing::kSmemBytes, stream>>>(tmA, tmB, a);
+  else
+    lp_linear_kernel<NarrowRing><<<grid, kThreads, NarrowRing::kSmemBytes, stream>>>(tmA, tmB, a);
   if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
   if (ev_stop != nullptr && cudaEventRecord(ev_stop, stream) != cudaSuccess) return LP_ERR_CUDA;
   lp_tile_merge_kernel<<<static_cast<unsigned>(T), 128, 0, stream>>>(
