@@ -34,6 +34,7 @@
 #include <cuda_runtime.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "lp_check.cuh"
 #include "lp_device.cuh"
@@ -48,9 +49,16 @@ using namespace tc;
 // Ring geometry of the gradient kernel (both operands K-major, like the fused
 // forward) and of the two products (M/N-major operands).  With the 256-bit G
 // stores below the wide ring saves ~8 us per call over the narrow one; the
-// products ran ~1% faster on the narrow one.
+// products ran ~1% faster on the narrow one (both products; the dH product
+// alone on the wide ring: no change).
 using GradRing = WideRing;
-using GemmRing = NarrowRing;
+using GradHRing = NarrowRing;  // dH = G W (A K-major)
+using GradWRing = NarrowRing;  // dW = G^T H (A M-major)
+template <bool kAMn>
+using GemmRing = std::conditional_t<kAMn, GradWRing, GradHRing>;
+// the products' staging area starts where either ring ends
+static_assert(WideRing::kSmemEnd == NarrowRing::kSmemEnd, "one staging offset");
+constexpr int kGemmRingEnd = NarrowRing::kSmemEnd;
 
 // Fixed vocabulary ranges of the dH product (split K), summed in order.  A
 // constant, so the bits never depend on the GPU; 19 makes the 32 output tiles
@@ -322,7 +330,7 @@ constexpr int kBoxFloats = 32 * 32;
 constexpr int kBoxes = 2;  // staging buffers per epilogue warp
 // dynamic shared memory of the product kernels: alignment slack, the
 // pipeline, then 4 warps' staging buffers
-constexpr int kGemmSmemBytes = 1024 + GemmRing::kSmemEnd + 4 * kBoxes * kBoxFloats * 4;
+constexpr int kGemmSmemBytes = 1024 + kGemmRingEnd + 4 * kBoxes * kBoxFloats * 4;
 static_assert(kGemmSmemBytes <= 232448, "fits the 227 KB per-CTA limit");
 
 __device__ __forceinline__ void bulk_store_3d(const CUtensorMap* map, int c0, int c1, int c2,
@@ -345,7 +353,7 @@ struct GemmEpilogue {
     a->tiles.decode(u, mb, nb, s);
     const int64_t row0 = static_cast<int64_t>(mb) * (2 * kBM) + rank * kBM + lane_grp * 32;
     const int64_t n0 = static_cast<int64_t>(nb) * kBN;
-    float* stg = reinterpret_cast<float*>(pipeline_smem_base() + GemmRing::kSmemEnd) +
+    float* stg = reinterpret_cast<float*>(pipeline_smem_base() + kGemmRingEnd) +
                  lane_grp * kBoxes * kBoxFloats;
     if (row0 >= a->M) return;
 #pragma unroll 1
@@ -440,7 +448,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     lp_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ GemmArgs a) {
   GemmEpilogue epi{&a};
-  run_pair_pipeline<GemmRing, GemmTiles, GemmEpilogue, kAMn, kBMn, SplitSumSide>(
+  run_pair_pipeline<GemmRing<kAMn>, GemmTiles, GemmEpilogue, kAMn, kBMn, SplitSumSide>(
       &tmA, &tmB, a.tiles, epi, a.err, a.withhold_first_load, a.side);
   if (a.ticket != nullptr) poison_if_failed(a);
 }
@@ -500,15 +508,16 @@ lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a,
       }) != cudaSuccess)
     return LP_ERR_CUDA;
   CUtensorMap tmA, tmB;
-  const bool okA = kAMn ? encode_bf16_2d(&tmA, A, K, M, ld_a, GemmRing::kBK)
+  using R = GemmRing<kAMn>;
+  const bool okA = kAMn ? encode_bf16_2d(&tmA, A, K, M, ld_a, R::kBK)
                         : encode_bf16_2d(&tmA, A, M, K, ld_a, kBM);
-  const bool okB = kBMn ? encode_bf16_2d(&tmB, B, K, N, ld_b, GemmRing::kBK)
+  const bool okB = kBMn ? encode_bf16_2d(&tmB, B, K, N, ld_b, R::kBK)
                         : encode_bf16_2d(&tmB, B, N, K, ld_b, kBNHalf);
   if (!okA || !okB) return LP_ERR_CUDA;
   GemmArgs g;
   g.tiles.n_mb = static_cast<int>((M + 2 * kBM - 1) / (2 * kBM));
   g.tiles.n_nb = static_cast<int>((N + kBN - 1) / kBN);
-  g.tiles.n_kb = static_cast<int>((K + GemmRing::kBK - 1) / GemmRing::kBK);
+  g.tiles.n_kb = static_cast<int>((K + R::kBK - 1) / R::kBK);
   g.tiles.kb_per_split = (g.tiles.n_kb + n_split - 1) / n_split;
   // every split gets at least one K block (the count depends on K alone)
   n_split = (g.tiles.n_kb + g.tiles.kb_per_split - 1) / g.tiles.kb_per_split;
