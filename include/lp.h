@@ -343,8 +343,9 @@ LP_API lp_status lp_linear_logprob_lse(const void* H, int64_t ld_h, const void* 
  *               or NULL to skip it.
  *   workspace   device memory, 256-byte aligned, at least
  *               lp_linear_logprob_backward_workspace_size(T, d, V) bytes.
- * If a device-side wait gives up, lp_get_device_error reports it and the
- * outputs are NaN.
+ * If a device-side wait gives up, lp_get_device_error reports it; grad_W is
+ * then NaN, and so is grad_H unless the wait was in the grad_W product (the
+ * last kernel of the call, whose failure leaves grad_H exact).
  */
 LP_API lp_status lp_linear_logprob_backward(const void* H, int64_t ld_h, const void* W,
                                             int64_t ld_w, const int64_t* targets, int64_t T,
