@@ -47,11 +47,12 @@ namespace {
 using namespace tc;
 
 // Ring geometry of the gradient kernel (both operands K-major, like the fused
-// forward) and of the two products (M/N-major operands).  With the 256-bit G
-// stores below the wide ring saves ~8 us per call over the narrow one; the
-// products ran ~1% faster on the narrow one (both products; the dH product
-// alone on the wide ring: no change).
-using GradRing = WideRing;
+// forward) and of the two products (M/N-major operands).  The gradient kernel
+// picks its ring by batch as the fused forward does (one 256-row block streams
+// W from HBM: narrow ring, 1-3 us per call less at T = 128; more: wide); with
+// the 256-bit G stores below the wide ring saves ~8 us per call at T = 512.  The products ran ~1% faster on
+// the narrow ring (both products; the dH product alone on the wide ring: no
+// change).
 using GradHRing = NarrowRing;  // dH = G W (A K-major)
 using GradWRing = NarrowRing;  // dW = G^T H (A M-major)
 template <bool kAMn>
@@ -195,12 +196,13 @@ struct GradEpilogue {
   __device__ __forceinline__ void finish(int, int) {}
 };
 
+template <class R>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     lp_grad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ GradArgs a) {
   if (blockIdx.x == 0 && threadIdx.x == 0) *a.ticket = 0u;
   GradEpilogue epi{&a};
-  run_pair_pipeline<GradRing>(&tmA, &tmB, a.tiles, epi, a.err);
+  run_pair_pipeline<R>(&tmA, &tmB, a.tiles, epi, a.err);
 }
 
 // ---------------------------------------------------------------------- GEMM
@@ -652,7 +654,12 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
   }
   static PerContextOnce attr;
   if (attr.run(dev.ctx_id, [] {
-        return set_smem_limit(reinterpret_cast<const void*>(lp_grad_kernel), GradRing::kSmemBytes);
+        cudaError_t e = set_smem_limit(reinterpret_cast<const void*>(lp_grad_kernel<WideRing>),
+                                       WideRing::kSmemBytes);
+        if (e == cudaSuccess)
+          e = set_smem_limit(reinterpret_cast<const void*>(lp_grad_kernel<NarrowRing>),
+                             NarrowRing::kSmemBytes);
+        return e;
       }) != cudaSuccess)
     return LP_ERR_CUDA;
 
@@ -689,7 +696,9 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
     GradArgs g;
     g.tiles.V = V;
     g.tiles.n_mb = static_cast<int>((T + 2 * kBM - 1) / (2 * kBM));
-    g.tiles.n_kb = static_cast<int>((d + GradRing::kBK - 1) / GradRing::kBK);
+    const bool wide = g.tiles.n_mb > 1;
+    const int bk = wide ? WideRing::kBK : NarrowRing::kBK;
+    g.tiles.n_kb = static_cast<int>((d + bk - 1) / bk);
     g.tiles.n_tiles_q = static_cast<int>(tiles_per_quarter(V));
     const int64_t total = int64_t(g.tiles.n_mb) * 4 * g.tiles.n_tiles_q;
     if (total >= (int64_t(1) << 31)) return LP_ERR_INVALID_ARGUMENT;
@@ -705,8 +714,11 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
     g.ld_g = L.V8;
     g.inv_tau = tau.inv_hi;
     g.T = static_cast<int>(T);
-    lp_grad_kernel<<<pair_grid(dev.sm_count, total), kThreads, GradRing::kSmemBytes, stream>>>(
-        tmA, tmB, g);
+    const int grid = pair_grid(dev.sm_count, total);
+    if (wide)
+      lp_grad_kernel<WideRing><<<grid, kThreads, WideRing::kSmemBytes, stream>>>(tmA, tmB, g);
+    else
+      lp_grad_kernel<NarrowRing><<<grid, kThreads, NarrowRing::kSmemBytes, stream>>>(tmA, tmB, g);
     if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
   }
 
