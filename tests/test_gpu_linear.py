@@ -157,6 +157,19 @@ def test_grid_size_invariance_and_repeats():
     assert len(seen) == 1
 
 
+@pytest.mark.parametrize("d", [512, 320])
+def test_ring_choice_keeps_bits(d):
+    """Batches of one 256-row block run the kernel with 64-deep K stages, larger
+    ones with 128-deep stages (d = 320: the last stage half past the end of
+    the rows, read as zeros); a row's bits must not notice."""
+    x = synth.fused_inputs("fused_tiny", device=DEV, T=257, d=d, V=20000, seed=6)
+    full = lp.linear_logprob(x.H, x.W, x.y)
+    for sl in (slice(0, 256), slice(1, 257), slice(100, 101)):
+        part = lp.linear_logprob(x.H[sl].contiguous(), x.W, x.y[sl].contiguous())
+        assert torch.equal(bits(part[0]), bits(full[0][sl])), sl
+        assert torch.equal(bits(part[1]), bits(full[1][sl])), sl
+
+
 def test_cuda_graph_replay_matches_eager():
     x = synth.fused_inputs("fused_tiny", device=DEV, T=200, d=256, V=30000, seed=6)
     T, d = x.H.shape
