@@ -72,6 +72,7 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-logits", action="store_true", help="skip the logits-path line item")
     p.add_argument("--no-backward", action="store_true", help="skip the backward line item")
+    p.add_argument("--no-sweep", action="store_true", help="skip the batch-size sweep item")
     p.add_argument("--tp", type=int, default=0,
                    help="vocabulary-parallel ranks, 1, 2 or 4 (must equal the number of "
                         "processes); 0: the default replica mode")
@@ -483,6 +484,10 @@ def run_lp(args):
         logits_item = bench_logits(lp, synth, torch, dev, stream, peaks, peaks_kind, max_over,
                                    world, rank)
 
+    sweep_item = None
+    if not args.no_sweep:
+        sweep_item = bench_batch_sweep(lp, torch, x, dev, stream, peaks, peaks_kind, max_over)
+
     backward_item = None
     if not args.no_backward:
         backward_item = bench_backward(lp, torch, x, dev, stream, peaks, peaks_kind, max_over,
@@ -508,6 +513,7 @@ def run_lp(args):
         "backend": lp.lp_backend_id(),
         "logits_path": logits_item,
         "backward_path": backward_item,
+        "batch_sweep": sweep_item,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -581,6 +587,48 @@ def bench_backward(lp, torch, x, dev, stream, peaks, peaks_kind, max_over, world
                          "algorithmic_flops_per_call": flops,
                          "note": "log-sum-exp and entropy saved from the forward (lp_linear_logprob_lse); one memset + 3 kernels per call",
                          "peak_source": f"{peaks_kind} bf16 burst"}}
+
+
+def bench_batch_sweep(lp, torch, x, dev, stream, peaks, peaks_kind, max_over):
+    """Secondary line item: the fused call at other batch sizes on the same W
+    (rows of the headline H repeated; timing only), each against its own
+    roofline: the slower of 2 T d V at the bf16 burst peak and W read once at
+    the copy bandwidth."""
+    T0, d = x.H.shape
+    V = x.W.shape[0]
+    sizes = (1, 16, 128, 256, 512, 2048)
+    reps = (max(sizes) + T0 - 1) // T0
+    H_all = torch.cat([x.H] * reps)
+    y_all = torch.cat([x.y] * reps)
+    out = {}
+    for T in sizes:
+        H = H_all[:T].contiguous()
+        y = y_all[:T].contiguous()
+        ws = torch.empty(lp.lp_linear_logprob_workspace_size(T, d, V), dtype=torch.uint8,
+                         device=dev)
+        logp = torch.empty(T, device=dev)
+        ent = torch.empty(T, device=dev)
+        for _ in range(3):
+            lp.lp_linear_logprob(H, x.W, y, logp, ent, ws)
+        K = 20
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(K):
+            lp.lp_linear_logprob(H, x.W, y, logp, ent, ws)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        us = max_over(e0.elapsed_time(e1)) / K * 1e3
+        flops_us = 2.0 * T * d * V / (peaks["bf16_tflops"] * 1e12) * 1e6
+        bytes_us = 2.0 * V * d / (peaks["hbm_gbs"] * 1e9) * 1e6
+        out[str(T)] = {"us_per_call": us, "tokens_per_s": T / (us * 1e-6),
+                       "bound": "hbm" if bytes_us >= flops_us else "tensor",
+                       "frac": max(flops_us, bytes_us) / us}
+    return {"workload": "fused_qwen3_8b W with T rows", "d": d, "V": V,
+            "timing": "20 back-to-back lp_linear_logprob calls per size (kernel + merge)",
+            "roofline": "max(2 T d V / measured bf16 burst, 2 V d bytes / measured copy bandwidth)",
+            "peak_source": peaks_kind, "sizes": out}
 
 
 def bench_logits(lp, synth, torch, dev, stream, peaks, peaks_kind, max_over, world, rank):
