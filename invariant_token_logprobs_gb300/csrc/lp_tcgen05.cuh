@@ -1,7 +1,8 @@
 // lp_tcgen05.cuh: the sm_103a tensor-core pipeline shared by the fused kernels.
 //
 // A persistent grid of CTA pairs (thread-block clusters of 2, one CTA per SM)
-// computes 256 x 256 fp32 tiles D = A B^T of two K-major bf16 operands with
+// computes 256 x 256 fp32 tiles D = A B^T of two bf16 operands (K-major, or
+// M/N-major for the backward's products) with
 // tcgen05.mma.cta_group::2 (M=256, N=256, K=16, kind::f16) into tensor memory,
 // and hands every finished tile to an epilogue.  CTA r of a pair holds rows
 // 128r..128r+127 of the A box and rows 128r..128r+127 of the B box in its own
@@ -12,15 +13,17 @@
 //
 // Roles (6 warps per CTA):
 //   warp 0     TMA loader (both CTAs): this CTA's halves of the A and B blocks
-//              (128 rows x 128 of K each, as two 64-wide boxes with 128-byte
-//              swizzle) into a 3-stage ring; the bytes of both CTAs complete
-//              one barrier in the leader CTA;
+//              into the operand ring, whose geometry is a template parameter
+//              (Ring: 3 stages of 128 of K, each operand as two 64-wide boxes
+//              with 128-byte swizzle, or 6 stages of 64); the bytes of both
+//              CTAs complete one barrier in the leader CTA;
 //   warp 1     tensor memory: 512 columns (two 128 x 256 fp32 accumulators)
 //              allocated by both CTAs; one lane of the leader issues the MMAs
 //              and commits them to barriers in both CTAs (multicast);
 //   warps 2-5  epilogue (both CTAs): wait for a finished accumulator, run the
 //              caller's epilogue on it (one row per thread), then arrive on the
-//              leader's accumulator-empty barrier.
+//              leader's accumulator-empty barrier;
+//   warp 6     (optional) a side job of the caller's, alongside the pipeline.
 // While the epilogues drain one accumulator the MMAs fill the other.
 //
 // Every mbarrier wait is bounded by %globaltimer: a wait that gives up sets
