@@ -33,6 +33,7 @@ import datetime as _dt
 import hashlib
 import json
 import os
+import re
 import shutil
 import statistics
 import subprocess
@@ -123,12 +124,21 @@ def host_cores() -> int:
         return os.cpu_count() or 1
 
 
+def code_text(src: str) -> str:
+    """C/C++/CUDA source without its comments, trailing blanks and empty lines:
+    what a profile's numbers depend on (an edit of a comment leaves it as is)."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
 def sha256_files(paths) -> str:
-    """SHA-256 of the files' bytes concatenated in the given order."""
+    """SHA-256 of the files' code (code_text) concatenated in the given order."""
     h = hashlib.sha256()
     for path in paths:
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path, encoding="utf-8") as f:
+            h.update(code_text(f.read()).encode("utf-8"))
+        h.update(b"\n")
     return h.hexdigest()
 
 

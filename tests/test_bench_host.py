@@ -93,3 +93,14 @@ def test_profile_traffic_per_call_field(tmp_path):
 def test_tp_option_parses_and_defaults_to_replicas():
     assert bench.parse_args([]).tp == 0
     assert bench.parse_args(["--tp", "4", "--gpus", "4"]).tp == 4
+
+
+def test_profile_hash_follows_code_not_comments(tmp_path):
+    import bench
+    a = tmp_path / "a.cu"
+    a.write_text("// header\n__global__ void k(int* p) {\n  *p = 1;  /* one */\n}\n")
+    h0 = bench.sha256_files([str(a)])
+    a.write_text("// a new header line\n\n__global__ void k(int* p) {\n  *p = 1;  // one\n}\n")
+    assert bench.sha256_files([str(a)]) == h0
+    a.write_text("__global__ void k(int* p) {\n  *p = 2;\n}\n")
+    assert bench.sha256_files([str(a)]) != h0
