@@ -117,6 +117,16 @@ bool encode_bf16_3d_store(CUtensorMap* map, void* base, int64_t S, int64_t rows,
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same for CTAs that work alone: one per SM.
+int single_grid(int sm_count, int64_t units) {
+  int ctas = sm_count;
+  const int limit = persistent_grid_limit();
+  if (limit > 0 && limit < ctas) ctas = limit;
+  if (units < ctas) ctas = static_cast<int>(units);
+  if (ctas < 1) ctas = 1;
+  return ctas;
+}
+
 int pair_grid(int sm_count, int64_t units) {
   int pairs = sm_count / 2;
   const int limit = persistent_grid_limit();
@@ -299,20 +309,36 @@ struct StateEpilogue {
   }
 };
 
-// The ring follows the batch: with one 256-row block (T <= 256) the kernel
-// streams W from HBM and the 6 x 64 ring ran ~2% faster (T = 1: 205 against
-// 209 us); from two blocks on it is tensor-bound and the 3 x 128 ring is 4-12%
-// faster (T = 512: 370 against 386 us; T = 2048: 1365 against 1540 us).  The
-// K order of the MMAs is the same in both, and so are the bits.
+// The pipeline follows the batch.  With one 256-row block (T <= 256) the
+// kernel streams W from HBM: up to 128 rows one CTA per tile (SingleRing), so
+// no tensor core multiplies the zero rows a pair's second half would hold;
+// 129..256 rows a pair with the 6 x 64 ring, which ran ~2% faster there than
+// 3 x 128 (T = 1: 205 against 209 us).  From two blocks on the kernel is
+// tensor-bound and the 3 x 128 ring is 4-12% faster (T = 512: 370 against
+// 386 us; T = 2048: 1365 against 1540 us).  Every form issues the MMAs of an
+// accumulator element in the same K order, so the bits do not change.
 template <class R>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    lp_linear_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ LinearArgs a) {
+__device__ __forceinline__ void linear_body(const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                            const LinearArgs& a) {
   // words 1..3 of the error header belong to the backward's kernels; a call
   // of this kernel starts them at zero too
   if (blockIdx.x == 0 && threadIdx.x == 0) a.err[1] = a.err[2] = a.err[3] = 0u;
   StateEpilogue epi{&a};
-  run_pair_pipeline<R>(&tmA, &tmB, a.tiles, epi, a.err, a.withhold_first_load);
+  run_pair_pipeline<R>(tmA, tmB, a.tiles, epi, a.err, a.withhold_first_load);
+}
+
+template <class R>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    lp_linear_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const __grid_constant__ LinearArgs a) {
+  linear_body<R>(&tmA, &tmB, a);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    lp_linear_single_kernel(const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ LinearArgs a) {
+  linear_body<SingleRing>(&tmA, &tmB, a);
 }
 
 // Merge the tile states of each quarter and then either finalise the row from
@@ -433,6 +459,9 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
         if (e == cudaSuccess)
           e = set_smem_limit(reinterpret_cast<const void*>(lp_linear_kernel<NarrowRing>),
                              NarrowRing::kSmemBytes);
+        if (e == cudaSuccess)
+          e = set_smem_limit(reinterpret_cast<const void*>(lp_linear_single_kernel),
+                             SingleRing::kSmemBytes);
         return e;
       }) != cudaSuccess)
     return LP_ERR_CUDA;
@@ -462,8 +491,9 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
   a.tiles.V = V_total;
   a.tiles.w_row0 = w_row0;
   a.tiles.n_mb = static_cast<int>((T + 2 * kBM - 1) / (2 * kBM));
+  const bool single = T <= kBM;  // one CTA per tile: no pair half of zero rows
   const bool wide = a.tiles.n_mb > 1;
-  const int bk = wide ? WideRing::kBK : NarrowRing::kBK;
+  const int bk = wide ? WideRing::kBK : single ? SingleRing::kBK : NarrowRing::kBK;
   a.tiles.n_kb = static_cast<int>((d + bk - 1) / bk);
   a.tiles.q_first = q_first;
   a.tiles.n_tiles_q = static_cast<int>(tiles_per_quarter(V_total));
@@ -479,12 +509,14 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
   a.n_q = n_q;
   a.withhold_first_load = fault_injection() == 1 ? 1 : 0;
 
-  const int grid = pair_grid(dev.sm_count, total);
+  const int grid = single ? single_grid(dev.sm_count, total) : pair_grid(dev.sm_count, total);
   cudaEvent_t ev_start, ev_stop;
   timing_events(&ev_start, &ev_stop);
   if (ev_start != nullptr && cudaEventRecord(ev_start, stream) != cudaSuccess) return LP_ERR_CUDA;
   if (wide)
     lp_linear_kernel<WideRing><<<grid, kThreads, WideRing::kSmemBytes, stream>>>(tmA, tmB, a);
+  else if (single)
+    lp_linear_single_kernel<<<grid, kThreads, SingleRing::kSmemBytes, stream>>>(tmA, tmB, a);
   else
     lp_linear_kernel<NarrowRing><<<grid, kThreads, NarrowRing::kSmemBytes, stream>>>(tmA, tmB, a);
   if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;

@@ -61,14 +61,18 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait
 static_assert(kBN == kTileN, "the vocabulary tile of the fused path is one MMA tile");
 
 // Geometry of the operand ring: BK of K per stage (BK / 64 boxes of 128-byte
-// swizzle rows side by side for a K-major operand), Stages stages.
-template <int BK, int Stages>
+// swizzle rows side by side for a K-major operand), Stages stages.  Pair: the
+// CTA is one of a 2-SM pair (cta_group::2, M = 256, this CTA's 128 rows of the
+// tile's B); otherwise it works alone (cta_group::1, M = 128, all 256 rows of
+// B, K-major operands only).
+template <int BK, int Stages, bool Pair = true>
 struct Ring {
+  static constexpr bool kPair = Pair;
   static constexpr int kBK = BK;
   static constexpr int kAtoms = BK / kAtomK;
   static constexpr int kStages = Stages;
   static constexpr int kABytes = kBM * BK * 2;
-  static constexpr int kBBytes = kBNHalf * BK * 2;
+  static constexpr int kBBytes = (Pair ? kBNHalf : kBN) * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kNumBars = 2 * Stages + 2 + 2 + 1;
   // bytes past the 1024-aligned dynamic shared-memory base the pipeline uses
@@ -91,14 +95,18 @@ using WideRing = Ring<128, 3>;
 // 64 of K per stage, 6 stages: the backward's products (M/N-major operands,
 // 8 K blocks per grad_W unit), which ran ~1% faster this way.
 using NarrowRing = Ring<64, 6>;
+// One CTA per tile, 4 stages of 64 of K (16 KB of A, 32 KB of B each): the
+// fused forward for batches of at most 128 rows, where the pair's second
+// 128-row half would multiply only zero rows.
+using SingleRing = Ring<64, 4, false>;
 
 // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B bf16
 // (bits 7-9 = 1, bits 10-12 = 1), A / B major-ness in bits 15 / 16 (0: K-major,
 // 1: M- or N-major), N >> 3 in bits 17-22, M >> 4 in bits 24-28; M = 256 for
 // the CTA pair.
-__host__ __device__ constexpr uint32_t idesc(bool a_mn, bool b_mn) {
+__host__ __device__ constexpr uint32_t idesc(bool a_mn, bool b_mn, int m = 2 * kBM) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) |
-         (uint32_t(kBN >> 3) << 17) | (uint32_t((2 * kBM) >> 4) << 24);
+         (uint32_t(kBN >> 3) << 17) | (uint32_t(m >> 4) << 24);
 }
 constexpr uint32_t kIdesc = idesc(false, false);
 
@@ -171,11 +179,25 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// The same into a CTA that works alone, counted on its own barrier.
+__device__ __forceinline__ void tma_load_2d_local(uint32_t dst, const CUtensorMap* map, int c0,
+                                                  int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
   return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_local(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
@@ -209,6 +231,23 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
       "[%0], %1;" ::"r"(bar),
       "h"(both)
+      : "memory");
+}
+
+// The same for a CTA that works alone.
+__device__ __forceinline__ void tc_commit_local(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_single(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t accumulate, uint32_t instr) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(instr), "r"(accumulate)
       : "memory");
 }
 
@@ -342,6 +381,8 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
   constexpr int kBBytes = R::kBBytes;
   constexpr int kStageBytes = R::kStageBytes;
   constexpr int kNumBars = R::kNumBars;
+  constexpr bool kPair = R::kPair;
+  static_assert(kPair || (!kAMn && !kBMn), "a lone CTA takes K-major operands only");
   uint8_t* smem = pipeline_smem_base();
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
@@ -356,9 +397,10 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = cluster_rank();  // 0: leader (issues the MMAs), 1: peer
-  const int pair = blockIdx.x >> 1;
-  const int n_pairs = gridDim.x >> 1;
+  // 0: leader (issues the MMAs), 1: peer; a lone CTA is its own leader
+  const uint32_t rank = kPair ? cluster_rank() : 0u;
+  const int pair = kPair ? blockIdx.x >> 1 : blockIdx.x;  // this CTA's (pair's) place in the grid
+  const int n_pairs = kPair ? gridDim.x >> 1 : gridDim.x;
   const int units = sch.units();
 
   // The error word of this call starts at zero; a wait can only give up (and
@@ -371,7 +413,7 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), 2 * kEpilogueThreads);
+      mbar_init(tempty_bar(b), (kPair ? 2 : 1) * kEpilogueThreads);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -380,16 +422,24 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmB)) : "memory");
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(tmem_slot)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    if constexpr (kPair) {
+      asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_slot)),
+                   "r"(kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    } else {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                       smem_u32(tmem_slot)),
+                   "r"(kTmemCols)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
   }
   tc_fence_before();
   __syncthreads();
   __syncwarp();
-  cluster_sync();  // both CTAs' barriers initialised and tensor memory allocated
+  if constexpr (kPair) cluster_sync();  // both CTAs' barriers initialised and tensor memory allocated
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -410,9 +460,9 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
             break;
           }
           const uint32_t sa = smem_u32(smem + stage * kStageBytes);
-          const uint32_t leader_full = cluster_addr(full_bar(stage), 0);
+          const uint32_t leader_full = kPair ? cluster_addr(full_bar(stage), 0) : full_bar(stage);
           if (rank == 0) {
-            mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytes);
+            mbar_arrive_expect_tx(full_bar(stage), (kPair ? 2 : 1) * kStageBytes);
             pending |= 1u << stage;
             pending_parity = (pending_parity & ~(1u << stage)) | (phase << stage);
           }
@@ -421,7 +471,19 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
           const bool withheld = (withhold_first_load != 0 && pair == 0 && rank == 0 &&
                                  u == pair && kb == kb0) ||
                                 !LP_CHECK(a_row >= 0 && b_row >= 0 && kb >= 0, kChkTmaCoord);
-          if (!withheld) {
+          if (!withheld && !kPair) {
+            // a lone CTA: its 128 rows of A and all 256 rows of the B tile (two
+            // 128-row boxes per 64 of K), counted on its own barrier
+#pragma unroll
+            for (int i = 0; i < kAtoms; ++i) {
+              tma_load_2d_local(sa + i * (kABytes / kAtoms), tmA, kb * kBK + i * kAtomK, a_row,
+                                leader_full);
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                tma_load_2d_local(sa + kABytes + i * (kBBytes / kAtoms) + h * (kBBytes / kAtoms / 2),
+                                  tmB, kb * kBK + i * kAtomK, b_row + h * kBNHalf, leader_full);
+            }
+          } else if (!withheld) {
             if (kAMn) {
               tma_load_2d(sa, tmA, a_row, kb * kBK, leader_full);
               tma_load_2d(sa + kABytes / 2, tmA, a_row + 64, kb * kBK, leader_full);
@@ -488,20 +550,30 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
               const uint64_t bd = kBMn ? sw128_mn_desc(sb + k * 2048, R::kMnBoxBytes)
                                        : sw128_desc(sb + (k / kSteps) * (kBBytes / kAtoms) +
                                                     (k % kSteps) * kUmmaK * 2);
-              tc_mma(d_tmem, ad, bd, (kb != kb0 || k != 0) ? 1u : 0u, idesc(kAMn, kBMn));
+              if constexpr (kPair)
+                tc_mma(d_tmem, ad, bd, (kb != kb0 || k != 0) ? 1u : 0u, idesc(kAMn, kBMn));
+              else
+                tc_mma_single(d_tmem, ad, bd, (kb != kb0 || k != 0) ? 1u : 0u,
+                              idesc(false, false, kBM));
             }
-            tc_commit_pair(empty_bar(stage));  // frees the stage in both CTAs
+            // frees the stage (in both CTAs of a pair)
+            if constexpr (kPair) tc_commit_pair(empty_bar(stage));
+            else tc_commit_local(empty_bar(stage));
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1u;
             }
           }
           if (!ok) break;
-          tc_commit_pair(tfull_bar(acc));  // accumulator ready in both CTAs
+          // accumulator ready (in both CTAs of a pair)
+          if constexpr (kPair) tc_commit_pair(tfull_bar(acc));
+          else tc_commit_local(tfull_bar(acc));
           acc ^= 1;
           if (acc == 0) acc_phase ^= 1u;
         }
-        tc_commit_pair(drain_bar);  // arrives once every MMA issued here is done
+        // arrives once every MMA issued here is done
+        if constexpr (kPair) tc_commit_pair(drain_bar);
+        else tc_commit_local(drain_bar);
       }
       drain_wait(drain_bar, 0);
     }
@@ -520,7 +592,8 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
       tc_fence_after();
       epi.consume(u, t_lane + static_cast<uint32_t>(acc * kBN), rank, lane_grp, lane);
       tc_fence_before();
-      mbar_arrive_cluster(cluster_addr(tempty_bar(acc), 0));
+      if constexpr (kPair) mbar_arrive_cluster(cluster_addr(tempty_bar(acc), 0));
+      else mbar_arrive_local(tempty_bar(acc));
       epi.after_release(u, rank, lane_grp, lane);
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
@@ -533,13 +606,18 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
   tc_fence_before();
   __syncthreads();
   __syncwarp();
-  cluster_sync();  // no remote arrive or copy into either CTA is still pending
+  if constexpr (kPair) cluster_sync();  // no remote arrive or copy into either CTA is still pending
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(kTmemCols)
-                 : "memory");
+    if constexpr (kPair)
+      asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                   "r"(kTmemCols)
+                   : "memory");
+    else
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                   "r"(kTmemCols)
+                   : "memory");
   }
 }
 
@@ -566,6 +644,9 @@ bool encode_bf16_3d_store(CUtensorMap* map, void* base, int64_t S, int64_t rows,
 // Persistent grid (in CTAs, even) for `units` units on `sm_count` SMs under the
 // process-wide CTA limit: one CTA pair per two SMs, never more pairs than units.
 int pair_grid(int sm_count, int64_t units);
+
+// The same in CTAs for CTAs that work alone (SingleRing): one per SM.
+int single_grid(int sm_count, int64_t units);
 
 // Let `kernel` launch with `bytes` of dynamic shared memory (once per kernel
 // and context).
