@@ -48,9 +48,9 @@ using namespace tc;
 
 // Ring geometry of the gradient kernel (both operands K-major, like the fused
 // forward) and of the two products (M/N-major operands).  The gradient kernel
-// picks its ring by batch as the fused forward does (one 256-row block streams
-// W from HBM: narrow ring, 1-3 us per call less at T = 128; more: wide); with
-// the 256-bit G stores below the wide ring saves ~8 us per call at T = 512.  The products ran ~1% faster on
+// picks its form by batch as the fused forward does (up to 128 rows: one CTA
+// per tile; one 256-row block: the narrow ring; more: the wide ring, which
+// with the 256-bit G stores below saves ~8 us per call at T = 512).  The products ran ~1% faster on
 // the narrow ring (both products; the dH product alone on the wide ring: no
 // change).
 using GradHRing = NarrowRing;  // dH = G W (A K-major)
@@ -197,12 +197,26 @@ struct GradEpilogue {
 };
 
 template <class R>
+__device__ __forceinline__ void grad_body(const CUtensorMap* tmA, const CUtensorMap* tmB,
+                                          const GradArgs& a) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) *a.ticket = 0u;
+  GradEpilogue epi{&a};
+  run_pair_pipeline<R>(tmA, tmB, a.tiles, epi, a.err);
+}
+
+template <class R>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     lp_grad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ GradArgs a) {
-  if (blockIdx.x == 0 && threadIdx.x == 0) *a.ticket = 0u;
-  GradEpilogue epi{&a};
-  run_pair_pipeline<R>(&tmA, &tmB, a.tiles, epi, a.err);
+  grad_body<R>(&tmA, &tmB, a);
+}
+
+// Batches of at most 128 rows: one CTA per tile, as in the fused forward.
+__global__ void __launch_bounds__(kThreads, 1)
+    lp_grad_single_kernel(const __grid_constant__ CUtensorMap tmA,
+                          const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ GradArgs a) {
+  grad_body<SingleRing>(&tmA, &tmB, a);
 }
 
 // ---------------------------------------------------------------------- GEMM
@@ -659,6 +673,9 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
         if (e == cudaSuccess)
           e = set_smem_limit(reinterpret_cast<const void*>(lp_grad_kernel<NarrowRing>),
                              NarrowRing::kSmemBytes);
+        if (e == cudaSuccess)
+          e = set_smem_limit(reinterpret_cast<const void*>(lp_grad_single_kernel),
+                             SingleRing::kSmemBytes);
         return e;
       }) != cudaSuccess)
     return LP_ERR_CUDA;
@@ -696,8 +713,9 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
     GradArgs g;
     g.tiles.V = V;
     g.tiles.n_mb = static_cast<int>((T + 2 * kBM - 1) / (2 * kBM));
+    const bool single = T <= kBM;
     const bool wide = g.tiles.n_mb > 1;
-    const int bk = wide ? WideRing::kBK : NarrowRing::kBK;
+    const int bk = wide ? WideRing::kBK : single ? SingleRing::kBK : NarrowRing::kBK;
     g.tiles.n_kb = static_cast<int>((d + bk - 1) / bk);
     g.tiles.n_tiles_q = static_cast<int>(tiles_per_quarter(V));
     const int64_t total = int64_t(g.tiles.n_mb) * 4 * g.tiles.n_tiles_q;
@@ -714,9 +732,11 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
     g.ld_g = L.V8;
     g.inv_tau = tau.inv_hi;
     g.T = static_cast<int>(T);
-    const int grid = pair_grid(dev.sm_count, total);
+    const int grid = single ? single_grid(dev.sm_count, total) : pair_grid(dev.sm_count, total);
     if (wide)
       lp_grad_kernel<WideRing><<<grid, kThreads, WideRing::kSmemBytes, stream>>>(tmA, tmB, g);
+    else if (single)
+      lp_grad_single_kernel<<<grid, kThreads, SingleRing::kSmemBytes, stream>>>(tmA, tmB, g);
     else
       lp_grad_kernel<NarrowRing><<<grid, kThreads, NarrowRing::kSmemBytes, stream>>>(tmA, tmB, g);
     if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
