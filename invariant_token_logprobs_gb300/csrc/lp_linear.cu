@@ -323,6 +323,9 @@ __device__ __forceinline__ void linear_body(const CUtensorMap* tmA, const CUtens
   // words 1..3 of the error header belong to the backward's kernels; a call
   // of this kernel starts them at zero too
   if (blockIdx.x == 0 && threadIdx.x == 0) a.err[1] = a.err[2] = a.err[3] = 0u;
+  // the merge kernel (a programmatic dependent of this grid) may be scheduled
+  // now: it waits for this grid to finish before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   StateEpilogue epi{&a};
   run_pair_pipeline<R>(tmA, tmB, a.tiles, epi, a.err, a.withhold_first_load);
 }
@@ -355,6 +358,9 @@ __global__ void __launch_bounds__(128)
                          float* __restrict__ entropy, QuarterState* __restrict__ partials_out,
                          float* __restrict__ lse) {
   __shared__ __align__(16) QuarterState qs[kQuarters];
+  // launched as a programmatic dependent of the fused kernel: wait for that
+  // grid to finish and its stores to be visible (a no-op in a plain launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int ql = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t row = blockIdx.x;
@@ -521,9 +527,24 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
     lp_linear_kernel<NarrowRing><<<grid, kThreads, NarrowRing::kSmemBytes, stream>>>(tmA, tmB, a);
   if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
   if (ev_stop != nullptr && cudaEventRecord(ev_stop, stream) != cudaSuccess) return LP_ERR_CUDA;
-  lp_tile_merge_kernel<<<static_cast<unsigned>(T), 128, 0, stream>>>(
-      a.chunks, targets, a.err, n_q, a.tiles.n_tiles_q, V_total, a.inv_tau, a.tau, T, logp, entropy,
-      reinterpret_cast<QuarterState*>(partials_out), lse);
+  // the merge as a programmatic dependent launch: its launch overlaps the
+  // tail of the fused kernel instead of following it (~2 us per call at
+  // T <= 128; no change at T = 512)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(T));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, lp_tile_merge_kernel, static_cast<const float4*>(a.chunks), targets,
+                         static_cast<const uint32_t*>(a.err), n_q, a.tiles.n_tiles_q, V_total,
+                         a.inv_tau, a.tau, T, logp, entropy,
+                         reinterpret_cast<QuarterState*>(partials_out), lse) != cudaSuccess)
+    return LP_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }
 
