@@ -494,14 +494,16 @@ def run_lp(args):
         logits_item = bench_logits(lp, synth, torch, dev, stream, peaks, peaks_kind, max_over,
                                    world, rank)
 
-    sweep_item = None
-    if not args.no_sweep:
-        sweep_item = bench_batch_sweep(lp, torch, x, dev, stream, peaks, peaks_kind, max_over)
-
     backward_item = None
     if not args.no_backward:
         backward_item = bench_backward(lp, torch, x, dev, stream, peaks, peaks_kind, max_over,
                                        world)
+
+    # last of the GPU items: its seconds of load would otherwise leave the
+    # items after it running in a hotter, more power-capped state
+    sweep_item = None
+    if not args.no_sweep:
+        sweep_item = bench_batch_sweep(lp, torch, x, dev, stream, peaks, peaks_kind, max_over)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
