@@ -151,8 +151,9 @@ using namespace tc;
 struct QuarterTiles {
   int64_t V;       // full vocabulary size
   int64_t w_row0;  // global vocabulary index of W row 0
-  int n_mb;        // 256-row blocks
-  int n_kb;        // 64-wide K blocks
+  int n_mb;        // row blocks
+  int mb_rows;     // rows per block: 256 for CTA pairs, 128 for CTAs alone
+  int n_kb;        // K blocks of the ring
   int q_first;
   int n_tiles_q;
   int total;
@@ -168,7 +169,7 @@ struct QuarterTiles {
                                          int& kb1) const {
     int mb, ql, j;
     decode(u, mb, ql, j);
-    a_row = mb * (2 * kBM) + static_cast<int>(rank) * kBM;
+    a_row = mb * mb_rows + static_cast<int>(rank) * kBM;
     b_row = static_cast<int>(quarter_begin(V, q_first + ql) - w_row0) + j * kBN +
             static_cast<int>(rank) * kBNHalf;
     kb0 = 0;
@@ -241,7 +242,8 @@ struct StateEpilogue {
                                           int lane) {
     int mb, ql, j;
     a->tiles.decode(u, mb, ql, j);
-    const int64_t row = static_cast<int64_t>(mb) * (2 * kBM) + rank * kBM + lane_grp * 32 + lane;
+    const int64_t row =
+        static_cast<int64_t>(mb) * a->tiles.mb_rows + rank * kBM + lane_grp * 32 + lane;
     const int64_t y = row < a->T ? a->targets[row] : -1;
     int valid;
     int64_t tile_c0;
@@ -298,7 +300,8 @@ struct StateEpilogue {
   __device__ __forceinline__ void after_release(int u, uint32_t rank, int lane_grp, int lane) {
     int mb, ql, j;
     a->tiles.decode(u, mb, ql, j);
-    const int64_t row = static_cast<int64_t>(mb) * (2 * kBM) + rank * kBM + lane_grp * 32 + lane;
+    const int64_t row =
+        static_cast<int64_t>(mb) * a->tiles.mb_rows + rank * kBM + lane_grp * 32 + lane;
     if (row < a->T) {
       const int64_t idx = (row * a->n_q + ql) * a->tiles.n_tiles_q + j;
       if (LP_CHECK(ql < a->n_q && j < a->tiles.n_tiles_q &&
@@ -317,6 +320,12 @@ struct StateEpilogue {
 // tensor-bound and the 3 x 128 ring is 4-12% faster (T = 512: 370 against
 // 386 us; T = 2048: 1365 against 1540 us).  Every form issues the MMAs of an
 // accumulator element in the same K order, so the bits do not change.
+// Batches of at most this many rows run one CTA per tile and 128-row block.
+// Above 128 rows a pair does the same tensor work with less shared-memory
+// traffic per SM: lone CTAs at T = 192 / 256 took 238 / 242 us against 216 /
+// 222 us as pairs (same bits).
+constexpr int64_t kSingleMaxRows = kBM;
+
 template <class R>
 __device__ __forceinline__ void linear_body(const CUtensorMap* tmA, const CUtensorMap* tmB,
                                             const LinearArgs& a) {
@@ -496,9 +505,10 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
   LinearArgs a;
   a.tiles.V = V_total;
   a.tiles.w_row0 = w_row0;
-  a.tiles.n_mb = static_cast<int>((T + 2 * kBM - 1) / (2 * kBM));
-  const bool single = T <= kBM;  // one CTA per tile: no pair half of zero rows
-  const bool wide = a.tiles.n_mb > 1;
+  const bool single = T <= kSingleMaxRows;  // one CTA per tile: no pair half of zero rows
+  a.tiles.mb_rows = single ? kBM : 2 * kBM;
+  a.tiles.n_mb = static_cast<int>((T + a.tiles.mb_rows - 1) / a.tiles.mb_rows);
+  const bool wide = !single && a.tiles.n_mb > 1;
   const int bk = wide ? WideRing::kBK : single ? SingleRing::kBK : NarrowRing::kBK;
   a.tiles.n_kb = static_cast<int>((d + bk - 1) / bk);
   a.tiles.q_first = q_first;
