@@ -3,16 +3,17 @@
 // the RL-Kernel H100 PCP evidence record, h100-pcp.json, section "validation").
 //
 // z = H W^T (bf16 inputs, fp32 accumulation) is formed one 256 x 256 tile at a
-// time in tensor memory by the CTA-pair pipeline of lp_tcgen05.cuh and reduced
+// time in tensor memory by the CTA-pair pipeline of lp_tcgen05.cuh (or, for
+// batches of at most 128 rows, one 128 x 256 tile per CTA alone) and reduced
 // on the spot to a per-row state (max, sum-exp, sum-exp*(z-max), target logit);
 // the T x V logits never reach global memory.
 //
 // Tiling.  The vocabulary is cut into four quarters [floor(qV/4),
 // floor((q+1)V/4)); each quarter into 256-column tiles counted from the
 // quarter's first column (the last tile of a quarter is masked past the
-// quarter's end).  Rows are cut into 256-row blocks.  A work unit is one
-// (row block, quarter, tile); its per-row state goes to the workspace, and a
-// second kernel merges the tiles of each quarter (rebased to the quarter's
+// quarter's end).  Rows are cut into 256-row blocks (128 for lone CTAs).  A
+// work unit is one (row block, quarter, tile); its per-row state goes to the
+// workspace, and a second kernel merges the tiles of each quarter (rebased to the quarter's
 // maximum, summed in a fixed tree) and then the quarters as (Q0 + Q1) +
 // (Q2 + Q3).  Every value depends only on the row and on the fixed tile grid
 // of its quarter: not on T, the row's offset, the shard, the grid size or the
