@@ -13,9 +13,9 @@
 // quarter's first column (the last tile of a quarter is masked past the
 // quarter's end).  Rows are cut into 256-row blocks (128 for lone CTAs).  A
 // work unit is one (row block, quarter, tile); its per-row state goes to the
-// workspace, and a second kernel merges the tiles of each quarter (rebased to the quarter's
-// maximum, summed in a fixed tree) and then the quarters as (Q0 + Q1) +
-// (Q2 + Q3).  Every value depends only on the row and on the fixed tile grid
+// workspace, and a second kernel merges the tiles of each quarter (rebased to
+// the quarter's maximum, summed in a fixed tree) and then the quarters as
+// (Q0 + Q1) + (Q2 + Q3).  Every value depends only on the row and on the fixed tile grid
 // of its quarter: not on T, the row's offset, the shard, the grid size or the
 // order in which CTAs pick up tiles.  Units are taken round-robin in
 // (tile, row block) order so that the pairs that share a W tile run at the
