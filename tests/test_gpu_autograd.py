@@ -1,0 +1,49 @@
+"""The torch.autograd binding of the fused path against direct calls of the
+library: forward bits, and gradients equal to lp_linear_logprob_backward's
+(rounded to the inputs' bf16) for a loss on both outputs and on logp alone."""
+
+import pytest
+import torch
+
+from invariant_token_logprobs_gb300 import lp, synth
+from invariant_token_logprobs_gb300.autograd import linear_logprob
+from _gpu_helpers import bits
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def _b16(t):
+    return t.contiguous().view(torch.int16).cpu()
+
+
+@pytest.mark.parametrize("T,tau", [(64, 1.0), (300, 0.7)])
+def test_autograd_matches_direct_calls(T, tau):
+    lp.load()
+    x = synth.fused_inputs("fused_tiny", device=DEV, T=T, d=256, V=20000, seed=11)
+    g = torch.Generator(device=DEV).manual_seed(3)
+    a = torch.randn(T, generator=g, device=DEV)
+    b = torch.randn(T, generator=g, device=DEV)
+    H = x.H.clone().requires_grad_(True)
+    W = x.W.clone().requires_grad_(True)
+    logp, ent = linear_logprob(H, W, x.y, tau)
+    ref_lp, ref_ent, _ = lp.linear_logprob_lse(x.H, x.W, x.y, tau)
+    assert torch.equal(bits(logp.detach()), bits(ref_lp))
+    assert torch.equal(bits(ent.detach()), bits(ref_ent))
+    ((logp * a).sum() + (ent * b).sum()).backward()
+    gH, gW = lp.linear_logprob_backward(x.H, x.W, x.y, a, b, temperature=tau,
+                                        grad_W_dtype=torch.bfloat16)
+    assert H.grad.dtype == torch.bfloat16 and W.grad.dtype == torch.bfloat16
+    assert torch.equal(_b16(H.grad), _b16(gH.to(torch.bfloat16)))
+    assert torch.equal(_b16(W.grad), _b16(gW))
+
+
+def test_autograd_logp_only_and_frozen_weight():
+    lp.load()
+    x = synth.fused_inputs("fused_tiny", device=DEV, T=48, d=256, V=8192, seed=12)
+    a = torch.randn(48, generator=torch.Generator(device=DEV).manual_seed(4), device=DEV)
+    H = x.H.clone().requires_grad_(True)
+    logp, _ = linear_logprob(H, x.W, x.y)
+    (logp * a).sum().backward()
+    gH, _ = lp.linear_logprob_backward(x.H, x.W, x.y, a, None, with_grad_W=False)
+    assert torch.equal(_b16(H.grad), _b16(gH.to(torch.bfloat16)))
