@@ -663,6 +663,30 @@ def bench_logits(lp, synth, torch, dev, stream, peaks, peaks_kind, max_over, wor
     ms = max_over(e0.elapsed_time(e1)) / K
     nbytes = 4.0 * T * V + 8.0 * T + 8.0 * T
     gbs = nbytes / (ms / 1e3) / 1e9
+    # the backward (dL/dz) on the same logits, with the forward's log Z and entropy
+    _, ent_s, lse_s = lp.logprob_from_logits_lse(z.z, z.y)
+    g = torch.Generator(device=dev).manual_seed(17)
+    gl = torch.randn(T, generator=g, device=dev)
+    ge = torch.randn(T, generator=g, device=dev)
+    grad = torch.empty_like(z.z)
+    for _ in range(3):
+        lp.lp_logprob_from_logits_backward(z.z, z.y, 1.0, lse_s, ent_s, gl, ge, grad)
+    KB = 20
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(KB):
+        lp.lp_logprob_from_logits_backward(z.z, z.y, 1.0, lse_s, ent_s, gl, ge, grad)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_b = max_over(e0.elapsed_time(e1)) / KB
+    bytes_b = 8.0 * T * V + 32.0 * T
+    gbs_b = bytes_b / (ms_b / 1e3) / 1e9
+    del grad
+    backward = {"us_per_call": ms_b * 1e3, "kernel": "lp_logits_grad_kernel",
+                "achieved": gbs_b, "unit": "GB/s", "frac": gbs_b / peaks["hbm_gbs"],
+                "algorithmic_bytes_per_launch": bytes_b,
+                "note": "lp_logprob_from_logits_backward, fp32 dL/dz [T, V] written (logits read "
+                        "once, gradient written once)"}
     return {"workload": "logits_peaked", "T": T, "V": V, "value": whole_job_throughput(T, 1, world, ms),
             "unit": "rows/s", "us_per_call": ms * 1e3, "gpu_launches_per_call": 1,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -670,7 +694,8 @@ def bench_logits(lp, synth, torch, dev, stream, peaks, peaks_kind, max_over, wor
                          "traffic": profile_traffic(LOGITS_PROFILE_SUMMARY, LOGITS_SOURCES),
                          "kernel": "lp_logits_final_kernel",
                          "algorithmic_bytes_per_launch": nbytes,
-                         "peak_source": f"{peaks_kind} copy bandwidth"}}
+                         "peak_source": f"{peaks_kind} copy bandwidth"},
+            "backward": backward}
 
 
 def run_tp(args):

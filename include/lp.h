@@ -294,6 +294,54 @@ LP_API lp_status lp_linear_logprob_partials_temperature(
     float* partials_out, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Backward of the logits path: the gradient of
+ *     L = sum_t grad_logp[t] * logp[t] + grad_entropy[t] * entropy[t]
+ * with respect to the logits, for logp and entropy of softmax(z / tau) (the
+ * trainer of the RL-Kernel H100 PCP evidence record back-propagates through
+ * the log-probabilities it computes; h100-pcp.json, section "comparison").
+ * With log p = z / tau - log Z and p = exp(log p):
+ *     dL/dz[t, v] = (grad_logp[t] (delta(v, y_t) - p) -
+ *                    grad_entropy[t] p (log p + entropy[t])) / tau,
+ * a term with p = 0 being 0 and a row whose target is outside [0, V)
+ * contributing no logp term.  Rows are independent and every element is
+ * computed alone, so the bits do not depend on T or the row's offset.
+ * ------------------------------------------------------------------------ */
+
+/*
+ * lp_logprob_from_logits_lse: lp_logprob_from_logits_temperature (same bits)
+ * that also writes lse_out[t] = log Z = log sum_v exp(z[t, v] / tau) (float32
+ * [T]); keep lse_out and entropy_out for lp_logprob_from_logits_backward.
+ * All three outputs are required.
+ */
+LP_API lp_status lp_logprob_from_logits_lse(const float* logits, int64_t ld_logits,
+                                            const int64_t* targets, int64_t T, int64_t V,
+                                            float temperature, float* logp_out,
+                                            float* entropy_out, float* lse_out, void* stream);
+
+/*
+ * lp_logprob_from_logits_backward:
+ *   logits, ld_logits, targets, T, V, temperature: as in
+ *               lp_logprob_from_logits_temperature.
+ *   saved_lse, saved_entropy  [T] float32 from lp_logprob_from_logits_lse on
+ *               the same logits, targets and temperature (required).
+ *   grad_logp, grad_entropy   [T] float32 upstream gradients, each NULL for
+ *               zero; at least one must be given.
+ *   grad_logits [T, V] float32 output, row stride ld_grad >= V elements; it
+ *               must not overlap the logits.  Rows and the logits' rows need
+ *               not be 16-byte aligned (aligned rows use 16-byte accesses).
+ * One pass over the logits: 8 T V bytes of HBM traffic.  Errors: as the
+ * other logits-path calls; an overlap of grad_logits and logits is
+ * LP_ERR_INVALID_ARGUMENT.
+ */
+LP_API lp_status lp_logprob_from_logits_backward(const float* logits, int64_t ld_logits,
+                                                 const int64_t* targets, int64_t T, int64_t V,
+                                                 float temperature, const float* saved_lse,
+                                                 const float* saved_entropy,
+                                                 const float* grad_logp,
+                                                 const float* grad_entropy, float* grad_logits,
+                                                 int64_t ld_grad, void* stream);
+
+/* ------------------------------------------------------------------------
  * Backward of the fused path: gradients of
  *     L = sum_t grad_logp[t] * logp[t] + grad_entropy[t] * entropy[t]
  * with respect to H and W, for logp and entropy of softmax(H W^T / tau).

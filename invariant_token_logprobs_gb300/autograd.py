@@ -1,6 +1,7 @@
-"""torch.autograd binding of the fused path.
+"""torch.autograd bindings of the fused path and of the logits path.
 
     logp, entropy = linear_logprob(H, W, y, temperature=1.0)
+    logp, entropy = logprob_from_logits(z, y, temperature=1.0)
 
 returns the selected-token log-probabilities and entropies of z = H W^T / tau
 (lp_linear_logprob_lse) and back-propagates into H and W through
@@ -53,3 +54,31 @@ def linear_logprob(H: torch.Tensor, W: torch.Tensor, y: torch.Tensor,
     """(logp [T], entropy [T]) float32 of the fused path, differentiable in H and W
     (bf16 H [T, d] and W [V, d], int64 targets y [T])."""
     return _LinearLogprob.apply(H, W, y, temperature)
+
+
+class _LogprobFromLogits(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, z, y, temperature):
+        logp, entropy, lse = lp.logprob_from_logits_lse(z, y, temperature)
+        ctx.save_for_backward(z, y, lse, entropy)
+        ctx.temperature = float(temperature)
+        ctx.set_materialize_grads(False)
+        return logp, entropy
+
+    @staticmethod
+    def backward(ctx, g_logp, g_entropy):
+        z, y, lse, entropy = ctx.saved_tensors
+        if not ctx.needs_input_grad[0] or (g_logp is None and g_entropy is None):
+            return None, None, None
+        gl = None if g_logp is None else g_logp.float().contiguous()
+        ge = None if g_entropy is None else g_entropy.float().contiguous()
+        grad = lp.logprob_from_logits_backward(z, y, gl, ge, ctx.temperature, saved_lse=lse,
+                                               saved_entropy=entropy)
+        return grad, None, None
+
+
+def logprob_from_logits(z: torch.Tensor, y: torch.Tensor, temperature: float = 1.0):
+    """(logp [T], entropy [T]) float32 of the logits path, differentiable in the
+    float32 logits z [T, V] (rows contiguous; int64 targets y [T]); the backward
+    is lp_logprob_from_logits_backward with the forward's log Z and entropy."""
+    return _LogprobFromLogits.apply(z, y, temperature)

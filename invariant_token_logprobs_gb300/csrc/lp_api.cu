@@ -223,7 +223,63 @@ lp_status lp_logprob_from_logits_temperature(const float* logits, int64_t ld_log
   const lp_status st = lp::current_device(&dev);
   if (st != LP_OK) return st;
   return lp::launch_logits_final(logits, ld_logits, targets, T, V, tau, logp_out,
-                                 entropy_out, static_cast<cudaStream_t>(stream));
+                                 entropy_out, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+lp_status lp_logprob_from_logits_lse(const float* logits, int64_t ld_logits,
+                                     const int64_t* targets, int64_t T, int64_t V,
+                                     float temperature, float* logp_out, float* entropy_out,
+                                     float* lse_out, void* stream) {
+  lp::TauArgs tau;
+  if (!lp::make_tau(temperature, &tau)) return LP_ERR_INVALID_ARGUMENT;
+  if (T < 0 || T > lp::kMaxDim / 4 || V < 1 || V > lp::kMaxDim || ld_logits < V)
+    return LP_ERR_INVALID_ARGUMENT;
+  if (T == 0) return LP_OK;
+  if (logits == nullptr || targets == nullptr || logp_out == nullptr || entropy_out == nullptr ||
+      lse_out == nullptr)
+    return LP_ERR_INVALID_ARGUMENT;
+  if (!lp::aligned(logits, 4) || !lp::aligned(targets, 8) || !lp::aligned(logp_out, 4) ||
+      !lp::aligned(entropy_out, 4) || !lp::aligned(lse_out, 4))
+    return LP_ERR_MISALIGNED;
+  lp::Device dev;
+  const lp_status st = lp::current_device(&dev);
+  if (st != LP_OK) return st;
+  return lp::launch_logits_final(logits, ld_logits, targets, T, V, tau, logp_out, entropy_out,
+                                 lse_out, static_cast<cudaStream_t>(stream));
+}
+
+lp_status lp_logprob_from_logits_backward(const float* logits, int64_t ld_logits,
+                                          const int64_t* targets, int64_t T, int64_t V,
+                                          float temperature, const float* saved_lse,
+                                          const float* saved_entropy, const float* grad_logp,
+                                          const float* grad_entropy, float* grad_logits,
+                                          int64_t ld_grad, void* stream) {
+  lp::TauArgs tau;
+  if (!lp::make_tau(temperature, &tau)) return LP_ERR_INVALID_ARGUMENT;
+  if (T < 0 || T > lp::kMaxDim / 4 || V < 1 || V > lp::kMaxDim || ld_logits < V || ld_grad < V)
+    return LP_ERR_INVALID_ARGUMENT;
+  if (T == 0) return LP_OK;
+  if (logits == nullptr || targets == nullptr || saved_lse == nullptr ||
+      saved_entropy == nullptr || grad_logits == nullptr ||
+      (grad_logp == nullptr && grad_entropy == nullptr))
+    return LP_ERR_INVALID_ARGUMENT;
+  if (!lp::aligned(logits, 4) || !lp::aligned(targets, 8) || !lp::aligned(saved_lse, 4) ||
+      !lp::aligned(saved_entropy, 4) || !lp::aligned(grad_logp, 4) ||
+      !lp::aligned(grad_entropy, 4) || !lp::aligned(grad_logits, 4))
+    return LP_ERR_MISALIGNED;
+  // grad_logits must not overlap the logits (they are read through the
+  // read-only path while the gradient is written)
+  const uintptr_t z0 = reinterpret_cast<uintptr_t>(logits);
+  const uintptr_t z1 = z0 + 4 * static_cast<uintptr_t>((T - 1) * ld_logits + V);
+  const uintptr_t g0 = reinterpret_cast<uintptr_t>(grad_logits);
+  const uintptr_t g1 = g0 + 4 * static_cast<uintptr_t>((T - 1) * ld_grad + V);
+  if (g0 < z1 && z0 < g1) return LP_ERR_INVALID_ARGUMENT;
+  lp::Device dev;
+  const lp_status st = lp::current_device(&dev);
+  if (st != LP_OK) return st;
+  return lp::launch_logits_backward(logits, ld_logits, targets, T, V, tau, saved_lse,
+                                    saved_entropy, grad_logp, grad_entropy, grad_logits, ld_grad,
+                                    static_cast<cudaStream_t>(stream));
 }
 
 lp_status lp_logprob_partials_from_logits_temperature(const float* logits_shard,

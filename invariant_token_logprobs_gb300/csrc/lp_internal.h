@@ -89,7 +89,11 @@ struct TauArgs {
 // logits path
 lp_status launch_logits_final(const float* logits, int64_t ld, const int64_t* targets,
                               int64_t T, int64_t V, const TauArgs& tau, float* logp,
-                              float* entropy, cudaStream_t stream);
+                              float* entropy, float* lse, cudaStream_t stream);
+lp_status launch_logits_backward(const float* logits, int64_t ld, const int64_t* targets,
+                                 int64_t T, int64_t V, const TauArgs& tau, const float* lse,
+                                 const float* entropy, const float* g_logp, const float* g_ent,
+                                 float* grad, int64_t ld_grad, cudaStream_t stream);
 lp_status launch_logits_partials(const float* logits_shard, int64_t ld,
                                  const int64_t* targets, int64_t T, int64_t V_total,
                                  int q_first, int n_q, const TauArgs& tau, float* partials,

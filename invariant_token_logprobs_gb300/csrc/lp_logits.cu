@@ -309,7 +309,8 @@ __device__ __forceinline__ QuarterState quarter_state_any(const float* __restric
 __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, kCtasPerSm)
     lp_logits_final_kernel(const float* __restrict__ logits, int64_t ld,
                            const int64_t* __restrict__ targets, int64_t T, int64_t V, TauArgs tau,
-                           float* __restrict__ logp, float* __restrict__ entropy) {
+                           float* __restrict__ logp, float* __restrict__ entropy,
+                           float* __restrict__ lse) {
   __shared__ __align__(16) QuarterState qstates[kQuarters];
   const int q = blockIdx.x & 3;
   const int64_t row = blockIdx.x >> 2;
@@ -343,6 +344,7 @@ __global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(kThreads, kCtasPerSm
     if (threadIdx.x == 0 && geo_ok) {
       logp[row] = lp;
       if (entropy != nullptr) entropy[row] = ent;
+      if (lse != nullptr) lse[row] = lz;
     }
   }
 }
@@ -392,14 +394,88 @@ __global__ void __launch_bounds__(128)
   }
 }
 
+// dL/dz of L = sum_t g_logp[t] logp[t] + g_ent[t] entropy[t] over given
+// logits, the logits-path twin of the fused backward's gradient epilogue:
+// with zs = z / tau, log p = zs - log Z and p = exp(log p),
+//   G = (g_logp (delta(v, y) - p) - g_ent p (log p + entropy)) / tau,
+// where a term with p = 0 (a -inf logit, or one far below the maximum) is 0
+// and a row whose target is outside [0, V) has no logp term.  log Z and the
+// entropy are the forward's (lp_logprob_from_logits_lse).  One CTA per (row,
+// kGradChunk columns); whole chunks of 16-byte-aligned rows load four float4
+// per thread before computing, the rest goes 4 bytes at a time.
+constexpr int kGradVec = 4;                          // float4 per thread and chunk
+constexpr int64_t kGradChunk = kThreads * 4 * kGradVec;  // 4096 columns
+
+__device__ __forceinline__ float logits_grad(float z, int64_t col, int64_t y, float inv_tau,
+                                             float log_z, float ent, float gl, float ge) {
+  const float zs = inv_tau == 1.f ? z : __fmul_rn(z, inv_tau);
+  const float lp = __fsub_rn(zs, log_z);
+  const float p = exp_fast(lp);
+  float g = p == 0.f ? 0.f : -__fmul_rn(p, __fmaf_rn(ge, __fadd_rn(lp, ent), gl));
+  if (col == y) g = __fadd_rn(g, gl);
+  return inv_tau == 1.f ? g : __fmul_rn(g, inv_tau);
+}
+
+__global__ void __launch_bounds__(kThreads)
+    lp_logits_grad_kernel(const float* __restrict__ logits, int64_t ld,
+                          const int64_t* __restrict__ targets, int64_t T, int64_t V,
+                          int64_t chunks, float inv_tau, const float* __restrict__ lse,
+                          const float* __restrict__ entropy, const float* __restrict__ g_logp,
+                          const float* __restrict__ g_ent, float* __restrict__ grad,
+                          int64_t ld_grad) {
+  const int64_t row = blockIdx.x / chunks;
+  const int64_t c0 = (blockIdx.x % chunks) * kGradChunk;
+  if (!LP_CHECK(row < T && V <= ld && V <= ld_grad, kChkRowIndex)) return;
+  const int64_t c1 = min(V, c0 + kGradChunk);
+  const int64_t y = targets[row];
+  const bool y_ok = y >= 0 && y < V;
+  const float gl = (g_logp != nullptr && y_ok) ? g_logp[row] : 0.f;
+  const float ge = g_ent != nullptr ? g_ent[row] : 0.f;
+  const float log_z = lse[row];
+  const float ent = entropy[row];
+  const float* zr = logits + row * ld;
+  float* gr = grad + row * ld_grad;
+  const int tid = threadIdx.x;
+  const bool vec = ((reinterpret_cast<uintptr_t>(zr) | reinterpret_cast<uintptr_t>(gr)) & 15u) == 0;
+  if (vec && c1 - c0 == kGradChunk) {
+    float4 z[kGradVec];
+#pragma unroll
+    for (int k = 0; k < kGradVec; ++k) z[k] = load_stream(zr + c0 + 4 * (tid + k * kThreads));
+#pragma unroll
+    for (int k = 0; k < kGradVec; ++k) {
+      const int64_t col = c0 + 4 * (tid + k * kThreads);
+      float4 g;
+      g.x = logits_grad(z[k].x, col, y, inv_tau, log_z, ent, gl, ge);
+      g.y = logits_grad(z[k].y, col + 1, y, inv_tau, log_z, ent, gl, ge);
+      g.z = logits_grad(z[k].z, col + 2, y, inv_tau, log_z, ent, gl, ge);
+      g.w = logits_grad(z[k].w, col + 3, y, inv_tau, log_z, ent, gl, ge);
+      *reinterpret_cast<float4*>(gr + col) = g;
+    }
+    return;
+  }
+  for (int64_t col = c0 + tid; col < c1; col += kThreads)
+    gr[col] = logits_grad(zr[col], col, y, inv_tau, log_z, ent, gl, ge);
+}
+
 }  // namespace
 
 lp_status launch_logits_final(const float* logits, int64_t ld, const int64_t* targets,
                               int64_t T, int64_t V, const TauArgs& tau, float* logp,
-                              float* entropy, cudaStream_t stream) {
+                              float* entropy, float* lse, cudaStream_t stream) {
   const int64_t blocks = T * kQuarters;
   lp_logits_final_kernel<<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-      logits, ld, targets, T, V, tau, logp, entropy);
+      logits, ld, targets, T, V, tau, logp, entropy, lse);
+  return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
+}
+
+lp_status launch_logits_backward(const float* logits, int64_t ld, const int64_t* targets,
+                                 int64_t T, int64_t V, const TauArgs& tau, const float* lse,
+                                 const float* entropy, const float* g_logp, const float* g_ent,
+                                 float* grad, int64_t ld_grad, cudaStream_t stream) {
+  const int64_t chunks = (V + kGradChunk - 1) / kGradChunk;
+  if (T * chunks >= (int64_t(1) << 31)) return LP_ERR_INVALID_ARGUMENT;
+  lp_logits_grad_kernel<<<static_cast<unsigned>(T * chunks), kThreads, 0, stream>>>(
+      logits, ld, targets, T, V, chunks, tau.inv_hi, lse, entropy, g_logp, g_ent, grad, ld_grad);
   return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }
 

@@ -37,6 +37,10 @@ __all__ = [
     "lp_linear_logprob_partials_workspace_size",
     "lp_linear_logprob_partials",
     "lp_logprob_from_logits_temperature",
+    "lp_logprob_from_logits_lse",
+    "lp_logprob_from_logits_backward",
+    "logprob_from_logits_lse",
+    "logprob_from_logits_backward",
     "lp_logprob_partials_from_logits_temperature",
     "lp_linear_logprob_temperature",
     "lp_linear_logprob_partials_temperature",
@@ -105,6 +109,10 @@ _SIGNATURES = {
         _int, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _int, _int, _vp, _vp, _sz, _vp]),
     "lp_logprob_from_logits_temperature": (
         _int, [_vp, _i64, _vp, _i64, _i64, ctypes.c_float, _vp, _vp, _vp]),
+    "lp_logprob_from_logits_lse": (
+        _int, [_vp, _i64, _vp, _i64, _i64, ctypes.c_float, _vp, _vp, _vp, _vp]),
+    "lp_logprob_from_logits_backward": (
+        _int, [_vp, _i64, _vp, _i64, _i64, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _i64, _vp]),
     "lp_logprob_partials_from_logits_temperature": (
         _int, [_vp, _i64, _vp, _i64, _i64, _int, _int, ctypes.c_float, _vp, _vp]),
     "lp_linear_logprob_temperature": (
@@ -270,6 +278,30 @@ def lp_logprob_from_logits_temperature(logits, targets, temperature, logp, entro
     _check("lp_logprob_from_logits_temperature", load().lp_logprob_from_logits_temperature(
         _ptr(logits), _row_stride(logits), _ptr(targets), T, V, float(temperature), _ptr(logp),
         _ptr(entropy), _stream(stream)))
+
+
+def lp_logprob_from_logits_lse(logits, targets, temperature, logp, entropy, lse,
+                               stream=None) -> None:
+    if logits.dtype != torch.float32 or targets.dtype != torch.int64:
+        raise TypeError("logits must be float32 and targets int64")
+    T, V = logits.shape
+    _check("lp_logprob_from_logits_lse", load().lp_logprob_from_logits_lse(
+        _ptr(logits), _row_stride(logits), _ptr(targets), T, V, float(temperature), _ptr(logp),
+        _ptr(entropy), _ptr(lse), _stream(stream)))
+
+
+def lp_logprob_from_logits_backward(logits, targets, temperature, saved_lse, saved_entropy,
+                                    grad_logp, grad_entropy, grad_logits, stream=None) -> None:
+    if logits.dtype != torch.float32 or grad_logits.dtype != torch.float32 \
+            or targets.dtype != torch.int64:
+        raise TypeError("logits and grad_logits must be float32 and targets int64")
+    T, V = logits.shape
+    if tuple(grad_logits.shape) != (T, V):
+        raise ValueError("grad_logits must have the logits' shape")
+    _check("lp_logprob_from_logits_backward", load().lp_logprob_from_logits_backward(
+        _ptr(logits), _row_stride(logits), _ptr(targets), T, V, float(temperature),
+        _ptr(saved_lse), _ptr(saved_entropy), _ptr(grad_logp), _ptr(grad_entropy),
+        _ptr(grad_logits), _row_stride(grad_logits), _stream(stream)))
 
 
 def lp_logprob_partials_from_logits_temperature(logits_shard, targets, vocab_total, shard_index,
@@ -444,6 +476,28 @@ def logprob_from_logits(z: torch.Tensor, y: torch.Tensor, with_entropy: bool = T
     else:
         lp_logprob_from_logits_temperature(z, y, temperature, logp, ent, stream)
     return logp, ent
+
+
+def logprob_from_logits_lse(z: torch.Tensor, y: torch.Tensor, temperature: float = 1.0,
+                            stream=None):
+    """(logp, entropy, lse) [T] fp32 of the logits path; keep entropy and lse for the backward."""
+    T = z.shape[0]
+    out = [torch.empty(T, dtype=torch.float32, device=z.device) for _ in range(3)]
+    lp_logprob_from_logits_lse(z, y, temperature, out[0], out[1], out[2], stream)
+    return tuple(out)
+
+
+def logprob_from_logits_backward(z: torch.Tensor, y: torch.Tensor, grad_logp=None,
+                                 grad_entropy=None, temperature: float = 1.0, saved_lse=None,
+                                 saved_entropy=None, stream=None) -> torch.Tensor:
+    """dL/dz [T, V] fp32 for L = sum grad_logp * logp + grad_entropy * entropy; log Z and
+    the entropy are taken from the forward when given, else computed first."""
+    if saved_lse is None or saved_entropy is None:
+        _, saved_entropy, saved_lse = logprob_from_logits_lse(z, y, temperature, stream)
+    grad = torch.empty(z.shape, dtype=torch.float32, device=z.device)
+    lp_logprob_from_logits_backward(z, y, temperature, saved_lse, saved_entropy, grad_logp,
+                                    grad_entropy, grad, stream)
+    return grad
 
 
 def vocab_shard_range(vocab_total: int, shard_index: int, n_shards: int) -> tuple[int, int]:

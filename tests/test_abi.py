@@ -22,7 +22,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = lp.declared_symbols()
-    assert len(names) == 24
+    assert len(names) == 26
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(lp._SIGNATURES)
@@ -161,6 +161,11 @@ def test_merge_argument_errors(lib):
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")
 def test_valid_call_without_gb300_fails_loudly(lib):
     assert lib.lp_logprob_from_logits(A, 100, A, 4, 100, A, A, None) == UNSUPPORTED
+    assert lib.lp_logprob_from_logits_lse(A, 100, A, 4, 100, ctypes.c_float(1.0), A, A, A,
+                                          None) == UNSUPPORTED
+    G = A + (1 << 16)
+    assert lib.lp_logprob_from_logits_backward(A, 100, A, 4, 100, ctypes.c_float(1.0), A, A, A,
+                                               None, G, 100, None) == UNSUPPORTED
     ws = lp.lp_linear_logprob_workspace_size(64, 256, 8192)
     assert lib.lp_linear_logprob(A, 256, A, 256, A, 64, 256, 8192, A, A, A, ws, None) == UNSUPPORTED
     arr = (ctypes.c_void_p * 1)(A)
@@ -171,3 +176,24 @@ def test_valid_call_without_gb300_fails_loudly(lib):
     assert lib.lp_set_fault_injection(-1) == INVALID
     assert lib.lp_set_fault_injection(2) == OK
     assert lib.lp_set_fault_injection(0) == OK
+
+
+def test_logits_backward_argument_checks(lib):
+    f = ctypes.c_float(1.0)
+    G = A + (1 << 16)
+    # no upstream gradient, no saved statistics, a short row stride, overlap
+    assert lib.lp_logprob_from_logits_backward(A, 100, A, 4, 100, f, A, A, None, None, G, 100,
+                                               None) == INVALID
+    assert lib.lp_logprob_from_logits_backward(A, 100, A, 4, 100, f, None, A, A, None, G, 100,
+                                               None) == INVALID
+    assert lib.lp_logprob_from_logits_backward(A, 100, A, 4, 100, f, A, A, A, None, G, 99,
+                                               None) == INVALID
+    assert lib.lp_logprob_from_logits_backward(A, 100, A, 4, 100, f, A, A, A, None, A + 396, 100,
+                                               None) == INVALID
+    assert lib.lp_logprob_from_logits_backward(A, 100, A, 4, 100, ctypes.c_float(0.0), A, A, A,
+                                               None, G, 100, None) == INVALID
+    assert lib.lp_logprob_from_logits_backward(A, 100, A, 4, 100, f, A, A, A + 2, None, G, 100,
+                                               None) == MISALIGNED
+    assert lib.lp_logprob_from_logits_lse(A, 100, A, 4, 100, f, A, A, None, None) == INVALID
+    assert lib.lp_logprob_from_logits_backward(A, 100, A, 0, 100, f, None, None, None, None, None,
+                                               100, None) == OK

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 from invariant_token_logprobs_gb300 import lp, synth
-from invariant_token_logprobs_gb300.autograd import linear_logprob
+from invariant_token_logprobs_gb300.autograd import linear_logprob, logprob_from_logits
 from _gpu_helpers import bits
 
 pytestmark = pytest.mark.gpu
@@ -47,3 +47,16 @@ def test_autograd_logp_only_and_frozen_weight():
     (logp * a).sum().backward()
     gH, _ = lp.linear_logprob_backward(x.H, x.W, x.y, a, None, with_grad_W=False)
     assert torch.equal(_b16(H.grad), _b16(gH.to(torch.bfloat16)))
+
+
+def test_logits_autograd_matches_direct_calls():
+    lp.load()
+    z = synth.logits_inputs("logits_peaked", device=DEV, T=32, V=9001, seed=15)
+    g = torch.Generator(device=DEV).manual_seed(5)
+    a = torch.randn(32, generator=g, device=DEV)
+    b = torch.randn(32, generator=g, device=DEV)
+    zz = z.z.clone().requires_grad_(True)
+    logp, ent = logprob_from_logits(zz, z.y, 0.7)
+    ((logp * a).sum() + (ent * b).sum()).backward()
+    ref = lp.logprob_from_logits_backward(z.z, z.y, a, b, temperature=0.7)
+    assert torch.equal(bits(zz.grad), bits(ref))
