@@ -32,6 +32,15 @@ def run_cases(lp, synth) -> dict:
     wide = torch.empty((16, 20001), device=DEV)
     wide[:, :20000] = x.z
     keep("logits.unaligned", *lp.logprob_from_logits(wide[:, :20000], x.y))
+    # logits-path backward: with log Z, aligned and unaligned rows, temperature
+    g = torch.Generator(device=DEV)
+    g.manual_seed(16)
+    gl = torch.randn(16, generator=g, device=DEV)
+    ge = torch.randn(16, generator=g, device=DEV)
+    keep("logits.lse", *lp.logprob_from_logits_lse(x.z, x.y, 0.7))
+    keep("logits.bwd", lp.logprob_from_logits_backward(x.z, x.y, gl, ge))
+    keep("logits.bwd.unaligned", lp.logprob_from_logits_backward(wide[:, :20000], x.y, gl, None,
+                                                                 temperature=0.7))
 
     # fused path: tiny, fewer than 16 rows, ragged V, temperature, shards, lse, no-alloc
     for T, d, V in [(64, 256, 8192), (5, 256, 3001), (300, 512, 20003)]:
