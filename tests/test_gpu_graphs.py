@@ -97,6 +97,42 @@ def test_logits_graph_replay_bytes_equal_eager(tau):
             assert torch.equal(bits(ent), bits(ref[1])), f"T={T} trial {trial} entropy"
 
 
+def test_logits_backward_graph_replay_bytes_equal_eager():
+    # forward with log Z and the backward captured together, as a trainer would
+    V = 151936
+    for T in SIZES:
+        z = torch.empty((T, V), device=DEV)
+        y = torch.empty((T,), dtype=torch.int64, device=DEV)
+        gl = torch.empty(T, device=DEV)
+        ge = torch.empty(T, device=DEV)
+        logp = torch.empty(T, device=DEV)
+        ent = torch.empty(T, device=DEV)
+        lse = torch.empty(T, device=DEV)
+        grad = torch.empty((T, V), device=DEV)
+
+        def fn():
+            lp.lp_logprob_from_logits_lse(z, y, 0.7, logp, ent, lse)
+            lp.lp_logprob_from_logits_backward(z, y, 0.7, lse, ent, gl, ge, grad)
+
+        x0 = synth.logits_inputs("logits_peaked", device=DEV, T=T, V=V, seed=60 + T)
+        z.copy_(x0.z)
+        y.copy_(x0.y)
+        gl.normal_()
+        ge.normal_()
+        g = _capture(fn)
+        for trial in range(2):
+            x = synth.logits_inputs("logits_peaked", device=DEV, T=T, V=V, seed=900 * T + trial)
+            z.copy_(x.z)
+            y.copy_(x.y)
+            gl.normal_()
+            ge.normal_()
+            g.replay()
+            torch.cuda.synchronize()
+            ref = lp.logprob_from_logits_backward(z.clone(), y.clone(), gl.clone(), ge.clone(),
+                                                  temperature=0.7)
+            assert torch.equal(bits(grad), bits(ref)), f"T={T} trial {trial}"
+
+
 def test_sharded_merge_graph_replay_bytes_equal_eager():
     """The 4-shard fused path (partials of each shard, then the fixed merge)
     captured as one graph equals the eager unsharded call."""
