@@ -341,6 +341,32 @@ LP_API lp_status lp_logprob_from_logits_backward(const float* logits, int64_t ld
                                                  const float* grad_entropy, float* grad_logits,
                                                  int64_t ld_grad, void* stream);
 
+/*
+ * Vocabulary-parallel training on the logits path.  Each rank merges the
+ * all-gathered quarter states with lp_merge_partials_lse, which also writes
+ * log Z per row, and then takes the gradient of its own shard of the logits
+ * with lp_logprob_partials_from_logits_backward: every element depends only on
+ * its logit and the row's log Z and entropy, so the shards' gradients are the
+ * columns of the single-GPU gradient, bit for bit, with no further exchange.
+ *
+ * lp_merge_partials_lse: lp_merge_partials (same bits) that also writes
+ *   lse_out[t] = log Z (float32 [T]); all three outputs are required.
+ * lp_logprob_partials_from_logits_backward: lp_logprob_from_logits_backward
+ *   over the shard lp_vocab_shard_range(vocab_total, shard_index, n_shards) of
+ *   the logits; logits_shard and grad_shard are [T, end - begin] (row strides
+ *   ld_logits and ld_grad), targets are global vocabulary indices, and
+ *   saved_lse / saved_entropy are the merged rows' (lp_merge_partials_lse).
+ */
+LP_API lp_status lp_merge_partials_lse(const float* const* shard_partials, int n_shards,
+                                       int64_t T, float* logp_out, float* entropy_out,
+                                       float* lse_out, void* stream);
+
+LP_API lp_status lp_logprob_partials_from_logits_backward(
+    const float* logits_shard, int64_t ld_logits, const int64_t* targets, int64_t T,
+    int64_t vocab_total, int shard_index, int n_shards, float temperature,
+    const float* saved_lse, const float* saved_entropy, const float* grad_logp,
+    const float* grad_entropy, float* grad_shard, int64_t ld_grad, void* stream);
+
 /* ------------------------------------------------------------------------
  * Backward of the fused path: gradients of
  *     L = sum_t grad_logp[t] * logp[t] + grad_entropy[t] * entropy[t]

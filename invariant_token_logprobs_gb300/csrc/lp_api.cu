@@ -248,12 +248,15 @@ lp_status lp_logprob_from_logits_lse(const float* logits, int64_t ld_logits,
                                  lse_out, static_cast<cudaStream_t>(stream));
 }
 
-lp_status lp_logprob_from_logits_backward(const float* logits, int64_t ld_logits,
-                                          const int64_t* targets, int64_t T, int64_t V,
-                                          float temperature, const float* saved_lse,
-                                          const float* saved_entropy, const float* grad_logp,
-                                          const float* grad_entropy, float* grad_logits,
-                                          int64_t ld_grad, void* stream) {
+namespace {
+// The logits-path backward over columns col0 .. col0 + V - 1 of a vocabulary
+// of V_total (the whole vocabulary, or one shard of it).
+lp_status logits_backward_checked(const float* logits, int64_t ld_logits, const int64_t* targets,
+                                  int64_t T, int64_t V, int64_t col0, int64_t V_total,
+                                  float temperature, const float* saved_lse,
+                                  const float* saved_entropy, const float* grad_logp,
+                                  const float* grad_entropy, float* grad_logits, int64_t ld_grad,
+                                  void* stream) {
   lp::TauArgs tau;
   if (!lp::make_tau(temperature, &tau)) return LP_ERR_INVALID_ARGUMENT;
   if (T < 0 || T > lp::kMaxDim / 4 || V < 1 || V > lp::kMaxDim || ld_logits < V || ld_grad < V)
@@ -277,9 +280,34 @@ lp_status lp_logprob_from_logits_backward(const float* logits, int64_t ld_logits
   lp::Device dev;
   const lp_status st = lp::current_device(&dev);
   if (st != LP_OK) return st;
-  return lp::launch_logits_backward(logits, ld_logits, targets, T, V, tau, saved_lse,
-                                    saved_entropy, grad_logp, grad_entropy, grad_logits, ld_grad,
-                                    static_cast<cudaStream_t>(stream));
+  return lp::launch_logits_backward(logits, ld_logits, targets, T, V, col0, V_total, tau,
+                                    saved_lse, saved_entropy, grad_logp, grad_entropy, grad_logits,
+                                    ld_grad, static_cast<cudaStream_t>(stream));
+}
+}  // namespace
+
+lp_status lp_logprob_from_logits_backward(const float* logits, int64_t ld_logits,
+                                          const int64_t* targets, int64_t T, int64_t V,
+                                          float temperature, const float* saved_lse,
+                                          const float* saved_entropy, const float* grad_logp,
+                                          const float* grad_entropy, float* grad_logits,
+                                          int64_t ld_grad, void* stream) {
+  return logits_backward_checked(logits, ld_logits, targets, T, V, 0, V, temperature, saved_lse,
+                                 saved_entropy, grad_logp, grad_entropy, grad_logits, ld_grad,
+                                 stream);
+}
+
+lp_status lp_logprob_partials_from_logits_backward(
+    const float* logits_shard, int64_t ld_logits, const int64_t* targets, int64_t T,
+    int64_t vocab_total, int shard_index, int n_shards, float temperature,
+    const float* saved_lse, const float* saved_entropy, const float* grad_logp,
+    const float* grad_entropy, float* grad_shard, int64_t ld_grad, void* stream) {
+  int64_t begin = 0, end = 0;
+  const lp_status st = lp_vocab_shard_range(vocab_total, shard_index, n_shards, &begin, &end);
+  if (st != LP_OK) return st;
+  return logits_backward_checked(logits_shard, ld_logits, targets, T, end - begin, begin,
+                                 vocab_total, temperature, saved_lse, saved_entropy, grad_logp,
+                                 grad_entropy, grad_shard, ld_grad, stream);
 }
 
 lp_status lp_logprob_partials_from_logits_temperature(const float* logits_shard,
@@ -327,7 +355,29 @@ lp_status lp_merge_partials(const float* const* shard_partials, int n_shards, in
   lp::Device dev;
   const lp_status st = lp::current_device(&dev);
   if (st != LP_OK) return st;
-  return lp::launch_merge_partials(shard_partials, n_shards, T, logp_out, entropy_out,
+  return lp::launch_merge_partials(shard_partials, n_shards, T, logp_out, entropy_out, nullptr,
+                                   static_cast<cudaStream_t>(stream));
+}
+
+lp_status lp_merge_partials_lse(const float* const* shard_partials, int n_shards, int64_t T,
+                                float* logp_out, float* entropy_out, float* lse_out,
+                                void* stream) {
+  if (!(n_shards == 1 || n_shards == 2 || n_shards == 4)) return LP_ERR_INVALID_ARGUMENT;
+  if (T < 0 || T > lp::kMaxDim) return LP_ERR_INVALID_ARGUMENT;
+  if (T == 0) return LP_OK;
+  if (shard_partials == nullptr || logp_out == nullptr || entropy_out == nullptr ||
+      lse_out == nullptr)
+    return LP_ERR_INVALID_ARGUMENT;
+  for (int i = 0; i < n_shards; ++i) {
+    if (shard_partials[i] == nullptr) return LP_ERR_INVALID_ARGUMENT;
+    if (!lp::aligned(shard_partials[i], 16)) return LP_ERR_MISALIGNED;
+  }
+  if (!lp::aligned(logp_out, 4) || !lp::aligned(entropy_out, 4) || !lp::aligned(lse_out, 4))
+    return LP_ERR_MISALIGNED;
+  lp::Device dev;
+  const lp_status st = lp::current_device(&dev);
+  if (st != LP_OK) return st;
+  return lp::launch_merge_partials(shard_partials, n_shards, T, logp_out, entropy_out, lse_out,
                                    static_cast<cudaStream_t>(stream));
 }
 

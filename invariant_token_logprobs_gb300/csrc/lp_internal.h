@@ -90,16 +90,18 @@ struct TauArgs {
 lp_status launch_logits_final(const float* logits, int64_t ld, const int64_t* targets,
                               int64_t T, int64_t V, const TauArgs& tau, float* logp,
                               float* entropy, float* lse, cudaStream_t stream);
+// the logits' V columns are global columns col0 .. col0 + V - 1 of V_total
 lp_status launch_logits_backward(const float* logits, int64_t ld, const int64_t* targets,
-                                 int64_t T, int64_t V, const TauArgs& tau, const float* lse,
-                                 const float* entropy, const float* g_logp, const float* g_ent,
-                                 float* grad, int64_t ld_grad, cudaStream_t stream);
+                                 int64_t T, int64_t V, int64_t col0, int64_t V_total,
+                                 const TauArgs& tau, const float* lse, const float* entropy,
+                                 const float* g_logp, const float* g_ent, float* grad,
+                                 int64_t ld_grad, cudaStream_t stream);
 lp_status launch_logits_partials(const float* logits_shard, int64_t ld,
                                  const int64_t* targets, int64_t T, int64_t V_total,
                                  int q_first, int n_q, const TauArgs& tau, float* partials,
                                  cudaStream_t stream);
 lp_status launch_merge_partials(const float* const* shard_partials, int n_shards, int64_t T,
-                                float* logp, float* entropy, cudaStream_t stream);
+                                float* logp, float* entropy, float* lse, cudaStream_t stream);
 
 // fused path
 size_t linear_workspace_bytes(int64_t T, int64_t d, int64_t V_total, int n_q);

@@ -377,7 +377,8 @@ __global__ void __launch_bounds__(128)
                              const QuarterState* __restrict__ p1,
                              const QuarterState* __restrict__ p2,
                              const QuarterState* __restrict__ p3, int n_shards, int64_t T,
-                             float* __restrict__ logp, float* __restrict__ entropy) {
+                             float* __restrict__ logp, float* __restrict__ entropy,
+                             float* __restrict__ lse) {
   const int64_t row = int64_t(blockIdx.x) * (blockDim.x / 4) + (threadIdx.x >> 2);
   const int q = threadIdx.x & 3;
   const QuarterState* shard[4] = {p0, p1, p2, p3};
@@ -391,6 +392,7 @@ __global__ void __launch_bounds__(128)
   if (row < T && q == 0) {
     logp[row] = lp;
     if (entropy != nullptr) entropy[row] = ent;
+    if (lse != nullptr) lse[row] = lz;
   }
 }
 
@@ -402,12 +404,16 @@ __global__ void __launch_bounds__(128)
 // and a row whose target is outside [0, V) has no logp term.  log Z and the
 // entropy are the forward's (lp_logprob_from_logits_lse).  One CTA per (row,
 // kGradChunk columns); whole chunks of 16-byte-aligned rows load four float4
-// per thread before computing, the rest goes 4 bytes at a time.
+// per thread before computing, the rest goes 4 bytes at a time.  The logits
+// may be a vocabulary shard: its V columns are global columns col0 .. col0 +
+// V - 1 of a vocabulary of V_total (every element depends only on its own
+// logit and the row's log Z and entropy, so shards give the bits of the whole).
 constexpr int kGradVec = 4;                          // float4 per thread and chunk
 constexpr int64_t kGradChunk = kThreads * 4 * kGradVec;  // 4096 columns
 
 __device__ __forceinline__ float logits_grad(float z, int64_t col, int64_t y, float inv_tau,
                                              float log_z, float ent, float gl, float ge) {
+  // col and y: shard-relative (y outside the shard never matches)
   const float zs = inv_tau == 1.f ? z : __fmul_rn(z, inv_tau);
   const float lp = __fsub_rn(zs, log_z);
   const float p = exp_fast(lp);
@@ -419,7 +425,8 @@ __device__ __forceinline__ float logits_grad(float z, int64_t col, int64_t y, fl
 __global__ void __launch_bounds__(kThreads)
     lp_logits_grad_kernel(const float* __restrict__ logits, int64_t ld,
                           const int64_t* __restrict__ targets, int64_t T, int64_t V,
-                          int64_t chunks, float inv_tau, const float* __restrict__ lse,
+                          int64_t col0, int64_t V_total, int64_t chunks, float inv_tau,
+                          const float* __restrict__ lse,
                           const float* __restrict__ entropy, const float* __restrict__ g_logp,
                           const float* __restrict__ g_ent, float* __restrict__ grad,
                           int64_t ld_grad) {
@@ -427,8 +434,9 @@ __global__ void __launch_bounds__(kThreads)
   const int64_t c0 = (blockIdx.x % chunks) * kGradChunk;
   if (!LP_CHECK(row < T && V <= ld && V <= ld_grad, kChkRowIndex)) return;
   const int64_t c1 = min(V, c0 + kGradChunk);
-  const int64_t y = targets[row];
-  const bool y_ok = y >= 0 && y < V;
+  const int64_t y_global = targets[row];
+  const bool y_ok = y_global >= 0 && y_global < V_total;
+  const int64_t y = y_global - col0;  // this shard's column of the target
   const float gl = (g_logp != nullptr && y_ok) ? g_logp[row] : 0.f;
   const float ge = g_ent != nullptr ? g_ent[row] : 0.f;
   const float log_z = lse[row];
@@ -469,13 +477,15 @@ lp_status launch_logits_final(const float* logits, int64_t ld, const int64_t* ta
 }
 
 lp_status launch_logits_backward(const float* logits, int64_t ld, const int64_t* targets,
-                                 int64_t T, int64_t V, const TauArgs& tau, const float* lse,
-                                 const float* entropy, const float* g_logp, const float* g_ent,
-                                 float* grad, int64_t ld_grad, cudaStream_t stream) {
+                                 int64_t T, int64_t V, int64_t col0, int64_t V_total,
+                                 const TauArgs& tau, const float* lse, const float* entropy,
+                                 const float* g_logp, const float* g_ent, float* grad,
+                                 int64_t ld_grad, cudaStream_t stream) {
   const int64_t chunks = (V + kGradChunk - 1) / kGradChunk;
   if (T * chunks >= (int64_t(1) << 31)) return LP_ERR_INVALID_ARGUMENT;
   lp_logits_grad_kernel<<<static_cast<unsigned>(T * chunks), kThreads, 0, stream>>>(
-      logits, ld, targets, T, V, chunks, tau.inv_hi, lse, entropy, g_logp, g_ent, grad, ld_grad);
+      logits, ld, targets, T, V, col0, V_total, chunks, tau.inv_hi, lse, entropy, g_logp, g_ent,
+      grad, ld_grad);
   return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }
 
@@ -491,14 +501,14 @@ lp_status launch_logits_partials(const float* logits_shard, int64_t ld,
 }
 
 lp_status launch_merge_partials(const float* const* shard_partials, int n_shards, int64_t T,
-                                float* logp, float* entropy, cudaStream_t stream) {
+                                float* logp, float* entropy, float* lse, cudaStream_t stream) {
   const QuarterState* p[4] = {nullptr, nullptr, nullptr, nullptr};
   for (int i = 0; i < n_shards; ++i)
     p[i] = reinterpret_cast<const QuarterState*>(shard_partials[i]);
   const int threads = 128;  // 32 rows per block, one thread per quarter
   const int64_t blocks = (T + threads / 4 - 1) / (threads / 4);
   lp_merge_partials_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-      p[0], p[1], p[2], p[3], n_shards, T, logp, entropy);
+      p[0], p[1], p[2], p[3], n_shards, T, logp, entropy, lse);
   return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }
 

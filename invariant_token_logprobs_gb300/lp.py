@@ -39,6 +39,8 @@ __all__ = [
     "lp_logprob_from_logits_temperature",
     "lp_logprob_from_logits_lse",
     "lp_logprob_from_logits_backward",
+    "lp_merge_partials_lse",
+    "lp_logprob_partials_from_logits_backward",
     "logprob_from_logits_lse",
     "logprob_from_logits_backward",
     "lp_logprob_partials_from_logits_temperature",
@@ -113,6 +115,10 @@ _SIGNATURES = {
         _int, [_vp, _i64, _vp, _i64, _i64, ctypes.c_float, _vp, _vp, _vp, _vp]),
     "lp_logprob_from_logits_backward": (
         _int, [_vp, _i64, _vp, _i64, _i64, ctypes.c_float, _vp, _vp, _vp, _vp, _vp, _i64, _vp]),
+    "lp_merge_partials_lse": (_int, [ctypes.POINTER(_vp), _int, _i64, _vp, _vp, _vp, _vp]),
+    "lp_logprob_partials_from_logits_backward": (
+        _int, [_vp, _i64, _vp, _i64, _i64, _int, _int, ctypes.c_float, _vp, _vp, _vp, _vp, _vp,
+               _i64, _vp]),
     "lp_logprob_partials_from_logits_temperature": (
         _int, [_vp, _i64, _vp, _i64, _i64, _int, _int, ctypes.c_float, _vp, _vp]),
     "lp_linear_logprob_temperature": (
@@ -224,6 +230,31 @@ def lp_merge_partials(shard_partials: Sequence[torch.Tensor], T: int, logp, entr
     arr = (_vp * len(shard_partials))(*[p.data_ptr() for p in shard_partials])
     _check("lp_merge_partials", load().lp_merge_partials(
         arr, len(shard_partials), T, _ptr(logp), _ptr(entropy), _stream(stream)))
+
+
+def lp_merge_partials_lse(shard_partials: Sequence[torch.Tensor], T: int, logp, entropy, lse,
+                          stream=None) -> None:
+    arr = (_vp * len(shard_partials))(*[p.data_ptr() for p in shard_partials])
+    _check("lp_merge_partials_lse", load().lp_merge_partials_lse(
+        arr, len(shard_partials), T, _ptr(logp), _ptr(entropy), _ptr(lse), _stream(stream)))
+
+
+def lp_logprob_partials_from_logits_backward(logits_shard, targets, vocab_total, shard_index,
+                                             n_shards, temperature, saved_lse, saved_entropy,
+                                             grad_logp, grad_entropy, grad_shard,
+                                             stream=None) -> None:
+    if logits_shard.dtype != torch.float32 or grad_shard.dtype != torch.float32 \
+            or targets.dtype != torch.int64:
+        raise TypeError("logits and gradient must be float32 and targets int64")
+    if tuple(grad_shard.shape) != tuple(logits_shard.shape):
+        raise ValueError("grad_shard must have the shard's shape")
+    T = logits_shard.shape[0]
+    _check("lp_logprob_partials_from_logits_backward",
+           load().lp_logprob_partials_from_logits_backward(
+               _ptr(logits_shard), _row_stride(logits_shard), _ptr(targets), T, vocab_total,
+               shard_index, n_shards, float(temperature), _ptr(saved_lse), _ptr(saved_entropy),
+               _ptr(grad_logp), _ptr(grad_entropy), _ptr(grad_shard), _row_stride(grad_shard),
+               _stream(stream)))
 
 
 def lp_linear_logprob_workspace_size(T: int, d: int, V: int) -> int:

@@ -23,6 +23,12 @@ their own all-gather kernels for this exchange (the strict R/R trace runbook,
 RL-Kernel issue #342, section 3, deterministic_all_gather_kernel); here the
 exchange is torch.distributed's all_gather_into_tensor.
 
+Training on the logits path needs nothing more: the forward's merge can also
+return each row's log Z (lp_merge_partials_lse), and every element of dL/dz
+depends only on its own logit and its row's log Z and entropy, so each rank
+takes the gradient of its own columns (lp_logprob_partials_from_logits_backward)
+and holds exactly those columns of the single-GPU gradient, with no exchange.
+
 Collective backends: NCCL gathers the device buffers directly; any other
 backend (gloo) gathers host copies, staged through pinned memory.  All compute
 runs in liblp's kernels; this module only moves the states.
@@ -119,3 +125,41 @@ def vocab_parallel_logprob_from_logits(z_shard: torch.Tensor, y: torch.Tensor, v
                                                 temperature=temperature)
         gathered = gather_partials(parts, group)
         return lp.merge_partials(gathered, with_entropy=with_entropy)
+
+
+def vocab_parallel_logprob_from_logits_lse(z_shard: torch.Tensor, y: torch.Tensor,
+                                           vocab_total: int, group=None,
+                                           temperature: float = 1.0, stream=None):
+    """(logp, entropy, lse) [T] of softmax(z / tau) from the column-split logits:
+    the forward of vocabulary-parallel training; every rank gets the same bits."""
+    rank, n, b, e = shard_of_rank(vocab_total, group)
+    if z_shard.shape[1] != e - b:
+        raise ValueError(f"rank {rank} holds {z_shard.shape[1]} logit columns, its shard has {e - b}")
+    T = z_shard.shape[0]
+    with _on(stream):
+        parts = lp.logprob_partials_from_logits(z_shard, y, vocab_total, rank, n,
+                                                temperature=temperature)
+        gathered = gather_partials(parts, group)
+        out = [torch.empty(T, dtype=torch.float32, device=z_shard.device) for _ in range(3)]
+        lp.lp_merge_partials_lse(gathered, T, out[0], out[1], out[2])
+        return tuple(out)
+
+
+def vocab_parallel_logprob_from_logits_backward(z_shard: torch.Tensor, y: torch.Tensor,
+                                                vocab_total: int, saved_lse: torch.Tensor,
+                                                saved_entropy: torch.Tensor, grad_logp=None,
+                                                grad_entropy=None, group=None,
+                                                temperature: float = 1.0,
+                                                stream=None) -> torch.Tensor:
+    """dL/dz for this rank's columns, from the merged rows' log Z and entropy
+    (vocab_parallel_logprob_from_logits_lse): no exchange, and the bits of the
+    same columns of the single-GPU gradient."""
+    rank, n, b, e = shard_of_rank(vocab_total, group)
+    if z_shard.shape[1] != e - b:
+        raise ValueError(f"rank {rank} holds {z_shard.shape[1]} logit columns, its shard has {e - b}")
+    grad = torch.empty(z_shard.shape, dtype=torch.float32, device=z_shard.device)
+    with _on(stream):
+        lp.lp_logprob_partials_from_logits_backward(z_shard, y, vocab_total, rank, n, temperature,
+                                                    saved_lse, saved_entropy, grad_logp,
+                                                    grad_entropy, grad)
+    return grad

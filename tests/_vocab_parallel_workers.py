@@ -9,6 +9,19 @@ import torch
 import torch.distributed as dist
 
 
+def upstream(T: int):
+    """The upstream gradients of the logits-path training test (same on every rank)."""
+    g = torch.Generator(device="cuda:0")
+    g.manual_seed(21)
+    return (torch.randn(T, generator=g, device="cuda:0"),
+            torch.randn(T, generator=g, device="cuda:0"))
+
+
+def sha256_of(t: torch.Tensor) -> str:
+    import hashlib
+    return hashlib.sha256(t.contiguous().cpu().numpy().tobytes()).hexdigest()
+
+
 def _init(rank: int, world: int, init_file: str) -> None:
     # a file rendezvous: no TCP port to pick or to collide on
     dist.init_process_group("gloo", init_method=f"file://{init_file}", rank=rank,
@@ -51,12 +64,25 @@ def gpu_vocab_parallel(rank: int, world: int, init_file: str, out_dir: str, path
             w_shard = x.W[b:e]
             del x.W
             logp, ent = vp.vocab_parallel_linear_logprob(x.H, w_shard, x.y, V)
-        else:
+        elif path == "logits":
             x = synth.logits_inputs("logits_peaked", device="cuda:0")
             V = x.z.shape[1]
             _, n, b, e = vp.shard_of_rank(V)
             logp, ent = vp.vocab_parallel_logprob_from_logits(x.z[:, b:e], x.y, V,
                                                               temperature=0.7)
+        else:  # logits_train: forward with log Z, then this rank's columns of dL/dz
+            x = synth.logits_inputs("logits_peaked", device="cuda:0")
+            T, V = x.z.shape
+            _, n, b, e = vp.shard_of_rank(V)
+            gl, ge = upstream(T)
+            logp, ent, lse = vp.vocab_parallel_logprob_from_logits_lse(x.z[:, b:e], x.y, V,
+                                                                       temperature=0.7)
+            grad = vp.vocab_parallel_logprob_from_logits_backward(x.z[:, b:e], x.y, V, lse, ent,
+                                                                  gl, ge, temperature=0.7)
+            torch.cuda.synchronize()
+            torch.save({"logp": logp.cpu(), "ent": ent.cpu(), "lse": lse.cpu(),
+                        "grad_sha": sha256_of(grad)}, os.path.join(out_dir, f"rank{rank}.pt"))
+            return
         torch.cuda.synchronize()
         torch.save({"logp": logp.cpu(), "ent": ent.cpu()}, os.path.join(out_dir, f"rank{rank}.pt"))
     finally:

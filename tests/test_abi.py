@@ -22,7 +22,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = lp.declared_symbols()
-    assert len(names) == 26
+    assert len(names) == 28
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(lp._SIGNATURES)
