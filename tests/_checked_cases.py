@@ -41,6 +41,21 @@ def run_cases(lp, synth) -> dict:
     keep("logits.bwd", lp.logprob_from_logits_backward(x.z, x.y, gl, ge))
     keep("logits.bwd.unaligned", lp.logprob_from_logits_backward(wide[:, :20000], x.y, gl, None,
                                                                  temperature=0.7))
+    # vocabulary-parallel training: merge with log Z, each shard's gradient columns
+    for n in (2, 4):
+        parts = []
+        for i in range(n):
+            b, e = lp.vocab_shard_range(20000, i, n)
+            parts.append(lp.logprob_partials_from_logits(x.z[:, b:e], x.y, 20000, i, n))
+        m = [torch.empty(16, device=DEV) for _ in range(3)]
+        lp.lp_merge_partials_lse(parts, 16, m[0], m[1], m[2])
+        keep(f"logits.merge_lse{n}", *m)
+        for i in range(n):
+            b, e = lp.vocab_shard_range(20000, i, n)
+            gs = torch.empty((16, e - b), device=DEV)
+            lp.lp_logprob_partials_from_logits_backward(x.z[:, b:e], x.y, 20000, i, n, 1.0, m[2],
+                                                        m[1], gl, ge, gs)
+            keep(f"logits.bwd.shard{n}.{i}", gs)
 
     # fused path: tiny, fewer than 16 rows, ragged V, temperature, shards, lse, no-alloc
     for T, d, V in [(64, 256, 8192), (5, 256, 3001), (300, 512, 20003)]:
