@@ -170,6 +170,14 @@ def test_valid_call_without_gb300_fails_loudly(lib):
     assert lib.lp_linear_logprob(A, 256, A, 256, A, 64, 256, 8192, A, A, A, ws, None) == UNSUPPORTED
     arr = (ctypes.c_void_p * 1)(A)
     assert lib.lp_merge_partials(arr, 1, 8, A, A, None) == UNSUPPORTED
+    assert lib.lp_merge_partials_lse(arr, 1, 8, A, A, A, None) == UNSUPPORTED
+    assert lib.lp_logprob_partials_from_logits_backward(A, 100, A, 4, 200, 1, 2, ctypes.c_float(1.0),
+                                                        A, A, A, None, A + (1 << 16), 100,
+                                                        None) == UNSUPPORTED
+    # a shard index outside [0, n_shards) is an argument error before any device check
+    assert lib.lp_logprob_partials_from_logits_backward(A, 100, A, 4, 200, 2, 2, ctypes.c_float(1.0),
+                                                        A, A, A, None, A + (1 << 16), 100,
+                                                        None) == INVALID
     assert lib.lp_set_persistent_grid_limit(-1) == INVALID
     assert lib.lp_set_persistent_grid_limit(0) == OK
     assert lib.lp_set_fault_injection(3) == INVALID
