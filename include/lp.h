@@ -380,12 +380,17 @@ LP_API lp_status lp_logprob_partials_from_logits_backward(
  * G is formed in fp32 from recomputed logits and rounded to bf16 for the two
  * tensor-core products (fp32 accumulation).  Results are deterministic; a row
  * of grad_H depends only on that row's inputs.  A row whose target is outside
- * [0, V) contributes no logp gradient.
+ * [0, V) contributes no logp gradient.  grad_H is summed over fixed
+ * vocabulary ranges in a fixed order: when V % 64 == 0, seven ranges per
+ * quarter of the vocabulary (the quarters of the forward's reduction tree),
+ * summed in order, and the quarter sums as (Q0 + Q1) + (Q2 + Q3), which is
+ * what lets a vocabulary-parallel backward reproduce it (below); otherwise 19
+ * ranges of the whole vocabulary, summed in order.
  * ------------------------------------------------------------------------ */
 
 /* Workspace bytes of lp_linear_logprob_backward: the forward's workspace, the
- * bf16 G [T, V] (2 T V bytes) and 19 fp32 partial grad_H (76 T d bytes);
- * 0 for invalid sizes. */
+ * bf16 G [T, V] (2 T V bytes) and the fp32 partial grad_H (28 of T d floats
+ * when V % 64 == 0, else 19); 0 for invalid sizes. */
 LP_API size_t lp_linear_logprob_backward_workspace_size(int64_t T, int64_t d, int64_t V);
 
 /*
@@ -455,6 +460,62 @@ LP_API lp_status lp_linear_logprob_backward_ex(const void* H, int64_t ld_h, cons
                                                float* grad_H, void* grad_W, int grad_W_dtype,
                                                void* workspace, size_t workspace_bytes,
                                                void* stream);
+
+/*
+ * Vocabulary-parallel training on the fused path (the RL-Kernel logprob
+ * report grades TP4 against TP1 bit for bit: report.json,
+ * candidates.*.tp4_equals_tp1).  W is split by rows into the shards of
+ * lp_vocab_shard_range; every rank holds all of H, the targets and the
+ * merged rows' log Z and entropy (lp_merge_partials_lse over the all-gathered
+ * quarter states of lp_linear_logprob_partials).  Each rank then calls
+ * lp_linear_logprob_partials_backward on its shard, which writes
+ *   grad_W_shard = G_shard^T H, the rows of the single-GPU grad_W, and
+ *   grad_H_partial = the quarter-tree subtree of the shard's quarters
+ *                    (Q_i, or Q_i + Q_i+1 for two shards),
+ * and the ranks all-gather the partials in shard order and merge them with
+ * lp_merge_grad_h_partials (P0, P0 + P1, or (P0 + P1) + (P2 + P3)): grad_H and
+ * the concatenated grad_W are the bits of lp_linear_logprob_backward on one
+ * GPU, for any finite W.  The exchange moves bytes only (4 T d per rank).
+ *
+ * lp_linear_logprob_partials_backward:
+ *   H, ld_h, targets, T, d, temperature: as in lp_linear_logprob_backward;
+ *               targets are global vocabulary indices.
+ *   W_shard, ld_w  the shard's rows [end - begin, d] of W.
+ *   vocab_total, shard_index, n_shards  the shard (as lp_vocab_shard_range);
+ *               n_shards > 1 needs vocab_total % 64 == 0 (the quarters must
+ *               start on 16-column boundaries), else LP_ERR_INVALID_ARGUMENT.
+ *   saved_lse, saved_entropy  [T] float32 of the merged rows (required).
+ *   grad_logp, grad_entropy   as in lp_linear_logprob_backward.
+ *   grad_H_partial [T, d] float32 output, dense rows, 16-byte aligned.
+ *   grad_W_shard   [end - begin, d] output of grad_W_dtype, dense rows,
+ *               16-byte aligned, or NULL to skip it.
+ *   workspace   256-byte aligned, at least
+ *               lp_linear_logprob_partials_backward_workspace_size(T, d,
+ *               vocab_total, n_shards) bytes.
+ * With n_shards == 1 it is lp_linear_logprob_backward_ex with saved
+ * statistics (same bits).  Device-side timeouts: as lp_linear_logprob_backward
+ * (NaN outputs; lp_get_device_error on the workspace).
+ */
+LP_API size_t lp_linear_logprob_partials_backward_workspace_size(int64_t T, int64_t d,
+                                                                 int64_t vocab_total,
+                                                                 int n_shards);
+
+LP_API lp_status lp_linear_logprob_partials_backward(
+    const void* H, int64_t ld_h, const void* W_shard, int64_t ld_w, const int64_t* targets,
+    int64_t T, int64_t d, int64_t vocab_total, int shard_index, int n_shards, float temperature,
+    const float* saved_lse, const float* saved_entropy, const float* grad_logp,
+    const float* grad_entropy, float* grad_H_partial, void* grad_W_shard, int grad_W_dtype,
+    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * lp_merge_grad_h_partials: grad_H [T, d] float32 (dense rows) = the n_shards
+ * (1, 2 or 4) partials shard_grad_h[i] ([T, d] float32, dense rows, in shard
+ * order; a host array of device pointers) added as P0, P0 + P1 or
+ * (P0 + P1) + (P2 + P3).  Every pointer 16-byte aligned, d % 8 == 0.  grad_H
+ * may be one of the partials.
+ */
+LP_API lp_status lp_merge_grad_h_partials(const float* const* shard_grad_h, int n_shards,
+                                          int64_t T, int64_t d, float* grad_H, void* stream);
 
 /* ------------------------------------------------------------------------
  * Diagnostics and tuning.

@@ -9,6 +9,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 
@@ -520,7 +521,7 @@ lp_status lp_linear_logprob_partials(const void* H, int64_t ld_h, const void* W_
 
 size_t lp_linear_logprob_backward_workspace_size(int64_t T, int64_t d, int64_t V) {
   if (T < 0 || d < 1 || V < 1 || V > lp::kMaxDim || d > lp::kMaxDim) return 0;
-  return lp::linear_backward_workspace_bytes(T, d, V);
+  return lp::linear_backward_workspace_bytes(T, d, V, V);
 }
 
 lp_status lp_linear_logprob_backward_ex(const void* H, int64_t ld_h, const void* W, int64_t ld_w,
@@ -544,15 +545,92 @@ lp_status lp_linear_logprob_backward_ex(const void* H, int64_t ld_h, const void*
   if (!lp::aligned(grad_logp, 4) || !lp::aligned(grad_entropy, 4) || !lp::aligned(grad_H, 16) ||
       !lp::aligned(grad_W, 16) || !lp::aligned(workspace, 256))
     return LP_ERR_MISALIGNED;
-  if (workspace_bytes < lp::linear_backward_workspace_bytes(T, d, V))
+  if (workspace_bytes < lp::linear_backward_workspace_bytes(T, d, V, V))
     return LP_ERR_WORKSPACE_TOO_SMALL;
   lp::Device dev;
   st = lp::current_device(&dev);
   if (st != LP_OK) return st;
-  return lp::launch_linear_backward(dev, H, ld_h, W, ld_w, targets, T, d, V, tau, saved_lse,
-                                    saved_entropy, grad_logp, grad_entropy, grad_H, grad_W,
+  return lp::launch_linear_backward(dev, H, ld_h, W, ld_w, targets, T, d, V, V, 0, 4, tau,
+                                    saved_lse, saved_entropy, grad_logp, grad_entropy, grad_H,
+                                    grad_W, grad_W_dtype == LP_GRAD_W_BFLOAT16, workspace,
+                                    static_cast<cudaStream_t>(stream));
+}
+
+size_t lp_linear_logprob_partials_backward_workspace_size(int64_t T, int64_t d,
+                                                          int64_t vocab_total, int n_shards) {
+  if (T < 0 || d < 1 || d > lp::kMaxDim || vocab_total < 1 || vocab_total > lp::kMaxDim)
+    return 0;
+  if (!(n_shards == 1 || n_shards == 2 || n_shards == 4)) return 0;
+  size_t most = 0;  // the widest shard's
+  for (int i = 0; i < n_shards; ++i) {
+    int64_t b = 0, e = 0;
+    lp_vocab_shard_range(vocab_total, i, n_shards, &b, &e);
+    if (e > b) most = std::max(most, lp::linear_backward_workspace_bytes(T, d, e - b, vocab_total));
+  }
+  return most;
+}
+
+lp_status lp_linear_logprob_partials_backward(
+    const void* H, int64_t ld_h, const void* W_shard, int64_t ld_w, const int64_t* targets,
+    int64_t T, int64_t d, int64_t vocab_total, int shard_index, int n_shards, float temperature,
+    const float* saved_lse, const float* saved_entropy, const float* grad_logp,
+    const float* grad_entropy, float* grad_H_partial, void* grad_W_shard, int grad_W_dtype,
+    void* workspace, size_t workspace_bytes, void* stream) {
+  lp::TauArgs tau;
+  if (!lp::make_tau(temperature, &tau)) return LP_ERR_INVALID_ARGUMENT;
+  if (grad_W_dtype != LP_GRAD_W_FLOAT32 && grad_W_dtype != LP_GRAD_W_BFLOAT16)
+    return LP_ERR_INVALID_ARGUMENT;
+  lp_status st = lp::check_shard(shard_index, n_shards);
+  if (st != LP_OK) return st;
+  st = lp::check_fused_args(H, ld_h, W_shard, ld_w, targets, T, d, vocab_total);
+  if (st != LP_OK) return st;
+  // the quarters must start on 16-column boundaries for a shard to compute a
+  // subtree of the single-GPU order of grad_H
+  if (n_shards > 1 && vocab_total % 64 != 0) return LP_ERR_INVALID_ARGUMENT;
+  if (T == 0) return LP_OK;
+  if (grad_H_partial == nullptr || workspace == nullptr || saved_lse == nullptr ||
+      saved_entropy == nullptr || (grad_logp == nullptr && grad_entropy == nullptr))
+    return LP_ERR_INVALID_ARGUMENT;
+  if (T > (int64_t(1) << 24)) return LP_ERR_INVALID_ARGUMENT;
+  if (!lp::aligned(saved_lse, 4) || !lp::aligned(saved_entropy, 4) ||
+      !lp::aligned(grad_logp, 4) || !lp::aligned(grad_entropy, 4) ||
+      !lp::aligned(grad_H_partial, 16) || !lp::aligned(grad_W_shard, 16) ||
+      !lp::aligned(workspace, 256))
+    return LP_ERR_MISALIGNED;
+  int q_first, n_q;
+  lp::shard_quarters(shard_index, n_shards, q_first, n_q);
+  const int64_t begin = lp::quarter_begin(vocab_total, q_first);
+  const int64_t end = lp::quarter_begin(vocab_total, q_first + n_q);
+  if (end == begin) return LP_ERR_INVALID_ARGUMENT;  // only vocab_total < 4, n_shards 4
+  if (workspace_bytes < lp::linear_backward_workspace_bytes(T, d, end - begin, vocab_total))
+    return LP_ERR_WORKSPACE_TOO_SMALL;
+  lp::Device dev;
+  st = lp::current_device(&dev);
+  if (st != LP_OK) return st;
+  return lp::launch_linear_backward(dev, H, ld_h, W_shard, ld_w, targets, T, d, end - begin,
+                                    vocab_total, q_first, n_q, tau, saved_lse, saved_entropy,
+                                    grad_logp, grad_entropy, grad_H_partial, grad_W_shard,
                                     grad_W_dtype == LP_GRAD_W_BFLOAT16, workspace,
                                     static_cast<cudaStream_t>(stream));
+}
+
+lp_status lp_merge_grad_h_partials(const float* const* shard_grad_h, int n_shards, int64_t T,
+                                   int64_t d, float* grad_H, void* stream) {
+  if (!(n_shards == 1 || n_shards == 2 || n_shards == 4)) return LP_ERR_INVALID_ARGUMENT;
+  if (T < 0 || T > lp::kMaxDim || d < 1 || d > lp::kMaxDim) return LP_ERR_INVALID_ARGUMENT;
+  if (d % 8 != 0) return LP_ERR_MISALIGNED;
+  if (T == 0) return LP_OK;
+  if (shard_grad_h == nullptr || grad_H == nullptr) return LP_ERR_INVALID_ARGUMENT;
+  for (int i = 0; i < n_shards; ++i) {
+    if (shard_grad_h[i] == nullptr) return LP_ERR_INVALID_ARGUMENT;
+    if (!lp::aligned(shard_grad_h[i], 16)) return LP_ERR_MISALIGNED;
+  }
+  if (!lp::aligned(grad_H, 16)) return LP_ERR_MISALIGNED;
+  lp::Device dev;
+  const lp_status st = lp::current_device(&dev);
+  if (st != LP_OK) return st;
+  return lp::launch_merge_grad_h(dev, shard_grad_h, n_shards, T * d, grad_H,
+                                 static_cast<cudaStream_t>(stream));
 }
 
 lp_status lp_linear_logprob_backward(const void* H, int64_t ld_h, const void* W, int64_t ld_w,

@@ -33,6 +33,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <mutex>
 #include <type_traits>
 
@@ -57,21 +58,34 @@ using GradHRing = NarrowRing;  // dH = G W (A K-major)
 using GradWRing = NarrowRing;  // dW = G^T H (A M-major)
 template <bool kAMn>
 using GemmRing = std::conditional_t<kAMn, GradWRing, GradHRing>;
+constexpr int kGemmBK = GradHRing::kBK;  // K block of both products
+static_assert(GradWRing::kBK == kGemmBK, "one K block for the product work list");
 // the products' staging area starts where either ring ends
 static_assert(WideRing::kSmemEnd == NarrowRing::kSmemEnd, "one staging offset");
 constexpr int kGemmRingEnd = NarrowRing::kSmemEnd;
 
-// Fixed vocabulary ranges of the dH product (split K), summed in order.  A
-// constant, so the bits never depend on the GPU; 19 makes the 32 output tiles
-// of T = 512, d = 4096 exactly 8 waves of 76 CTA pairs (608 units).
+// Fixed vocabulary ranges of the dH product (split K).  When every quarter of
+// the vocabulary starts on a 16-column boundary (V % 64 == 0) each quarter is
+// cut into kRangesPerQuarter ranges, summed in order within the quarter, and
+// the quarter sums are added as (Q0 + Q1) + (Q2 + Q3): a shard of whole
+// quarters computes one subtree of that order, so the shards' partial dH merge
+// to the bits of one GPU.  Otherwise the whole vocabulary is cut into
+// kSplitsDH ranges summed in order.  Constants, so the bits never depend on
+// the GPU or the batch; 7 per quarter makes the 32 output tiles of T = 512,
+// d = 4096 11.8 waves of 76 CTA pairs, 19 exactly 8.
 constexpr int kSplitsDH = 19;
+constexpr int kRangesPerQuarter = 7;
+constexpr int kMaxSplitsDH = 4 * kRangesPerQuarter;
+static_assert(kMaxSplitsDH >= kSplitsDH, "partial buffers for either order");
 
 inline int64_t round8(int64_t x) { return (x + 7) / 8 * 8; }
 
 // ------------------------------------------------------------------ gradient
 
 struct GradTiles {  // same work list as the forward kernel: (row block, quarter, tile)
-  int64_t V;
+  int64_t V;       // full vocabulary size
+  int64_t w_row0;  // global vocabulary index of W's row 0 and of G's column 0
+  int q_first;     // first quarter of this call (a shard's quarters: q_first ..)
   int n_mb;
   int n_kb;
   int n_tiles_q;
@@ -88,7 +102,8 @@ struct GradTiles {  // same work list as the forward kernel: (row block, quarter
     int mb, q, j;
     decode(u, mb, q, j);
     a_row = mb * (2 * kBM) + static_cast<int>(rank) * kBM;
-    b_row = static_cast<int>(quarter_begin(V, q)) + j * kBN + static_cast<int>(rank) * kBNHalf;
+    b_row = static_cast<int>(quarter_begin(V, q_first + q) - w_row0) + j * kBN +
+            static_cast<int>(rank) * kBNHalf;
     kb0 = 0;
     kb1 = n_kb;
   }
@@ -101,7 +116,7 @@ struct GradArgs {
   const float* g_ent;     // [T] or NULL
   const float* lse;       // [T] log Z of the scaled logits
   const float* ent;       // [T] entropy
-  __nv_bfloat16* G;       // [T][ld_g]
+  __nv_bfloat16* G;       // [T][ld_g], column c: vocabulary index w_row0 + c
   uint32_t* err;
   uint32_t* ticket;       // finish counter of the dW product, zeroed here
   int64_t ld_g;
@@ -125,8 +140,8 @@ struct GradEpilogue {
     a->tiles.decode(u, mb, q, j);
     const int64_t row = static_cast<int64_t>(mb) * (2 * kBM) + rank * kBM + lane_grp * 32 + lane;
     const bool row_ok = row < a->T;
-    const int64_t qc0 = quarter_begin(a->tiles.V, q);
-    const int64_t qw = quarter_begin(a->tiles.V, q + 1) - qc0;
+    const int64_t qc0 = quarter_begin(a->tiles.V, a->tiles.q_first + q);
+    const int64_t qw = quarter_begin(a->tiles.V, a->tiles.q_first + q + 1) - qc0;
     const int64_t c0 = qc0 + static_cast<int64_t>(j) * kBN;
     const int valid = static_cast<int>(
         max(static_cast<int64_t>(0), min(static_cast<int64_t>(kBN), qw - int64_t(j) * kBN)));
@@ -167,7 +182,7 @@ struct GradEpilogue {
         pk[i >> 1] = *reinterpret_cast<const uint32_t*>(&b2);
       }
       const int n = min(64, valid - p * 64);
-      const int64_t col0 = c0 + p * 64;
+      const int64_t col0 = c0 + p * 64 - a->tiles.w_row0;  // column of G
       if (!LP_CHECK(row < a->T && col0 >= 0 && col0 + n <= a->ld_g, kChkGStore)) continue;
       __nv_bfloat16* grow = a->G + row * a->ld_g + col0;
       // a thread writes its row's 128 bytes: as four whole 32-byte sectors when
@@ -228,6 +243,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 struct GemmTiles {
   int n_mb, n_nb, n_split, n_kb, kb_per_split, total;
   int nb_fastest;
+  // K in segments of seg_w elements (seg_w a multiple of 16; 0: one segment,
+  // all of K), each of n_kb K blocks in seg_splits splits; split s is split
+  // s % seg_splits of segment s / seg_splits
+  int seg_w, seg_splits;
   __device__ __forceinline__ int units() const { return total; }
   __device__ __forceinline__ void decode(int u, int& mb, int& nb, int& s) const {
     if (nb_fastest) {
@@ -248,8 +267,28 @@ struct GemmTiles {
     decode(u, mb, nb, s);
     a_row = mb * (2 * kBM) + static_cast<int>(rank) * kBM;
     b_row = nb * kBN + static_cast<int>(rank) * kBNHalf;
-    kb0 = s * kb_per_split;
+    kb0 = (s % seg_splits) * kb_per_split;
     kb1 = min(n_kb, kb0 + kb_per_split);
+  }
+};
+
+// The work list with its segments' K offsets and last-block steps (the dH
+// product); the dW product (one segment, K = T) takes GemmTiles alone and
+// issues every K block whole.
+struct SegGemmTiles : GemmTiles {
+  __device__ __forceinline__ int k_offset(int u) const {
+    int mb, nb, s;
+    decode(u, mb, nb, s);
+    return (s / seg_splits) * seg_w;
+  }
+  __device__ __forceinline__ int k_steps_last(int u) const {
+    constexpr int kFull = kGemmBK / kUmmaK;
+    if (seg_w == 0) return kFull;
+    int mb, nb, s;
+    decode(u, mb, nb, s);
+    const int kb1 = min(n_kb, (s % seg_splits + 1) * kb_per_split);
+    if (kb1 < n_kb) return kFull;
+    return (seg_w - (n_kb - 1) * kGemmBK + kUmmaK - 1) / kUmmaK;
   }
 };
 
@@ -266,31 +305,55 @@ __device__ __forceinline__ float4 load_once(const float4* p) {
   return v;
 }
 
-// out[i] = sum_s part[s][i] for s = 0 .. n_split-1 in order (n_split <=
-// kSplitsDH), for i = i0, i0 + stride, ... < n4 (float4 elements: n4 = n / 4,
-// part and out 16-byte aligned); NaN when an error word of the kernels that
-// made the partials (words 0..2 of the call) is set.
-__device__ __forceinline__ void split_sum(const float4* __restrict__ part, int64_t n4, int n_split,
-                                          const uint32_t* __restrict__ err,
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+  return make_float4(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y), __fadd_rn(a.z, b.z),
+                     __fadd_rn(a.w, b.w));
+}
+
+// out[i] = the fixed-order sum of the n_seg * seg_len partials part[s][i]
+// (n_seg 1, 2 or 4; n_seg * seg_len <= kMaxSplitsDH): each segment's seg_len
+// partials (the ranges of one quarter, or of the whole vocabulary) in order,
+// then the segment sums as S0, S0 + S1 or (S0 + S1) + (S2 + S3); for i = i0,
+// i0 + stride, ... < n4 (float4 elements: n4 = n / 4, part and out 16-byte
+// aligned); NaN when an error word of the kernels that made the partials
+// (words 0..2 of the call) is set.
+__device__ __forceinline__ void split_sum(const float4* __restrict__ part, int64_t n4, int n_seg,
+                                          int seg_len, const uint32_t* __restrict__ err,
                                           float4* __restrict__ out, int64_t i0, int64_t stride) {
   const bool failed = (err[0] | err[1] | err[2]) != 0u;
+  const int n_split = n_seg * seg_len;
+  const bool shape_ok = LP_CHECK(n_split <= kMaxSplitsDH && seg_len >= 1 &&
+                                     (n_seg == 1 || n_seg == 2 || n_seg == 4),
+                                 kChkSplitIndex);
   for (int64_t i = i0; i < n4; i += stride) {
-    float4 x[kSplitsDH];
+    float4 x[kMaxSplitsDH];
 #pragma unroll
-    for (int k = 0; k < kSplitsDH; ++k)
+    for (int k = 0; k < kMaxSplitsDH; ++k)
       if (k < n_split)
-        x[k] = LP_CHECK(n_split <= kSplitsDH, kChkSplitIndex) ? load_once(part + k * n4 + i)
-                                                              : make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 s = x[0];
+        x[k] = shape_ok ? load_once(part + k * n4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    // the running segment's sum, the even segment before it, S0 + S1, S2 + S3
+    float4 cur = x[0], left = x[0], s01 = x[0], s23 = x[0];
+    int seg = 0;
+    int next_seg = seg_len;  // first partial of the next segment
 #pragma unroll
-    for (int k = 1; k < kSplitsDH; ++k) {
+    for (int k = 1; k < kMaxSplitsDH; ++k) {
       if (k < n_split) {
-        s.x = __fadd_rn(s.x, x[k].x);
-        s.y = __fadd_rn(s.y, x[k].y);
-        s.z = __fadd_rn(s.z, x[k].z);
-        s.w = __fadd_rn(s.w, x[k].w);
+        if (k == next_seg) {  // segment seg is complete
+          if ((seg & 1) == 0) left = cur;
+          else if (seg == 1) s01 = add4(left, cur);
+          else s23 = add4(left, cur);
+          ++seg;
+          next_seg += seg_len;
+          cur = x[k];
+        } else {
+          cur = add4(cur, x[k]);
+        }
       }
     }
+    float4 s;
+    if (n_seg == 1) s = cur;
+    else if (n_seg == 2) s = add4(left, cur);
+    else s = add4(s01, add4(left, cur));
     const float q = quiet_nan();
     out[i] = failed ? make_float4(q, q, q, q) : s;
   }
@@ -302,12 +365,13 @@ __device__ __forceinline__ void split_sum(const float4* __restrict__ part, int64
 struct SplitSumSide {
   const float4* part;
   int64_t n4;
-  int n_split;
+  int n_seg;
+  int seg_len;
   const uint32_t* err;
   float4* out;
   __device__ __forceinline__ void operator()(int lane) const {
     if (part == nullptr) return;
-    split_sum(part, n4, n_split, err, out, static_cast<int64_t>(blockIdx.x) * 32 + lane,
+    split_sum(part, n4, n_seg, seg_len, err, out, static_cast<int64_t>(blockIdx.x) * 32 + lane,
               static_cast<int64_t>(gridDim.x) * 32);
   }
 };
@@ -464,18 +528,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     lp_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ GemmArgs a) {
   GemmEpilogue epi{&a};
-  run_pair_pipeline<GemmRing<kAMn>, GemmTiles, GemmEpilogue, kAMn, kBMn, SplitSumSide>(
-      &tmA, &tmB, a.tiles, epi, a.err, a.withhold_first_load, a.side);
+  if constexpr (kAMn) {
+    run_pair_pipeline<GemmRing<kAMn>, GemmTiles, GemmEpilogue, kAMn, kBMn, SplitSumSide>(
+        &tmA, &tmB, a.tiles, epi, a.err, a.withhold_first_load, a.side);
+  } else {
+    const SegGemmTiles tiles{a.tiles};
+    run_pair_pipeline<GemmRing<kAMn>, SegGemmTiles, GemmEpilogue, kAMn, kBMn, SplitSumSide>(
+        &tmA, &tmB, tiles, epi, a.err, a.withhold_first_load, a.side);
+  }
   if (a.ticket != nullptr) poison_if_failed(a);
 }
 
 // ------------------------------------------------------------- plain kernels
 
 // dH's split sum on its own (when dW is not asked for).
-__global__ void lp_split_sum_kernel(const float4* __restrict__ part, int64_t n4, int n_split,
-                                    const uint32_t* __restrict__ err, float4* __restrict__ out) {
-  split_sum(part, n4, n_split, err, out, static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x,
+__global__ void lp_split_sum_kernel(const float4* __restrict__ part, int64_t n4, int n_seg,
+                                    int seg_len, const uint32_t* __restrict__ err,
+                                    float4* __restrict__ out) {
+  split_sum(part, n4, n_seg, seg_len, err, out,
+            static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x,
             static_cast<int64_t>(gridDim.x) * blockDim.x);
+}
+
+// grad_H = the shards' partial dH in the order of one GPU's quarter tree:
+// P0, P0 + P1 or (P0 + P1) + (P2 + P3) (n_shards 1, 2 or 4), float4 elements.
+struct ShardParts {
+  const float4* p[4];
+};
+__global__ void lp_merge_grad_h_kernel(ShardParts parts, int n_shards, int64_t n4,
+                                       float4* out) {  // out may be one of the parts
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 a = parts.p[0][i];
+    if (n_shards == 1) {
+      out[i] = a;
+    } else if (n_shards == 2) {
+      out[i] = add4(a, parts.p[1][i]);
+    } else {
+      out[i] = add4(add4(a, parts.p[1][i]), add4(parts.p[2][i], parts.p[3][i]));
+    }
+  }
 }
 
 struct BackwardLayout {
@@ -485,15 +577,26 @@ struct BackwardLayout {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-BackwardLayout backward_layout(int64_t T, int64_t d, int64_t V) {
+// Whether the dH product splits K by quarters (and how many partials it writes
+// at most) for a vocabulary of V_total.
+bool quarter_splits(int64_t V_total) { return V_total % 64 == 0; }
+int max_splits_dh(int64_t V_total) {
+  return quarter_splits(V_total) ? kMaxSplitsDH : kSplitsDH;
+}
+
+// V: the columns of this call (a shard's, or all V_total)
+BackwardLayout backward_layout(int64_t T, int64_t d, int64_t V, int64_t V_total) {
   BackwardLayout L;
   L.V8 = round8(V);
-  size_t o = align256(linear_workspace_bytes(T, d, V, 4));
+  // the forward's workspace (for recomputed statistics; a shard has them
+  // given), or only the header with the error words
+  size_t o = align256(V == V_total ? linear_workspace_bytes(T, d, V, 4) : kWorkspaceHeader);
   L.off_lse = o; o = align256(o + sizeof(float) * T);
   L.off_logp = o; o = align256(o + sizeof(float) * T);
   L.off_ent = o; o = align256(o + sizeof(float) * T);
   L.off_g = o; o = align256(o + 2 * static_cast<size_t>(T) * L.V8);
-  L.off_dh = o; o = align256(o + sizeof(float) * kSplitsDH * static_cast<size_t>(T) * d);
+  L.off_dh = o;
+  o = align256(o + sizeof(float) * max_splits_dh(V_total) * static_cast<size_t>(T) * d);
   L.total = o;
   return L;
 }
@@ -503,7 +606,7 @@ BackwardLayout backward_layout(int64_t T, int64_t d, int64_t V) {
 // What a product launch does besides C = A B^T: the side warps' split sum and
 // the last CTA's NaN fill (both off by default).
 struct GemmExtras {
-  SplitSumSide side{nullptr, 0, 0, nullptr, nullptr};
+  SplitSumSide side{nullptr, 0, 1, 1, nullptr, nullptr};
   uint32_t* ticket = nullptr;
   const uint32_t* err_all = nullptr;
   void* poison_out = nullptr;
@@ -511,10 +614,15 @@ struct GemmExtras {
   int withhold_first_load = 0;
 };
 
+// K is split into n_seg = K / seg_w segments of seg_w elements (seg_w == 0:
+// one segment, all of K), each into at most n_split splits of whole K blocks
+// (fewer when the segment has fewer blocks); *n_split_out = the splits of one
+// segment.  Every segment starts on a multiple of 16 elements and, for the
+// K-major A, on a 16-byte boundary.
 template <bool kAMn, bool kBMn>
 lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a, const void* B,
-                      int64_t N, int64_t ld_b, int64_t K, int n_split, void* C, int64_t ldc,
-                      int64_t split_stride, uint32_t* err, cudaStream_t stream,
+                      int64_t N, int64_t ld_b, int64_t K, int64_t seg_w, int n_split, void* C,
+                      int64_t ldc, int64_t split_stride, uint32_t* err, cudaStream_t stream,
                       int* n_split_out, bool nb_fastest, bool out_bf16 = false,
                       const GemmExtras& x = GemmExtras()) {
   static PerContextOnce attr;
@@ -533,13 +641,21 @@ lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a,
   GemmArgs g;
   g.tiles.n_mb = static_cast<int>((M + 2 * kBM - 1) / (2 * kBM));
   g.tiles.n_nb = static_cast<int>((N + kBN - 1) / kBN);
-  g.tiles.n_kb = static_cast<int>((K + R::kBK - 1) / R::kBK);
+  const int64_t n_seg = seg_w > 0 ? K / seg_w : 1;
+  if (seg_w > 0 && (seg_w % kUmmaK != 0 || n_seg * seg_w != K || seg_w >= (int64_t(1) << 30)))
+    return LP_ERR_INVALID_ARGUMENT;
+  const int64_t seg_len = seg_w > 0 ? seg_w : K;
+  g.tiles.n_kb = static_cast<int>((seg_len + R::kBK - 1) / R::kBK);
   g.tiles.kb_per_split = (g.tiles.n_kb + n_split - 1) / n_split;
-  // every split gets at least one K block (the count depends on K alone)
-  n_split = (g.tiles.n_kb + g.tiles.kb_per_split - 1) / g.tiles.kb_per_split;
+  // every split gets at least one K block (the count depends on the segment
+  // length alone)
+  const int seg_splits = (g.tiles.n_kb + g.tiles.kb_per_split - 1) / g.tiles.kb_per_split;
+  g.tiles.seg_w = static_cast<int>(seg_w);
+  g.tiles.seg_splits = seg_splits;
+  n_split = static_cast<int>(n_seg) * seg_splits;
   g.tiles.n_split = n_split;
   g.tiles.nb_fastest = nb_fastest ? 1 : 0;
-  if (n_split_out != nullptr) *n_split_out = n_split;
+  if (n_split_out != nullptr) *n_split_out = seg_splits;
   const int64_t total = int64_t(g.tiles.n_mb) * g.tiles.n_nb * n_split;
   if (total >= (int64_t(1) << 31)) return LP_ERR_INVALID_ARGUMENT;
   g.tiles.total = static_cast<int>(total);
@@ -576,10 +692,10 @@ struct SmallLayout {
   size_t off_h, off_y, off_gl, off_ge, off_lse, off_ent, off_gh, total;
 };
 
-SmallLayout small_layout(int64_t d, int64_t V) {
+SmallLayout small_layout(int64_t d, int64_t V, int64_t V_total) {
   SmallLayout L;
   const int64_t d8 = (d + 7) / 8 * 8;
-  size_t o = align256(backward_layout(kSmallRows, d, V).total);
+  size_t o = align256(backward_layout(kSmallRows, d, V, V_total).total);
   L.inner = o;
   L.off_h = o; o = align256(o + 2 * static_cast<size_t>(kSmallRows * d8));
   L.off_y = o; o = align256(o + 8 * kSmallRows);
@@ -631,19 +747,20 @@ __global__ void lp_copy_rows_kernel(const float* __restrict__ gh, int64_t n,
 
 }  // namespace
 
-size_t linear_backward_workspace_bytes(int64_t T, int64_t d, int64_t V) {
-  if (T > 0 && T < kSmallRows) return small_layout(d, V).total;
-  return backward_layout(T, d, V).total;
+size_t linear_backward_workspace_bytes(int64_t T, int64_t d, int64_t V, int64_t V_total) {
+  if (T > 0 && T < kSmallRows) return small_layout(d, V, V_total).total;
+  return backward_layout(T, d, V, V_total).total;
 }
 
 lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h, const void* W,
                                  int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
-                                 int64_t V, const TauArgs& tau, const float* saved_lse,
+                                 int64_t V, int64_t V_total, int q_first, int n_q,
+                                 const TauArgs& tau, const float* saved_lse,
                                  const float* saved_entropy, const float* g_logp,
                                  const float* g_ent, float* grad_h, void* grad_w,
                                  bool grad_w_bf16, void* workspace, cudaStream_t stream) {
   if (T > 0 && T < kSmallRows) {
-    const SmallLayout S = small_layout(d, V);
+    const SmallLayout S = small_layout(d, V, V_total);
     uint8_t* base = static_cast<uint8_t*>(workspace);
     const int64_t d8 = (d + 7) / 8 * 8;
     uint4* h16 = reinterpret_cast<uint4*>(base + S.off_h);
@@ -659,8 +776,9 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
                                        ge16, lse16, ent16);
     if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
     const lp_status st =
-        launch_linear_backward(dev, h16, d8, W, ld_w, y16, kSmallRows, d, V, tau, lse16,
-                               ent16, gl16, ge16, gh16, grad_w, grad_w_bf16, workspace, stream);
+        launch_linear_backward(dev, h16, d8, W, ld_w, y16, kSmallRows, d, V, V_total, q_first,
+                               n_q, tau, lse16, ent16, gl16, ge16, gh16, grad_w, grad_w_bf16,
+                               workspace, stream);
     if (st != LP_OK) return st;
     lp_copy_rows_kernel<<<static_cast<unsigned>((T * d + 255) / 256), 256, 0, stream>>>(
         gh16, T * d, grad_h);
@@ -680,7 +798,9 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
       }) != cudaSuccess)
     return LP_ERR_CUDA;
 
-  const BackwardLayout L = backward_layout(T, d, V);
+  // a shard (n_q < 4) comes with the merged rows' statistics
+  if (n_q < 4 && (saved_lse == nullptr || saved_entropy == nullptr)) return LP_ERR_INVALID_ARGUMENT;
+  const BackwardLayout L = backward_layout(T, d, V, V_total);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* err = reinterpret_cast<uint32_t*>(ws);  // words 0..3, one per pipeline kernel
   const float* lse = saved_lse;
@@ -711,14 +831,16 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
     if (!encode_bf16_2d(&tmA, H, T, d, ld_h, kBM)) return LP_ERR_CUDA;
     if (!encode_bf16_2d(&tmB, W, V, d, ld_w, kBNHalf)) return LP_ERR_CUDA;
     GradArgs g;
-    g.tiles.V = V;
+    g.tiles.V = V_total;
+    g.tiles.w_row0 = quarter_begin(V_total, q_first);
+    g.tiles.q_first = q_first;
     g.tiles.n_mb = static_cast<int>((T + 2 * kBM - 1) / (2 * kBM));
     const bool single = T <= kBM;
     const bool wide = g.tiles.n_mb > 1;
     const int bk = wide ? WideRing::kBK : single ? SingleRing::kBK : NarrowRing::kBK;
     g.tiles.n_kb = static_cast<int>((d + bk - 1) / bk);
-    g.tiles.n_tiles_q = static_cast<int>(tiles_per_quarter(V));
-    const int64_t total = int64_t(g.tiles.n_mb) * 4 * g.tiles.n_tiles_q;
+    g.tiles.n_tiles_q = static_cast<int>(tiles_per_quarter(V_total));
+    const int64_t total = int64_t(g.tiles.n_mb) * n_q * g.tiles.n_tiles_q;
     if (total >= (int64_t(1) << 31)) return LP_ERR_INVALID_ARGUMENT;
     g.tiles.total = static_cast<int>(total);
     g.targets = targets;
@@ -742,18 +864,24 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
     if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
   }
 
-  // 3. dH = G W (W read N-major) over 19 fixed vocabulary ranges, summed in order
-  int n_split = kSplitsDH;
+  // 3. dH = G W (W read N-major) over fixed vocabulary ranges: per quarter
+  // when the quarters start on 16-column boundaries (a shard's quarters are
+  // then the subtree of one GPU's order), else over the whole vocabulary
+  const bool by_quarter = quarter_splits(V_total);
+  const int64_t seg_w = by_quarter ? V_total / 4 : 0;
+  const int n_seg = by_quarter ? n_q : 1;
+  int seg_splits = 0;
   // row blocks fastest: the pairs of one W range run together
-  st = launch_gemm<false, true>(dev, G, T, L.V8, W, d, ld_w, V, kSplitsDH, dh_part, d, T * d,
-                                err + 2, stream, &n_split, false);
+  st = launch_gemm<false, true>(dev, G, T, L.V8, W, d, ld_w, V, seg_w,
+                                by_quarter ? kRangesPerQuarter : kSplitsDH, dh_part, d, T * d,
+                                err + 2, stream, &seg_splits, false);
   if (st != LP_OK) return st;
   // T * d is a multiple of 4 (d % 8 == 0); dh_part and grad_h are 16-byte aligned
-  const SplitSumSide sum{reinterpret_cast<const float4*>(dh_part), T * d / 4, n_split, err,
-                         reinterpret_cast<float4*>(grad_h)};
+  const SplitSumSide sum{reinterpret_cast<const float4*>(dh_part), T * d / 4, n_seg, seg_splits,
+                         err, reinterpret_cast<float4*>(grad_h)};
   if (grad_w == nullptr) {
-    lp_split_sum_kernel<<<dev.sm_count * 4, 256, 0, stream>>>(sum.part, sum.n4, sum.n_split, err,
-                                                              sum.out);
+    lp_split_sum_kernel<<<dev.sm_count * 4, 256, 0, stream>>>(sum.part, sum.n4, sum.n_seg,
+                                                              sum.seg_len, err, sum.out);
     return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
   }
 
@@ -767,8 +895,20 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
   x.poison_n = V * d;
   x.withhold_first_load = fault_injection() == 2 ? 1 : 0;
   // column blocks fastest: a block of G is used by 16 consecutive units
-  return launch_gemm<true, true>(dev, G, V, L.V8, H, d, ld_h, T, 1, grad_w, d, 0, err + 3, stream,
-                                 nullptr, true, grad_w_bf16, x);
+  return launch_gemm<true, true>(dev, G, V, L.V8, H, d, ld_h, T, 0, 1, grad_w, d, 0, err + 3,
+                                 stream, nullptr, true, grad_w_bf16, x);
+}
+
+lp_status launch_merge_grad_h(const Device& dev, const float* const* shard_grad_h, int n_shards,
+                              int64_t n, float* grad_h, cudaStream_t stream) {
+  ShardParts parts{};
+  for (int i = 0; i < 4; ++i)
+    parts.p[i] = reinterpret_cast<const float4*>(shard_grad_h[i < n_shards ? i : 0]);
+  const int64_t n4 = n / 4;
+  const int64_t blocks = std::min<int64_t>((n4 + 255) / 256, int64_t(dev.sm_count) * 8);
+  lp_merge_grad_h_kernel<<<static_cast<unsigned>(std::max<int64_t>(blocks, 1)), 256, 0, stream>>>(
+      parts, n_shards, n4, reinterpret_cast<float4*>(grad_h));
+  return cudaGetLastError() == cudaSuccess ? LP_OK : LP_ERR_CUDA;
 }
 
 cudaError_t take_check_word_backward(uint32_t* out) { return take_check_word(out); }

@@ -125,14 +125,22 @@ lp_status launch_linear_stats(const Device& dev, const void* H, int64_t ld_h, co
                               float* entropy, float* partials_out, float* lse,
                               void* workspace, cudaStream_t stream);
 
-// backward of the fused path
-size_t linear_backward_workspace_bytes(int64_t T, int64_t d, int64_t V);
+// backward of the fused path over the quarters [q_first, q_first + n_q) of a
+// vocabulary of V_total (V = their columns = W's rows; all four: the whole
+// vocabulary); a shard's grad_h is its partial dH (the subtree sum of its
+// quarters), merged by launch_merge_grad_h
+size_t linear_backward_workspace_bytes(int64_t T, int64_t d, int64_t V, int64_t V_total);
 lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h, const void* W,
                                  int64_t ld_w, const int64_t* targets, int64_t T, int64_t d,
-                                 int64_t V, const TauArgs& tau, const float* saved_lse,
+                                 int64_t V, int64_t V_total, int q_first, int n_q,
+                                 const TauArgs& tau, const float* saved_lse,
                                  const float* saved_entropy, const float* g_logp,
                                  const float* g_ent, float* grad_h, void* grad_w,
                                  bool grad_w_bf16, void* workspace, cudaStream_t stream);
+// grad_h [n] = the n_shards (1, 2, 4) partial dH in the quarter tree's order
+// (n a multiple of 4, every pointer 16-byte aligned)
+lp_status launch_merge_grad_h(const Device& dev, const float* const* shard_grad_h, int n_shards,
+                              int64_t n, float* grad_h, cudaStream_t stream);
 
 // Read and clear the check word of each translation unit (lp_check.cuh).
 cudaError_t take_check_word_logits(uint32_t* out);

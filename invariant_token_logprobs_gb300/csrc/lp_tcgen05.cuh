@@ -41,6 +41,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "lp_check.cuh"
 #include "lp_internal.h"
@@ -339,6 +340,14 @@ __device__ __forceinline__ uint8_t* pipeline_smem_base() {
 //   void coords(int u, uint32_t rank, int& a_row, int& b_row, int& kb0, int& kb1) const;
 //     rows of this CTA's A and B boxes and the K blocks [kb0, kb1) of unit u
 //     (kb1 > kb0 always).
+//   Optional, for K split into segments that do not start on a K block:
+//   int k_offset(int u) const;
+//     first K element of the unit's segment (a multiple of 16): K block kb
+//     covers K elements k_offset + kb * BK ..;
+//   int k_steps_last(int u) const;
+//     MMA steps (16 K each, 1 .. BK / 16) of the unit's last K block: the
+//     steps past the segment's end are not issued, so the elements loaded
+//     there (the next segment's) add nothing.
 // Epi (one per epilogue thread):
 //   void consume(int u, uint32_t taddr, uint32_t rank, int lane_grp, int lane);
 //     read the finished 128 x 256 accumulator (this thread's lane at taddr,
@@ -368,6 +377,14 @@ struct NoSide {
   __device__ __forceinline__ void operator()(int) const {}
 };
 
+// Whether a Sched has the optional segment members (k_offset, k_steps_last).
+template <class S, class = void>
+struct HasKSegments : std::false_type {};
+template <class S>
+struct HasKSegments<S, std::void_t<decltype(std::declval<const S&>().k_offset(0)),
+                                   decltype(std::declval<const S&>().k_steps_last(0))>>
+    : std::true_type {};
+
 template <class R, class Sched, class Epi, bool kAMn = false, bool kBMn = false,
           class Side = NoSide>
 __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const CUtensorMap* tmB,
@@ -383,6 +400,9 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
   constexpr int kNumBars = R::kNumBars;
   constexpr bool kPair = R::kPair;
   static_assert(kPair || (!kAMn && !kBMn), "a lone CTA takes K-major operands only");
+  // the MMA issuer steps descriptors by address / 16 within 14 bits: every
+  // shared address of the ring (all of a CTA's shared memory) is below 2^18
+  static_assert(232448 < (1 << 18), "shared memory per CTA below 2^18 bytes");
   uint8_t* smem = pipeline_smem_base();
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
@@ -454,7 +474,10 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
       for (int u = pair; ok && u < units; u += n_pairs) {
         int a_row, b_row, kb0, kb1;
         sch.coords(u, rank, a_row, b_row, kb0, kb1);
+        int k_off = 0;
+        if constexpr (HasKSegments<Sched>::value) k_off = sch.k_offset(u);
         for (int kb = kb0; kb < kb1; ++kb) {
+          const int k0 = k_off + kb * kBK;  // first K element of the block
           if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, err, kErrLoader)) {
             ok = false;
             break;
@@ -470,36 +493,36 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
           // withheld (the stage's bounded waits then give up: no fault)
           const bool withheld = (withhold_first_load != 0 && pair == 0 && rank == 0 &&
                                  u == pair && kb == kb0) ||
-                                !LP_CHECK(a_row >= 0 && b_row >= 0 && kb >= 0, kChkTmaCoord);
+                                !LP_CHECK(a_row >= 0 && b_row >= 0 && k0 >= 0, kChkTmaCoord);
           if (!withheld && !kPair) {
             // a lone CTA: its 128 rows of A and all 256 rows of the B tile (two
             // 128-row boxes per 64 of K), counted on its own barrier
 #pragma unroll
             for (int i = 0; i < kAtoms; ++i) {
-              tma_load_2d_local(sa + i * (kABytes / kAtoms), tmA, kb * kBK + i * kAtomK, a_row,
+              tma_load_2d_local(sa + i * (kABytes / kAtoms), tmA, k0 + i * kAtomK, a_row,
                                 leader_full);
 #pragma unroll
               for (int h = 0; h < 2; ++h)
                 tma_load_2d_local(sa + kABytes + i * (kBBytes / kAtoms) + h * (kBBytes / kAtoms / 2),
-                                  tmB, kb * kBK + i * kAtomK, b_row + h * kBNHalf, leader_full);
+                                  tmB, k0 + i * kAtomK, b_row + h * kBNHalf, leader_full);
             }
           } else if (!withheld) {
             if (kAMn) {
-              tma_load_2d(sa, tmA, a_row, kb * kBK, leader_full);
-              tma_load_2d(sa + kABytes / 2, tmA, a_row + 64, kb * kBK, leader_full);
+              tma_load_2d(sa, tmA, a_row, k0, leader_full);
+              tma_load_2d(sa + kABytes / 2, tmA, a_row + 64, k0, leader_full);
             } else {
 #pragma unroll
               for (int i = 0; i < kAtoms; ++i)
-                tma_load_2d(sa + i * (kABytes / kAtoms), tmA, kb * kBK + i * kAtomK, a_row,
+                tma_load_2d(sa + i * (kABytes / kAtoms), tmA, k0 + i * kAtomK, a_row,
                             leader_full);
             }
             if (kBMn) {
-              tma_load_2d(sa + kABytes, tmB, b_row, kb * kBK, leader_full);
-              tma_load_2d(sa + kABytes + kBBytes / 2, tmB, b_row + 64, kb * kBK, leader_full);
+              tma_load_2d(sa + kABytes, tmB, b_row, k0, leader_full);
+              tma_load_2d(sa + kABytes + kBBytes / 2, tmB, b_row + 64, k0, leader_full);
             } else {
 #pragma unroll
               for (int i = 0; i < kAtoms; ++i)
-                tma_load_2d(sa + kABytes + i * (kBBytes / kAtoms), tmB, kb * kBK + i * kAtomK,
+                tma_load_2d(sa + kABytes + i * (kBBytes / kAtoms), tmB, k0 + i * kAtomK,
                             b_row, leader_full);
             }
           }
@@ -532,7 +555,10 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+          int last_steps = kBK / kUmmaK;
+          if constexpr (HasKSegments<Sched>::value) last_steps = sch.k_steps_last(u);
           for (int kb = kb0; kb < kb1; ++kb) {
+            const int n_steps = kb == kb1 - 1 ? last_steps : kBK / kUmmaK;
             if (!wait_bar(full_bar(stage), phase, abort_flag, err, kErrMma)) {
               ok = false;
               break;
@@ -540,21 +566,43 @@ __device__ __forceinline__ void run_pair_pipeline(const CUtensorMap* tmA, const 
             tc_fence_after();
             const uint32_t sa = smem_u32(smem + stage * kStageBytes);
             const uint32_t sb = sa + kABytes;
-#pragma unroll
-            for (int k = 0; k < kBK / kUmmaK; ++k) {
-              // K-major: box k / 4 of the stage, 32 bytes per step within it
+            // The descriptors of the stage's first step; a later step's differ
+            // only in the start address field (address / 16, bits 0-13), and
+            // shared addresses stay below 2^18, so adding the step's offset / 16
+            // gives exactly the step's descriptor (no carry out of the field)
+            // with one add instead of rebuilding it.
+            const uint64_t da = kAMn ? sw128_mn_desc(sa, R::kMnBoxBytes) : sw128_desc(sa);
+            const uint64_t db = kBMn ? sw128_mn_desc(sb, R::kMnBoxBytes) : sw128_desc(sb);
+            // one MMA step (16 K) of the stage
+            auto issue = [&](int k) {
+              // K-major: box k / 4 of the stage, 32 bytes per step within it;
+              // M- or N-major: 8 K rows of 128 bytes per step
               constexpr int kSteps = kAtomK / kUmmaK;
-              const uint64_t ad = kAMn ? sw128_mn_desc(sa + k * 2048, R::kMnBoxBytes)
-                                       : sw128_desc(sa + (k / kSteps) * (kABytes / kAtoms) +
-                                                    (k % kSteps) * kUmmaK * 2);
-              const uint64_t bd = kBMn ? sw128_mn_desc(sb + k * 2048, R::kMnBoxBytes)
-                                       : sw128_desc(sb + (k / kSteps) * (kBBytes / kAtoms) +
-                                                    (k % kSteps) * kUmmaK * 2);
+              const uint32_t offA = kAMn ? k * 2048
+                                         : (k / kSteps) * (kABytes / kAtoms) +
+                                               (k % kSteps) * kUmmaK * 2;
+              const uint32_t offB = kBMn ? k * 2048
+                                         : (k / kSteps) * (kBBytes / kAtoms) +
+                                               (k % kSteps) * kUmmaK * 2;
+              const uint64_t ad = da + (offA >> 4);
+              const uint64_t bd = db + (offB >> 4);
               if constexpr (kPair)
                 tc_mma(d_tmem, ad, bd, (kb != kb0 || k != 0) ? 1u : 0u, idesc(kAMn, kBMn));
               else
                 tc_mma_single(d_tmem, ad, bd, (kb != kb0 || k != 0) ? 1u : 0u,
                               idesc(false, false, kBM));
+            };
+            // whole blocks through the unrolled steps (the issuing thread's
+            // instruction count per MMA matters: a loop that can exit early
+            // cost the products several percent); a segment's last block
+            // issues only its steps
+            if (n_steps == kBK / kUmmaK) {
+#pragma unroll
+              for (int k = 0; k < kBK / kUmmaK; ++k) issue(k);
+            } else {
+#pragma unroll
+              for (int k = 0; k < kBK / kUmmaK; ++k)
+                if (k < n_steps) issue(k);
             }
             // frees the stage (in both CTAs of a pair)
             if constexpr (kPair) tc_commit_pair(empty_bar(stage));

@@ -50,6 +50,11 @@ __all__ = [
     "lp_linear_logprob_lse",
     "lp_linear_logprob_backward",
     "lp_linear_logprob_backward_ex",
+    "lp_linear_logprob_partials_backward_workspace_size",
+    "lp_linear_logprob_partials_backward",
+    "lp_merge_grad_h_partials",
+    "linear_logprob_partials_backward",
+    "merge_grad_h_partials",
     "GRAD_W_FLOAT32",
     "GRAD_W_BFLOAT16",
     "linear_logprob_lse",
@@ -136,6 +141,11 @@ _SIGNATURES = {
     "lp_linear_logprob_backward_ex": (
         _int, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, ctypes.c_float, _vp, _vp, _vp, _vp,
                _vp, _vp, _int, _vp, _sz, _vp]),
+    "lp_linear_logprob_partials_backward_workspace_size": (_sz, [_i64, _i64, _i64, _int]),
+    "lp_linear_logprob_partials_backward": (
+        _int, [_vp, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _int, _int, ctypes.c_float, _vp, _vp,
+               _vp, _vp, _vp, _vp, _int, _vp, _sz, _vp]),
+    "lp_merge_grad_h_partials": (_int, [ctypes.POINTER(_vp), _int, _i64, _i64, _vp, _vp]),
     "lp_get_device_error": (_int, [_vp, _sz, ctypes.POINTER(ctypes.c_uint32), _vp]),
     "lp_set_persistent_grid_limit": (_int, [_int]),
     "lp_set_kernel_timing_events": (_int, [_vp, _vp]),
@@ -417,6 +427,72 @@ def lp_linear_logprob_backward_ex(H, W, targets, temperature, saved_lse, saved_e
         float(temperature), _ptr(saved_lse), _ptr(saved_entropy), _ptr(grad_logp),
         _ptr(grad_entropy), _ptr(grad_H), _ptr(grad_W), dtype, _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def _grad_w_dtype_code(grad_W) -> int:
+    if grad_W is None or grad_W.dtype == torch.float32:
+        return GRAD_W_FLOAT32
+    if grad_W.dtype == torch.bfloat16:
+        return GRAD_W_BFLOAT16
+    raise TypeError("grad_W must be float32 or bfloat16")
+
+
+def lp_linear_logprob_partials_backward_workspace_size(T: int, d: int, vocab_total: int,
+                                                       n_shards: int) -> int:
+    return int(load().lp_linear_logprob_partials_backward_workspace_size(T, d, vocab_total,
+                                                                         n_shards))
+
+
+def lp_linear_logprob_partials_backward(H, W_shard, targets, vocab_total, shard_index, n_shards,
+                                        temperature, saved_lse, saved_entropy, grad_logp,
+                                        grad_entropy, grad_H_partial, grad_W_shard, workspace,
+                                        stream=None) -> None:
+    """The shard's backward (grad_W_shard float32 or bfloat16, from its dtype, or None)."""
+    _check_bf16(H, W_shard, targets)
+    T, d = H.shape
+    _check("lp_linear_logprob_partials_backward", load().lp_linear_logprob_partials_backward(
+        _ptr(H), _row_stride(H), _ptr(W_shard), _row_stride(W_shard), _ptr(targets), T, d,
+        vocab_total, shard_index, n_shards, float(temperature), _ptr(saved_lse),
+        _ptr(saved_entropy), _ptr(grad_logp), _ptr(grad_entropy), _ptr(grad_H_partial),
+        _ptr(grad_W_shard), _grad_w_dtype_code(grad_W_shard), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def lp_merge_grad_h_partials(shard_grad_h: Sequence[torch.Tensor], grad_H, stream=None) -> None:
+    T, d = grad_H.shape
+    for p in shard_grad_h:
+        if p.dtype != torch.float32 or tuple(p.shape) != (T, d) or not p.is_contiguous():
+            raise ValueError("partials must be contiguous float32 [T, d]")
+    arr = (_vp * len(shard_grad_h))(*[p.data_ptr() for p in shard_grad_h])
+    _check("lp_merge_grad_h_partials", load().lp_merge_grad_h_partials(
+        arr, len(shard_grad_h), T, d, _ptr(grad_H), _stream(stream)))
+
+
+def linear_logprob_partials_backward(H, W_shard, y, vocab_total, shard_index, n_shards,
+                                     saved_lse, saved_entropy, grad_logp=None, grad_entropy=None,
+                                     temperature: float = 1.0, with_grad_W: bool = True,
+                                     grad_W_dtype=torch.float32, workspace=None, stream=None):
+    """(grad_H partial [T, d] fp32, grad_W_shard [rows of W_shard, d] or None) of one
+    vocabulary shard, from the merged rows' log Z and entropy."""
+    T, d = H.shape
+    if workspace is None:
+        workspace = _workspace(
+            lp_linear_logprob_partials_backward_workspace_size(T, d, vocab_total, n_shards),
+            H.device)
+    gH = torch.empty((T, d), dtype=torch.float32, device=H.device)
+    gW = (torch.empty((W_shard.shape[0], d), dtype=grad_W_dtype, device=H.device)
+          if with_grad_W else None)
+    lp_linear_logprob_partials_backward(H, W_shard, y, vocab_total, shard_index, n_shards,
+                                        temperature, saved_lse, saved_entropy, grad_logp,
+                                        grad_entropy, gH, gW, workspace, stream)
+    return gH, gW
+
+
+def merge_grad_h_partials(shard_grad_h: Sequence[torch.Tensor], stream=None) -> torch.Tensor:
+    """grad_H [T, d] fp32 from the shards' partials, in shard order."""
+    out = torch.empty_like(shard_grad_h[0])
+    lp_merge_grad_h_partials(shard_grad_h, out, stream)
+    return out
 
 
 def linear_logprob_lse(H, W, y, temperature: float = 1.0, workspace=None, stream=None):

@@ -29,6 +29,19 @@ depends only on its own logit and its row's log Z and entropy, so each rank
 takes the gradient of its own columns (lp_logprob_partials_from_logits_backward)
 and holds exactly those columns of the single-GPU gradient, with no exchange.
 
+Training on the fused path (vocab_parallel_linear_logprob_lse, then
+vocab_parallel_linear_logprob_backward) has one exchange in the backward: each
+rank's grad_W rows are G_shard^T H, the rows of the single-GPU grad_W, but
+grad_H = G W sums over the whole vocabulary.  liblp sums grad_H over fixed
+vocabulary ranges inside each quarter and then adds the quarter sums as
+(Q0 + Q1) + (Q2 + Q3), so a rank's partial grad_H
+(lp_linear_logprob_partials_backward) is one subtree of that order; the
+partials are all-gathered in rank order (4 T d bytes per rank, byte movement
+again) and every rank adds them in the same tree (lp_merge_grad_h_partials).
+grad_H is then the single-GPU bits on every rank: an all-reduce, whose order
+depends on the collective, would not give that.  This needs V % 64 == 0 (the
+quarters start on 16-column boundaries).
+
 Collective backends: NCCL gathers the device buffers directly; any other
 backend (gloo) gathers host copies, staged through pinned memory.  All compute
 runs in liblp's kernels; this module only moves the states.
@@ -48,7 +61,11 @@ __all__ = [
     "shard_of_rank",
     "gather_partials",
     "vocab_parallel_linear_logprob",
+    "vocab_parallel_linear_logprob_lse",
+    "vocab_parallel_linear_logprob_backward",
     "vocab_parallel_logprob_from_logits",
+    "vocab_parallel_logprob_from_logits_lse",
+    "vocab_parallel_logprob_from_logits_backward",
 ]
 
 
@@ -103,13 +120,57 @@ def vocab_parallel_linear_logprob(H: torch.Tensor, W_shard: torch.Tensor, y: tor
     across the ranks of `group`; every rank passes the same H and y and its own
     W_shard = W[begin:end] (see shard_of_rank)."""
     rank, n, b, e = shard_of_rank(vocab_total, group)
-    if W_shard.shape[0] != e - b:
-        raise ValueError(f"rank {rank} holds {W_shard.shape[0]} rows of W, its shard has {e - b}")
+    _check_w_shard(W_shard, rank, b, e)
     with _on(stream):
         parts = lp.linear_logprob_partials(H, W_shard, y, vocab_total, rank, n,
                                            workspace=workspace, temperature=temperature)
         gathered = gather_partials(parts, group)
         return lp.merge_partials(gathered, with_entropy=with_entropy)
+
+
+def _check_w_shard(W_shard, rank, b, e):
+    if W_shard.shape[0] != e - b:
+        raise ValueError(f"rank {rank} holds {W_shard.shape[0]} rows of W, its shard has {e - b}")
+
+
+def vocab_parallel_linear_logprob_lse(H: torch.Tensor, W_shard: torch.Tensor, y: torch.Tensor,
+                                      vocab_total: int, group=None, temperature: float = 1.0,
+                                      workspace=None, stream=None):
+    """(logp, entropy, lse) [T] of softmax(H W^T / tau), W split by rows: the
+    forward of vocabulary-parallel training on the fused path; every rank gets
+    the same bits (those of lp_linear_logprob_lse on one GPU)."""
+    rank, n, b, e = shard_of_rank(vocab_total, group)
+    _check_w_shard(W_shard, rank, b, e)
+    T = H.shape[0]
+    with _on(stream):
+        parts = lp.linear_logprob_partials(H, W_shard, y, vocab_total, rank, n,
+                                           workspace=workspace, temperature=temperature)
+        gathered = gather_partials(parts, group)
+        out = [torch.empty(T, dtype=torch.float32, device=H.device) for _ in range(3)]
+        lp.lp_merge_partials_lse(gathered, T, out[0], out[1], out[2])
+        return tuple(out)
+
+
+def vocab_parallel_linear_logprob_backward(H: torch.Tensor, W_shard: torch.Tensor,
+                                           y: torch.Tensor, vocab_total: int,
+                                           saved_lse: torch.Tensor, saved_entropy: torch.Tensor,
+                                           grad_logp=None, grad_entropy=None, group=None,
+                                           temperature: float = 1.0, with_grad_W: bool = True,
+                                           grad_W_dtype=torch.float32, workspace=None,
+                                           stream=None):
+    """(grad_H [T, d] fp32, grad_W_shard [end - begin, d] or None) from the merged
+    rows' log Z and entropy (vocab_parallel_linear_logprob_lse): grad_H is the
+    same on every rank and equal to the single-GPU result bit for bit, and
+    grad_W_shard is rows begin..end of the single-GPU grad_W."""
+    rank, n, b, e = shard_of_rank(vocab_total, group)
+    _check_w_shard(W_shard, rank, b, e)
+    with _on(stream):
+        part, gW = lp.linear_logprob_partials_backward(
+            H, W_shard, y, vocab_total, rank, n, saved_lse, saved_entropy, grad_logp,
+            grad_entropy, temperature=temperature, with_grad_W=with_grad_W,
+            grad_W_dtype=grad_W_dtype, workspace=workspace)
+        gathered = gather_partials(part, group)
+        return lp.merge_grad_h_partials(gathered), gW
 
 
 def vocab_parallel_logprob_from_logits(z_shard: torch.Tensor, y: torch.Tensor, vocab_total: int,

@@ -87,5 +87,23 @@ def run_cases(lp, synth) -> dict:
         _, ent, lse = lp.linear_logprob_lse(f.H, f.W, f.y, temperature=0.8)
         keep(f"bwd{T}.saved", *lp.linear_logprob_backward(f.H, f.W, f.y, gl, None, temperature=0.8,
                                                           saved_lse=lse, saved_entropy=ent))
+    # vocabulary-parallel backward: every shard's partial grad_H and grad_W rows, the
+    # merge (V % 64 == 0: quarter-ordered grad_H), and the padded small batch
+    for T, d, V in [(64, 256, 8192), (5, 64, 4096 + 64), (300, 128, 20480)]:
+        f = synth.fused_inputs("fused_tiny", device=DEV, T=T, d=d, V=V, seed=T + 5)
+        g = torch.Generator(device=DEV)
+        g.manual_seed(T + 1)
+        gl = torch.randn(T, generator=g, device=DEV)
+        ge = torch.randn(T, generator=g, device=DEV)
+        _, ent, lse = lp.linear_logprob_lse(f.H, f.W, f.y)
+        for n in (1, 2, 4):
+            parts = []
+            for i in range(n):
+                b, e = lp.vocab_shard_range(V, i, n)
+                ph, pw = lp.linear_logprob_partials_backward(f.H, f.W[b:e], f.y, V, i, n, lse, ent,
+                                                             gl, ge)
+                keep(f"bwd{T}.shard{n}.{i}", ph, pw)
+                parts.append(ph)
+            keep(f"bwd{T}.shard{n}.merged", lp.merge_grad_h_partials(parts))
     torch.cuda.synchronize()
     return out

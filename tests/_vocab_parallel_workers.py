@@ -70,6 +70,24 @@ def gpu_vocab_parallel(rank: int, world: int, init_file: str, out_dir: str, path
             _, n, b, e = vp.shard_of_rank(V)
             logp, ent = vp.vocab_parallel_logprob_from_logits(x.z[:, b:e], x.y, V,
                                                               temperature=0.7)
+        elif path == "fused_train":
+            # forward with log Z over the shards, then this rank's backward: its grad_W
+            # rows, its partial grad_H, the all-gather and the merge of the partials
+            x = synth.fused_inputs("fused_qwen3_8b", device="cuda:0")
+            T, V = x.H.shape[0], x.W.shape[0]
+            _, n, b, e = vp.shard_of_rank(V)
+            w_shard = x.W[b:e].contiguous()
+            del x.W
+            gl, ge = upstream(T)
+            logp, ent, lse = vp.vocab_parallel_linear_logprob_lse(x.H, w_shard, x.y, V,
+                                                                  temperature=0.9)
+            gH, gW = vp.vocab_parallel_linear_logprob_backward(x.H, w_shard, x.y, V, lse, ent,
+                                                               gl, ge, temperature=0.9)
+            torch.cuda.synchronize()
+            torch.save({"logp": logp.cpu(), "ent": ent.cpu(), "lse": lse.cpu(),
+                        "grad_h_sha": sha256_of(gH), "grad_w_sha": sha256_of(gW)},
+                       os.path.join(out_dir, f"rank{rank}.pt"))
+            return
         else:  # logits_train: forward with log Z, then this rank's columns of dL/dz
             x = synth.logits_inputs("logits_peaked", device="cuda:0")
             T, V = x.z.shape

@@ -22,7 +22,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     names = lp.declared_symbols()
-    assert len(names) == 28
+    assert len(names) == 31
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(lp._SIGNATURES)
@@ -147,6 +147,68 @@ def test_backward_argument_errors(lib):
     assert lp.lp_linear_logprob_backward_workspace_size(-1, 8, 8) == 0
 
 
+def _backward_ws(T, d, V, V_total):
+    # header + quarter states, log Z / logp / entropy, bf16 G [T, round8(V)], and the
+    # partial grad_H: 28 of them when V_total % 64 == 0 (7 per quarter), else 19
+    a = lambda x: -(-x // 256) * 256
+    tiles = -(-((V_total + 3) // 4) // 256)
+    # a shard has its statistics given: no forward workspace, only the header
+    o = a(256 + 4 * tiles * T * 16 if V == V_total else 256) + 3 * a(4 * T)
+    o += a(2 * T * (-(-V // 8) * 8))
+    return o + a(4 * (28 if V_total % 64 == 0 else 19) * T * d)
+
+
+def test_backward_workspace_layout(lib):
+    assert lp.lp_linear_logprob_backward_workspace_size(64, 256, 8192) == _backward_ws(64, 256, 8192, 8192)
+    assert lp.lp_linear_logprob_backward_workspace_size(64, 256, 8200) == _backward_ws(64, 256, 8200, 8200)
+    for n in (1, 2, 4):
+        assert lp.lp_linear_logprob_partials_backward_workspace_size(512, 4096, 151936, n) == \
+            _backward_ws(512, 4096, 151936 // n, 151936)
+    # one shard: the whole vocabulary, any V
+    assert lp.lp_linear_logprob_partials_backward_workspace_size(64, 256, 8200, 1) == \
+        lp.lp_linear_logprob_backward_workspace_size(64, 256, 8200)
+    assert lp.lp_linear_logprob_partials_backward_workspace_size(64, 256, 8192, 3) == 0
+    assert lp.lp_linear_logprob_partials_backward_workspace_size(-1, 256, 8192, 2) == 0
+
+
+def test_shard_backward_argument_errors(lib):
+    f = lib.lp_linear_logprob_partials_backward
+    ws = lp.lp_linear_logprob_partials_backward_workspace_size(64, 256, 8192, 2)
+    #       H  ldh  W  ldw y  T   d    Vtot  i  n  tau  lse ent gl ge gH gW dt ws  wsb stream
+    base = [A, 256, A, 256, A, 64, 256, 8192, 1, 2, 1.0, A, A, A, A, A, A, 0, A, ws, None]
+
+    def call(**kw):
+        idx = dict(H=0, T=5, V=7, i=8, n=9, tau=10, lse=11, ent=12, gl=13, ge=14, gH=15, gW=16,
+                   dt=17, ws=18, wsb=19)
+        a = list(base)
+        for k, v in kw.items():
+            a[idx[k]] = v
+        return f(*a)
+
+    assert call(T=0) == OK
+    assert call(i=2) == INVALID                     # shard index
+    assert call(n=3) == INVALID                     # shard count
+    assert call(V=8200) == INVALID                  # quarters not on 16-column boundaries
+    assert call(lse=None) == INVALID                # a shard needs the merged statistics
+    assert call(ent=None) == INVALID
+    assert call(gl=None, ge=None) == INVALID        # no upstream gradient
+    assert call(dt=2) == INVALID                    # grad_W dtype
+    assert call(tau=0.0) == INVALID
+    assert call(gH=None) == INVALID
+    assert call(gH=A + 8) == MISALIGNED
+    assert call(wsb=ws - 1) == WS_SMALL
+    g = lib.lp_merge_grad_h_partials
+    arr = (ctypes.c_void_p * 4)(A, A, A, A)
+    assert g(arr, 3, 8, 256, A, None) == INVALID
+    assert g(arr, 4, 0, 256, A, None) == OK
+    assert g(arr, 4, 8, 252, A, None) == MISALIGNED  # d % 8
+    bad = (ctypes.c_void_p * 2)(A, A + 8)
+    assert g(bad, 2, 8, 256, A, None) == MISALIGNED
+    none = (ctypes.c_void_p * 2)(A, None)
+    assert g(none, 2, 8, 256, A, None) == INVALID
+    assert g(arr, 2, 8, 256, A + 4, None) == MISALIGNED
+
+
 def test_merge_argument_errors(lib):
     f = lib.lp_merge_partials
     arr = (ctypes.c_void_p * 4)(A, A, A, A)
@@ -178,6 +240,11 @@ def test_valid_call_without_gb300_fails_loudly(lib):
     assert lib.lp_logprob_partials_from_logits_backward(A, 100, A, 4, 200, 2, 2, ctypes.c_float(1.0),
                                                         A, A, A, None, A + (1 << 16), 100,
                                                         None) == INVALID
+    wsb = lp.lp_linear_logprob_partials_backward_workspace_size(64, 256, 8200, 1)
+    assert lib.lp_linear_logprob_partials_backward(A, 256, A, 256, A, 64, 256, 8200, 0, 1,
+                                                   ctypes.c_float(1.0), A, A, A, None, A, A, 0,
+                                                   A, wsb, None) == UNSUPPORTED
+    assert lib.lp_merge_grad_h_partials(arr, 1, 8, 256, A, None) == UNSUPPORTED
     assert lib.lp_set_persistent_grid_limit(-1) == INVALID
     assert lib.lp_set_persistent_grid_limit(0) == OK
     assert lib.lp_set_fault_injection(3) == INVALID

@@ -7,8 +7,9 @@ it to bf16 before two tensor-core products with fp32 accumulation.  bf16 keeps
 (the unit roundoff of an 8-bit significand); a product term G[t,v] X[.,k] then
 carries at most 2^-8 |G X| of error.  The products add at most about
 n 2^-24 sum |terms| for n terms summed in one fp32 chain: grad_H = G W sums
-V terms in 19 fixed ranges (n = V/19 + 19), grad_W = G^T H sums T terms
-(n = T).  So the tests allow (2^-8 + n 2^-24) sum |G X| + 1e-6 per element,
+V terms in 19 fixed ranges (n = V/19 + 19), or, when V % 64 == 0, in 7 ranges
+per quarter added in order and then as (Q0 + Q1) + (Q2 + Q3) (n = V/28 + 9,
+below V/19 + 19); grad_W = G^T H sums T terms (n = T).  So the tests allow (2^-8 + n 2^-24) sum |G X| + 1e-6 per element,
 the sums taken in fp64 from the oracle's G.  These are absolute-sum bounds:
 they hold also where the terms cancel (the entropy-only gradient, whose rows
 of G sum to zero).  A bf16 grad_W must be the fp32 grad_W of the same call

@@ -6,10 +6,13 @@ another: each rank's partials kernel finishes before its states are
 exchanged on the host).  Fused path at the Qwen3-Next head shape
 (T=16384, d=2048, V=151936, 1/2 or 1/4 of W per rank); logits path on the
 peaked 1024 x 151936 logits at temperature 0.7, forward only and forward with
-log Z plus each rank's columns of dL/dz.  Every rank's merged logp, entropy
-(and log Z) must equal the unsharded single-process call bit for bit (the
-prior-art report's tp4_equals_tp1), and each rank's gradient columns the same
-columns of the single-process gradient.
+log Z plus each rank's columns of dL/dz.  Fused training at the Qwen3-8B head
+(T=512, d=4096, V=151936, temperature 0.9): forward with log Z, then each
+rank's grad_W rows and partial grad_H, all-gathered and merged.  Every rank's
+merged logp, entropy (and log Z) must equal the unsharded single-process call
+bit for bit (the prior-art report's tp4_equals_tp1), each rank's gradient
+columns (or grad_W rows) the same part of the single-process gradient, and
+every rank's grad_H the single-process grad_H.
 """
 
 import os
@@ -48,12 +51,28 @@ def references():
             b, e = lp.vocab_shard_range(V, r, n)
             shas[(n, r)] = workers.sha256_of(grad[:, b:e])
     del z, grad
+    # fused training: forward with log Z and the single-GPU backward
+    x = synth.fused_inputs("fused_qwen3_8b", device=DEV)
+    T, V = x.H.shape[0], x.W.shape[0]
+    gl, ge = workers.upstream(T)
+    f_lp, f_ent, f_lse = lp.linear_logprob_lse(x.H, x.W, x.y, 0.9)
+    gH, gW = lp.linear_logprob_backward(x.H, x.W, x.y, gl, ge, 0.9, saved_lse=f_lse,
+                                        saved_entropy=f_ent)
+    w_shas = {}
+    for n in (2, 4):
+        for r in range(n):
+            b, e = lp.vocab_shard_range(V, r, n)
+            w_shas[(n, r)] = workers.sha256_of(gW[b:e])
+    h_sha = workers.sha256_of(gH)
+    del x, gH, gW
     torch.cuda.synchronize()
     return {"fused": [t.cpu() for t in fused], "logits": [t.cpu() for t in logits],
-            "logits_train": [t.cpu() for t in (t_lp, t_ent, t_lse)], "grad_sha": shas}
+            "logits_train": [t.cpu() for t in (t_lp, t_ent, t_lse)], "grad_sha": shas,
+            "fused_train": [t.cpu() for t in (f_lp, f_ent, f_lse)], "grad_w_sha": w_shas,
+            "grad_h_sha": h_sha}
 
 
-@pytest.mark.parametrize("path", ["fused", "logits", "logits_train"])
+@pytest.mark.parametrize("path", ["fused", "logits", "logits_train", "fused_train"])
 @pytest.mark.parametrize("world", [2, 4])
 def test_vocab_parallel_equals_single_gpu(world, path, references, tmp_path):
     ctx = mp.get_context("spawn")
@@ -73,3 +92,7 @@ def test_vocab_parallel_equals_single_gpu(world, path, references, tmp_path):
         if path == "logits_train":
             assert torch.equal(bits(got["lse"]), bits(references[path][2])), (world, r)
             assert got["grad_sha"] == references["grad_sha"][(world, r)], (world, r)
+        if path == "fused_train":
+            assert torch.equal(bits(got["lse"]), bits(references[path][2])), (world, r)
+            assert got["grad_h_sha"] == references["grad_h_sha"], (world, r)
+            assert got["grad_w_sha"] == references["grad_w_sha"][(world, r)], (world, r)
