@@ -584,6 +584,13 @@ def bench_backward(lp, torch, x, dev, stream, peaks, peaks_kind, max_over, world
     ms16 = max_over(e0.elapsed_time(e1)) / K
     tf16 = flops / (ms16 / 1e3) / 1e12
     del ws, gW16
+    # algorithmic bytes of one call: W read by the logits recompute and by G W,
+    # H once, G (bf16 [T, V]) written once and read by both products, the
+    # fp32 partial grad_H written and read (28 when V % 64 == 0, else 19),
+    # grad_H and the fp32 grad_W written once
+    n_part = 28 if V % 64 == 0 else 19
+    alg_bytes = (2 * V * d * 2 + T * d * 2 + 3 * T * V * 2 + 2 * n_part * T * d * 4
+                 + T * d * 4 + V * d * 4)
     return {"workload": "fused_qwen3_8b backward (grad_H and grad_W, fp32 out)", "T": T, "d": d,
             "V": V, "value": world * T / (ms / 1e3), "unit": "tokens/s", "us_per_call": ms * 1e3,
             "bf16_grad_W": {"us_per_call": ms16 * 1e3, "achieved_tflops": tf16,
@@ -594,7 +601,7 @@ def bench_backward(lp, torch, x, dev, stream, peaks, peaks_kind, max_over, world
                          "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],
                          "traffic": profile_traffic(BACKWARD_PROFILE_SUMMARY, BACKWARD_SOURCES,
                                                     "dram_bytes_per_call_full_size"),
-                         "algorithmic_bytes_per_call": 5.72e9,
+                         "algorithmic_bytes_per_call": float(alg_bytes),
                          "kernel": "whole backward call (3 tensor-core kernels; the split sum of grad_H runs in the grad_W product)",
                          "algorithmic_flops_per_call": flops,
                          "note": "log-sum-exp and entropy saved from the forward (lp_linear_logprob_lse); one memset + 3 kernels per call",

@@ -475,7 +475,7 @@ LP_API lp_status lp_linear_logprob_backward_ex(const void* H, int64_t ld_h, cons
  * and the ranks all-gather the partials in shard order and merge them with
  * lp_merge_grad_h_partials (P0, P0 + P1, or (P0 + P1) + (P2 + P3)): grad_H and
  * the concatenated grad_W are the bits of lp_linear_logprob_backward on one
- * GPU, for any finite W.  The exchange moves bytes only (4 T d per rank).
+ * GPU.  The exchange moves bytes only (4 T d per rank).
  *
  * lp_linear_logprob_partials_backward:
  *   H, ld_h, targets, T, d, temperature: as in lp_linear_logprob_backward;
