@@ -204,3 +204,59 @@ def test_backward_graph_replay_bytes_equal_eager(saved):
         torch.cuda.synchronize()
         assert torch.equal(bits(got_h.reshape(-1)), bits(gH.reshape(-1)))
         assert torch.equal(bits(got_w.reshape(-1)), bits(gW.reshape(-1)))
+
+
+def test_shard_backward_graph_replay_bytes_equal_eager():
+    """Two shards' backward and the merge of their partial grad_H captured once
+    on static buffers (V % 64 == 0: the quarter order); replays equal eager
+    calls and the single-GPU backward."""
+    T, d, V, n = 48, 128, 16384, 2
+    W = synth.fused_inputs("fused_tiny", device=DEV, T=1, d=d, V=V, seed=5).W
+    H = torch.empty((T, d), dtype=torch.bfloat16, device=DEV)
+    y = torch.empty(T, dtype=torch.int64, device=DEV)
+    gl = torch.empty(T, device=DEV)
+    ge = torch.empty(T, device=DEV)
+    lse = torch.empty(T, device=DEV)
+    ent = torch.empty(T, device=DEV)
+    logp = torch.empty(T, device=DEV)
+    fws = torch.empty(lp.lp_linear_logprob_workspace_size(T, d, V), dtype=torch.uint8, device=DEV)
+    wsz = lp.lp_linear_logprob_partials_backward_workspace_size(T, d, V, n)
+    ws = [torch.empty(wsz, dtype=torch.uint8, device=DEV) for _ in range(n)]
+    rng = [lp.vocab_shard_range(V, i, n) for i in range(n)]
+    parts = [torch.empty((T, d), device=DEV) for _ in range(n)]
+    rows = [torch.empty((e - b, d), device=DEV) for b, e in rng]
+    gH = torch.empty((T, d), device=DEV)
+
+    def fill(seed):
+        x = synth.fused_inputs("fused_tiny", device=DEV, T=T, d=d, V=V, seed=seed)
+        H.copy_(x.H)
+        y.copy_(x.y)
+        g = torch.Generator(device=DEV)
+        g.manual_seed(seed)
+        gl.copy_(torch.randn(T, generator=g, device=DEV))
+        ge.copy_(torch.randn(T, generator=g, device=DEV))
+        lp.lp_linear_logprob_lse(H, W, y, 1.0, logp, ent, lse, fws)
+
+    def call():
+        for i, (b, e) in enumerate(rng):
+            lp.lp_linear_logprob_partials_backward(H, W[b:e], y, V, i, n, 1.0, lse, ent, gl, ge,
+                                                   parts[i], rows[i], ws[i])
+        lp.lp_merge_grad_h_partials(parts, gH)
+
+    fill(200)
+    graph = _capture(call)
+    for seed in (201, 202):
+        fill(seed)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        got_h, got_w = gH.clone(), torch.cat(rows)
+        call()
+        torch.cuda.synchronize()
+        assert torch.equal(got_h.view(torch.int32), gH.view(torch.int32)), seed
+        assert torch.equal(got_w.view(torch.int32), torch.cat(rows).view(torch.int32)), seed
+        ref_h, ref_w = lp.linear_logprob_backward(H, W, y, gl, ge, saved_lse=lse,
+                                                  saved_entropy=ent)
+        torch.cuda.synchronize()
+        assert torch.equal(ref_h.view(torch.int32), got_h.view(torch.int32)), seed
+        assert torch.equal(ref_w.view(torch.int32), got_w.view(torch.int32)), seed
