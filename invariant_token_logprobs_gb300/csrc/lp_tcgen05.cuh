@@ -144,11 +144,10 @@ __device__ __forceinline__ uint64_t global_timer() {
   return t;
 }
 
-// Bounded wait for the phase of `bar` with parity `parity`.  Returns false when
-// the CTA is aborting or this wait gave up (then it raises the abort).
-static __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                      uint32_t* err, uint32_t role_bit) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The part of wait_bar after a first try found the phase incomplete.
+static __device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort_flag, uint32_t* err,
+                                                  uint32_t role_bit) {
   const uint64_t t0 = global_timer();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -159,6 +158,16 @@ static __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, vola
       return false;
     }
   }
+}
+
+// Bounded wait for the phase of `bar` with parity `parity`.  Returns false when
+// the CTA is aborting or this wait gave up (then it raises the abort).  The
+// first try is inline: a phase that is already complete costs no call (the
+// MMA issuer's wait per K block is on the products' critical path).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                         uint32_t* err, uint32_t role_bit) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return wait_bar_slow(bar, parity, abort_flag, err, role_bit);
 }
 
 // Bounded wait used while draining after an abort; never raises anything.
