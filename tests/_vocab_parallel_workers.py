@@ -19,7 +19,10 @@ def upstream(T: int):
 
 def sha256_of(t: torch.Tensor) -> str:
     import hashlib
-    return hashlib.sha256(t.contiguous().cpu().numpy().tobytes()).hexdigest()
+    t = t.contiguous()
+    if t.dtype == torch.bfloat16:  # numpy has no bfloat16: hash the same bytes as int16
+        t = t.view(torch.int16)
+    return hashlib.sha256(t.cpu().numpy().tobytes()).hexdigest()
 
 
 def _init(rank: int, world: int, init_file: str) -> None:
@@ -86,6 +89,23 @@ def gpu_vocab_parallel(rank: int, world: int, init_file: str, out_dir: str, path
             torch.cuda.synchronize()
             torch.save({"logp": logp.cpu(), "ent": ent.cpu(), "lse": lse.cpu(),
                         "grad_h_sha": sha256_of(gH), "grad_w_sha": sha256_of(gW)},
+                       os.path.join(out_dir, f"rank{rank}.pt"))
+            return
+        elif path == "fused_autograd":
+            # the same through torch.autograd: a loss on logp and entropy, .backward()
+            from invariant_token_logprobs_gb300 import autograd as ag
+            x = synth.fused_inputs("fused_qwen3_8b", device="cuda:0")
+            T, V = x.H.shape[0], x.W.shape[0]
+            _, n, b, e = vp.shard_of_rank(V)
+            w_shard = x.W[b:e].contiguous().requires_grad_(True)
+            del x.W
+            H = x.H.clone().requires_grad_(True)
+            gl, ge = upstream(T)
+            logp, ent = ag.vocab_parallel_linear_logprob(H, w_shard, x.y, V, temperature=0.9)
+            ((logp * gl).sum() + (ent * ge).sum()).backward()
+            torch.cuda.synchronize()
+            torch.save({"logp": logp.detach().cpu(), "ent": ent.detach().cpu(),
+                        "grad_h_sha": sha256_of(H.grad), "grad_w_sha": sha256_of(w_shard.grad)},
                        os.path.join(out_dir, f"rank{rank}.pt"))
             return
         else:  # logits_train: forward with log Z, then this rank's columns of dL/dz

@@ -60,3 +60,35 @@ def test_logits_autograd_matches_direct_calls():
     ((logp * a).sum() + (ent * b).sum()).backward()
     ref = lp.logprob_from_logits_backward(z.z, z.y, a, b, temperature=0.7)
     assert torch.equal(bits(zz.grad), bits(ref))
+
+
+def test_vocab_parallel_autograd_single_rank_matches_direct_calls():
+    """Without a process group (one rank, the whole vocabulary) the
+    vocabulary-parallel bindings give the single-GPU bindings' bits."""
+    from invariant_token_logprobs_gb300.autograd import (vocab_parallel_linear_logprob,
+                                                         vocab_parallel_logprob_from_logits)
+    lp.load()
+    x = synth.fused_inputs("fused_tiny", device=DEV, T=40, d=128, V=8192, seed=21)
+    g = torch.Generator(device=DEV).manual_seed(6)
+    a = torch.randn(40, generator=g, device=DEV)
+    b = torch.randn(40, generator=g, device=DEV)
+    outs = []
+    for fn in (lambda H, W: linear_logprob(H, W, x.y, 0.8),
+               lambda H, W: vocab_parallel_linear_logprob(H, W, x.y, 8192, None, 0.8)):
+        H = x.H.clone().requires_grad_(True)
+        W = x.W.clone().requires_grad_(True)
+        logp, ent = fn(H, W)
+        ((logp * a).sum() + (ent * b).sum()).backward()
+        outs.append((logp.detach(), ent.detach(), H.grad, W.grad))
+    for u, v in zip(*outs):
+        assert torch.equal(u.contiguous().view(torch.int16 if u.dtype == torch.bfloat16 else torch.int32),
+                           v.contiguous().view(torch.int16 if v.dtype == torch.bfloat16 else torch.int32))
+    z = synth.logits_inputs("logits_peaked", device=DEV, T=24, V=5000, seed=22)
+    grads = []
+    for fn in (lambda zz: logprob_from_logits(zz, z.y, 0.7),
+               lambda zz: vocab_parallel_logprob_from_logits(zz, z.y, 5000, None, 0.7)):
+        zz = z.z.clone().requires_grad_(True)
+        logp, ent = fn(zz)
+        ((logp * a[:24]).sum() + (ent * b[:24]).sum()).backward()
+        grads.append(zz.grad)
+    assert torch.equal(bits(grads[0]), bits(grads[1]))

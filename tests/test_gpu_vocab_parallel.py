@@ -12,7 +12,9 @@ rank's grad_W rows and partial grad_H, all-gathered and merged.  Every rank's
 merged logp, entropy (and log Z) must equal the unsharded single-process call
 bit for bit (the prior-art report's tp4_equals_tp1), each rank's gradient
 columns (or grad_W rows) the same part of the single-process gradient, and
-every rank's grad_H the single-process grad_H.
+every rank's grad_H the single-process grad_H; the same training step through
+the vocabulary-parallel autograd binding must give every rank the
+single-process autograd gradients (bf16) of H and of its rows of W.
 """
 
 import os
@@ -64,15 +66,30 @@ def references():
             b, e = lp.vocab_shard_range(V, r, n)
             w_shas[(n, r)] = workers.sha256_of(gW[b:e])
     h_sha = workers.sha256_of(gH)
-    del x, gH, gW
+    del gH, gW
+    # the same through the single-GPU autograd binding (bf16 gradients)
+    from invariant_token_logprobs_gb300 import autograd as ag
+    H = x.H.clone().requires_grad_(True)
+    Wg = x.W.clone().requires_grad_(True)
+    a_lp, a_ent = ag.linear_logprob(H, Wg, x.y, 0.9)
+    ((a_lp * gl).sum() + (a_ent * ge).sum()).backward()
+    aw_shas = {}
+    for n in (2, 4):
+        for r in range(n):
+            b, e = lp.vocab_shard_range(V, r, n)
+            aw_shas[(n, r)] = workers.sha256_of(Wg.grad[b:e])
+    ah_sha = workers.sha256_of(H.grad)
+    a_out = [a_lp.detach().cpu(), a_ent.detach().cpu()]
+    del x, H, Wg, a_lp, a_ent
     torch.cuda.synchronize()
     return {"fused": [t.cpu() for t in fused], "logits": [t.cpu() for t in logits],
             "logits_train": [t.cpu() for t in (t_lp, t_ent, t_lse)], "grad_sha": shas,
             "fused_train": [t.cpu() for t in (f_lp, f_ent, f_lse)], "grad_w_sha": w_shas,
-            "grad_h_sha": h_sha}
+            "grad_h_sha": h_sha, "fused_autograd": a_out, "ag_w_sha": aw_shas, "ag_h_sha": ah_sha}
 
 
-@pytest.mark.parametrize("path", ["fused", "logits", "logits_train", "fused_train"])
+@pytest.mark.parametrize("path", ["fused", "logits", "logits_train", "fused_train",
+                                  "fused_autograd"])
 @pytest.mark.parametrize("world", [2, 4])
 def test_vocab_parallel_equals_single_gpu(world, path, references, tmp_path):
     ctx = mp.get_context("spawn")
@@ -96,3 +113,6 @@ def test_vocab_parallel_equals_single_gpu(world, path, references, tmp_path):
             assert torch.equal(bits(got["lse"]), bits(references[path][2])), (world, r)
             assert got["grad_h_sha"] == references["grad_h_sha"], (world, r)
             assert got["grad_w_sha"] == references["grad_w_sha"][(world, r)], (world, r)
+        if path == "fused_autograd":
+            assert got["grad_h_sha"] == references["ag_h_sha"], (world, r)
+            assert got["grad_w_sha"] == references["ag_w_sha"][(world, r)], (world, r)
