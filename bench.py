@@ -388,6 +388,19 @@ def run_lp(args):
     kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in zip(k_start, k_stop))
     kernel_ms = max_over(kernel_ms)
 
+    # the repeat property of the pages' candidates (distinct results in 10
+    # repeats): ten more calls on the same inputs, each output hashed
+    torch.cuda.nvtx.range_push("lp.bench.repeats")
+    hashes = []
+    for _ in range(10):
+        lp.lp_linear_logprob(x.H, x.W, x.y, logp, ent, ws)
+        both = torch.cat([logp, ent]).cpu().view(torch.int32).numpy().tobytes()
+        hashes.append(hashlib.sha256(both).hexdigest())
+    torch.cuda.nvtx.range_pop()
+    repeats = {"calls": 10, "distinct_results": len(set(hashes)),
+               "outputs_sha256": hashes[0][:16],
+               "note": "logp and entropy of the headline inputs, hashed after each call"}
+
     flops = 2.0 * T * d * V
     w_bytes = 2.0 * V * d + 2.0 * T * d + 8.0 * T + 8.0 * T
     peak_tf = peaks["bf16_tflops"]
@@ -468,8 +481,10 @@ def run_lp(args):
         torch.cuda.synchronize()
         return max_over(e0.elapsed_time(e1))
 
+    torch.cuda.nvtx.range_push("lp.bench.e2e")
     e2e_ms = timed(pipelined, K2)
     serial_ms = timed(serial, K2)
+    torch.cuda.nvtx.range_pop()
     # the host copies (slot 1: the pipelined run, slot 0: the serial run) hold the
     # same bits as the device-resident run's outputs
     ref_lp = logp.cpu().view(torch.int32)
@@ -491,19 +506,25 @@ def run_lp(args):
     logits_item = None
     if not args.no_logits:
         del h_host
+        torch.cuda.nvtx.range_push("lp.bench.logits")
         logits_item = bench_logits(lp, synth, torch, dev, stream, peaks, peaks_kind, max_over,
                                    world, rank)
+        torch.cuda.nvtx.range_pop()
 
     backward_item = None
     if not args.no_backward:
+        torch.cuda.nvtx.range_push("lp.bench.backward")
         backward_item = bench_backward(lp, torch, x, dev, stream, peaks, peaks_kind, max_over,
                                        world)
+        torch.cuda.nvtx.range_pop()
 
     # last of the GPU items: its seconds of load would otherwise leave the
     # items after it running in a hotter, more power-capped state
     sweep_item = None
     if not args.no_sweep:
+        torch.cuda.nvtx.range_push("lp.bench.batch_sweep")
         sweep_item = bench_batch_sweep(lp, torch, x, dev, stream, peaks, peaks_kind, max_over)
+        torch.cuda.nvtx.range_pop()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -522,6 +543,7 @@ def run_lp(args):
         "e2e": e2e,
         "gpu_launches": 2 * K,
         "clocks": clocks,
+        "repeats": repeats,
         "backend": lp.lp_backend_id(),
         "logits_path": logits_item,
         "backward_path": backward_item,
