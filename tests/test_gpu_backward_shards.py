@@ -145,3 +145,28 @@ def test_merge_in_place_and_without_grad_W():
     lp.lp_merge_grad_h_partials(no_w, no_w[0])  # the output is partial 0
     torch.cuda.synchronize()
     assert torch.equal(bits(no_w[0]), bits(merged))
+
+
+@pytest.mark.parametrize("T,V", [(20, 64), (33, 192), (17, 320), (3, 128)])
+def test_tiny_quarters(T, V):
+    """Quarters of 16 to 80 columns (one to five 16-deep MMA steps, at most two K
+    blocks), shards of a few W rows: 1, 2 and 4 shards against the single-GPU
+    backward, and the single-GPU backward against the fp64 oracle."""
+    d = 64
+    x = synth.fused_inputs("fused_tiny", device=DEV, T=T, d=d, V=V, seed=T * V)
+    gl, ge = _upstream(T, T + V)
+    _, ent, lse = lp.linear_logprob_lse(x.H, x.W, x.y)
+    gH, gW = lp.linear_logprob_backward(x.H, x.W, x.y, gl, ge, saved_lse=lse, saved_entropy=ent)
+    for n in (1, 2, 4):
+        _, mH, mW = _sharded(x, V, n, gl, ge, lse, ent)
+        torch.cuda.synchronize()
+        assert torch.equal(bits(mH), bits(gH)), n
+        assert torch.equal(bits(mW), bits(gW)), n
+    h = x.H.float().cpu().numpy().astype(np.float64)
+    w = x.W.float().cpu().numpy().astype(np.float64)
+    G = olp.selected_logprob_grad_logits(olp.linear_logits(h, w), x.y.cpu().numpy(),
+                                         gl.double().cpu().numpy(), ge.double().cpu().numpy())
+    bound_h = (2.0 ** -8 + (V / 7 + 9) * 2.0 ** -24) * (np.abs(G) @ np.abs(w)) + 1e-6
+    assert np.all(np.abs(gH.double().cpu().numpy() - G @ w) <= bound_h)
+    bound_w = (2.0 ** -8 + T * 2.0 ** -24) * (np.abs(G).T @ np.abs(h)) + 1e-6
+    assert np.all(np.abs(gW.double().cpu().numpy() - G.T @ h) <= bound_w)
