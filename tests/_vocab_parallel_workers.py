@@ -125,3 +125,37 @@ def gpu_vocab_parallel(rank: int, world: int, init_file: str, out_dir: str, path
         torch.save({"logp": logp.cpu(), "ent": ent.cpu()}, os.path.join(out_dir, f"rank{rank}.pt"))
     finally:
         dist.destroy_process_group()
+
+
+def host_fused_backward(rank: int, world: int, init_file: str, out_dir: str) -> None:
+    """The fused backward's orchestration on CPU: the library's compute calls are
+    replaced by fakes that record their arguments, so what is checked is the
+    shard each rank asks for, the rank order of the gathered partial grad_H and
+    what the merge receives."""
+    from invariant_token_logprobs_gb300 import lp
+    from invariant_token_logprobs_gb300 import vocab_parallel as vp
+    _init(rank, world, init_file)
+    try:
+        calls = {}
+        T, d, V = 3, 8, 4096
+
+        def fake_partials_backward(H, W_shard, y, vocab_total, shard_index, n_shards, lse, ent,
+                                   gl, ge, **kw):
+            calls["shard"] = (shard_index, n_shards, W_shard.shape[0], vocab_total)
+            part = torch.full((T, d), float(shard_index + 1)) + torch.arange(T * d).view(T, d)
+            return part, torch.full((W_shard.shape[0], d), float(-shard_index))
+
+        def fake_merge(parts, stream=None):
+            calls["merged"] = [p.clone() for p in parts]
+            return torch.stack(parts).sum(0)
+
+        lp.linear_logprob_partials_backward = fake_partials_backward
+        lp.merge_grad_h_partials = fake_merge
+        _, n, b, e = vp.shard_of_rank(V)
+        H = torch.zeros((T, d))
+        gH, gW = vp.vocab_parallel_linear_logprob_backward(
+            H, torch.zeros((e - b, d)), torch.zeros(T, dtype=torch.int64), V,
+            torch.zeros(T), torch.zeros(T), torch.zeros(T), None)
+        torch.save({"calls": calls, "gH": gH, "gW": gW}, os.path.join(out_dir, f"rank{rank}.pt"))
+    finally:
+        dist.destroy_process_group()

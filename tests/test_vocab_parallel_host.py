@@ -43,3 +43,23 @@ def test_single_process_is_its_own_group():
     got = vp.gather_partials(part)
     assert len(got) == 1 and got[0] is part
     assert vp.shard_of_rank(151936) == (0, 1, 0, 151936)
+
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_fused_backward_gathers_partials_in_rank_order(world, tmp_path):
+    """Each rank asks for its own shard, every rank's merge receives the partial
+    grad_H of every rank in rank order, and each rank keeps its own grad_W rows."""
+    mp.spawn(workers.host_fused_backward, args=(world, str(tmp_path / "rendezvous"), str(tmp_path)),
+             nprocs=world, join=True)
+    T, d, V = 3, 8, 4096
+    for rank in range(world):
+        res = torch.load(os.path.join(tmp_path, f"rank{rank}.pt"))
+        b, e = lp.vocab_shard_range(V, rank, world)
+        assert res["calls"]["shard"] == (rank, world, e - b, V)
+        merged = res["calls"]["merged"]
+        assert len(merged) == world
+        for src in range(world):
+            expect = torch.full((T, d), float(src + 1)) + torch.arange(T * d).view(T, d)
+            assert torch.equal(merged[src], expect), (rank, src)
+        assert torch.equal(res["gH"], torch.stack(merged).sum(0))
+        assert torch.equal(res["gW"], torch.full((e - b, d), float(-rank)))
