@@ -401,6 +401,34 @@ def run_lp(args):
                "outputs_sha256": hashes[0][:16],
                "note": "logp and entropy of the headline inputs, hashed after each call"}
 
+    # the other two properties the pages grade, on the same inputs (one GPU):
+    # 2 and 4 vocabulary shards merged against the unsharded call, and rows
+    # computed in batches of 1 and 7 against the same rows of the T-row call
+    torch.cuda.nvtx.range_push("lp.bench.properties")
+    ref = torch.cat([logp, ent]).view(torch.int32)
+    tp_equal = {}
+    for n in (2, 4):
+        parts = []
+        for i in range(n):
+            b, e = lp.vocab_shard_range(V, i, n)
+            parts.append(lp.linear_logprob_partials(x.H, x.W[b:e], x.y, V, i, n))
+        m_lp, m_ent = lp.merge_partials(parts)
+        tp_equal[f"tp{n}_equals_tp1"] = bool(torch.equal(torch.cat([m_lp, m_ent]).view(torch.int32),
+                                                         ref))
+    batch_equal = True
+    for r0, rows in ((0, 7), (T // 2, 1), (T - 7, 7)):
+        s_lp, s_ent = lp.linear_logprob(x.H[r0:r0 + rows].contiguous(), x.W,
+                                        x.y[r0:r0 + rows].contiguous())
+        batch_equal &= bool(torch.equal(s_lp.view(torch.int32), logp[r0:r0 + rows].view(torch.int32))
+                            and torch.equal(s_ent.view(torch.int32),
+                                            ent[r0:r0 + rows].view(torch.int32)))
+    torch.cuda.nvtx.range_pop()
+    properties = dict(tp_equal, batch_bitwise=batch_equal,
+                      distinct_results_in_repeats=repeats["distinct_results"],
+                      note="checked on the headline inputs on one GPU after the timed loops: "
+                           "shards' quarter states merged in the fixed order, and sub-batches "
+                           "of 1 and 7 rows, bit for bit against the T-row call")
+
     flops = 2.0 * T * d * V
     w_bytes = 2.0 * V * d + 2.0 * T * d + 8.0 * T + 8.0 * T
     peak_tf = peaks["bf16_tflops"]
@@ -544,6 +572,7 @@ def run_lp(args):
         "gpu_launches": 2 * K,
         "clocks": clocks,
         "repeats": repeats,
+        "properties": properties,
         "backend": lp.lp_backend_id(),
         "logits_path": logits_item,
         "backward_path": backward_item,
