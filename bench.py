@@ -634,7 +634,23 @@ def bench_backward(lp, torch, x, dev, stream, peaks, peaks_kind, max_over, world
         raise RuntimeError("device-side wait gave up in the backward")
     ms16 = max_over(e0.elapsed_time(e1)) / K
     tf16 = flops / (ms16 / 1e3) / 1e12
-    del ws, gW16
+    del gW16
+    # grad_W added into a float32 main gradient (the accumulate mode)
+    main = torch.zeros((V, d), device=dev)
+    for _ in range(2):
+        lp.lp_linear_logprob_backward_ex(x.H, x.W, x.y, 1.0, lse, ent, gl, ge, gH, main, ws,
+                                         accumulate=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(K):
+        lp.lp_linear_logprob_backward_ex(x.H, x.W, x.y, 1.0, lse, ent, gl, ge, gH, main, ws,
+                                         accumulate=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if lp.lp_get_device_error(ws) != 0:
+        raise RuntimeError("device-side wait gave up in the backward")
+    ms_acc = max_over(e0.elapsed_time(e1)) / K
+    del ws, main
     # algorithmic bytes of one call: W read by the logits recompute and by G W,
     # H once, G (bf16 [T, V]) written once and read by both products, the
     # fp32 partial grad_H written and read (28 when V % 64 == 0, else 19),
@@ -647,6 +663,10 @@ def bench_backward(lp, torch, x, dev, stream, peaks, peaks_kind, max_over, world
             "bf16_grad_W": {"us_per_call": ms16 * 1e3, "achieved_tflops": tf16,
                             "frac": tf16 / peaks["bf16_tflops"],
                             "note": "grad_W written in bf16 (lp_linear_logprob_backward_ex)"},
+            "fp32_accumulate": {"us_per_call": ms_acc * 1e3,
+                                "note": "grad_W added into a float32 main gradient "
+                                        "(LP_GRAD_W_FLOAT32_ACCUMULATE): 4 V d more bytes read "
+                                        "than writing it, and no second pass to add it"},
             "gpu_launches_per_call": 3,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"],
                          "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"],

@@ -434,11 +434,17 @@ LP_API lp_status lp_linear_logprob_backward(const void* H, int64_t ld_h, const v
                                             float* grad_H, float* grad_W, void* workspace,
                                             size_t workspace_bytes, void* stream);
 
-/* Element type of grad_W for lp_linear_logprob_backward_ex. */
+/* Element type of grad_W for lp_linear_logprob_backward_ex, and whether it is
+ * written or added to. */
 typedef enum lp_grad_w_dtype {
-  LP_GRAD_W_FLOAT32 = 0,  /* float32 [V, d] */
-  LP_GRAD_W_BFLOAT16 = 1  /* bfloat16 [V, d], each element the float32 result rounded to
-                             nearest even */
+  LP_GRAD_W_FLOAT32 = 0,   /* float32 [V, d], written */
+  LP_GRAD_W_BFLOAT16 = 1,  /* bfloat16 [V, d], each element the float32 result rounded to
+                              nearest even, written */
+  LP_GRAD_W_FLOAT32_ACCUMULATE = 2  /* float32 [V, d] that already holds a gradient (a
+                              trainer's main gradient): grad_W[v, k] + (G^T H)[v, k] is
+                              stored in it, one float32 add per element made by the TMA
+                              unit's reduction (round to nearest; the same bits on every
+                              run) */
 } lp_grad_w_dtype;
 
 /*
@@ -448,8 +454,11 @@ typedef enum lp_grad_w_dtype {
  * the same float32 products rounded once to bf16 on the way out, which halves
  * the product's 4 V d bytes of output (the trainer of the RL-Kernel H100 PCP
  * evidence record keeps bf16 weights; its fp32 main gradients can accumulate
- * these).  If a device-side wait gives up, the bf16 output is NaN too.  Other
- * arguments as in lp_linear_logprob_backward; an unknown dtype gives
+ * these).  With LP_GRAD_W_FLOAT32_ACCUMULATE the product is added into the
+ * float32 grad_W the caller passes (gradient accumulation over micro-batches
+ * without a second pass over 4 V d bytes).  If a device-side wait gives up,
+ * grad_W is NaN (also when accumulating: the previous contents are lost).
+ * Other arguments as in lp_linear_logprob_backward; an unknown dtype gives
  * LP_ERR_INVALID_ARGUMENT.
  */
 LP_API lp_status lp_linear_logprob_backward_ex(const void* H, int64_t ld_h, const void* W,

@@ -533,7 +533,8 @@ lp_status lp_linear_logprob_backward_ex(const void* H, int64_t ld_h, const void*
                                         void* stream) {
   lp::TauArgs tau;
   if (!lp::make_tau(temperature, &tau)) return LP_ERR_INVALID_ARGUMENT;
-  if (grad_W_dtype != LP_GRAD_W_FLOAT32 && grad_W_dtype != LP_GRAD_W_BFLOAT16)
+  if (grad_W_dtype != LP_GRAD_W_FLOAT32 && grad_W_dtype != LP_GRAD_W_BFLOAT16 &&
+      grad_W_dtype != LP_GRAD_W_FLOAT32_ACCUMULATE)
     return LP_ERR_INVALID_ARGUMENT;
   lp_status st = lp::check_fused_args(H, ld_h, W, ld_w, targets, T, d, V);
   if (st != LP_OK || T == 0) return st;
@@ -552,7 +553,7 @@ lp_status lp_linear_logprob_backward_ex(const void* H, int64_t ld_h, const void*
   if (st != LP_OK) return st;
   return lp::launch_linear_backward(dev, H, ld_h, W, ld_w, targets, T, d, V, V, 0, 4, tau,
                                     saved_lse, saved_entropy, grad_logp, grad_entropy, grad_H,
-                                    grad_W, grad_W_dtype == LP_GRAD_W_BFLOAT16, workspace,
+                                    grad_W, grad_W_dtype, workspace,
                                     static_cast<cudaStream_t>(stream));
 }
 
@@ -578,7 +579,8 @@ lp_status lp_linear_logprob_partials_backward(
     void* workspace, size_t workspace_bytes, void* stream) {
   lp::TauArgs tau;
   if (!lp::make_tau(temperature, &tau)) return LP_ERR_INVALID_ARGUMENT;
-  if (grad_W_dtype != LP_GRAD_W_FLOAT32 && grad_W_dtype != LP_GRAD_W_BFLOAT16)
+  if (grad_W_dtype != LP_GRAD_W_FLOAT32 && grad_W_dtype != LP_GRAD_W_BFLOAT16 &&
+      grad_W_dtype != LP_GRAD_W_FLOAT32_ACCUMULATE)
     return LP_ERR_INVALID_ARGUMENT;
   lp_status st = lp::check_shard(shard_index, n_shards);
   if (st != LP_OK) return st;
@@ -610,7 +612,7 @@ lp_status lp_linear_logprob_partials_backward(
   return lp::launch_linear_backward(dev, H, ld_h, W_shard, ld_w, targets, T, d, end - begin,
                                     vocab_total, q_first, n_q, tau, saved_lse, saved_entropy,
                                     grad_logp, grad_entropy, grad_H_partial, grad_W_shard,
-                                    grad_W_dtype == LP_GRAD_W_BFLOAT16, workspace,
+                                    grad_W_dtype, workspace,
                                     static_cast<cudaStream_t>(stream));
 }
 

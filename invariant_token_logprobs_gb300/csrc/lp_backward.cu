@@ -387,6 +387,7 @@ struct GemmArgs {
   int n_split;      // matrices of C (split products)
   uint32_t* err;
   int out_bf16;     // C is bf16 (32 x 64 boxes) instead of fp32 (32 x 32 boxes)
+  int out_add;      // fp32 boxes are added into C (TMA reduction) instead of stored
   SplitSumSide side;
   // NaN fill of poison_out[0, poison_n) (C's type) by the last CTA to finish
   // when any of the call's four error words is set (ticket == nullptr: none);
@@ -418,6 +419,19 @@ __device__ __forceinline__ void bulk_store_3d(const CUtensorMap* map, int c0, in
   asm volatile(
       "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
           reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(src)
+      : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// The box added element by element into C (an fp32 add in the memory system;
+// every element of C is the target of exactly one box of one launch, so the
+// result does not depend on timing) instead of stored.
+__device__ __forceinline__ void bulk_reduce_add_3d(const CUtensorMap* map, int c0, int c1, int c2,
+                                                   uint32_t src) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], "
+      "[%4];" ::"l"(reinterpret_cast<uint64_t>(map)),
       "r"(c0), "r"(c1), "r"(c2), "r"(src)
       : "memory");
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
@@ -484,8 +498,13 @@ struct GemmEpilogue {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0 && LP_CHECK(col < a->N && row0 < a->M && s >= 0 && s < a->n_split,
-                                  kChkOutBox))
-          bulk_store_3d(&a->tmC, static_cast<int>(col), static_cast<int>(row0), s, smem_u32(box));
+                                  kChkOutBox)) {
+          if (a->out_add)
+            bulk_reduce_add_3d(&a->tmC, static_cast<int>(col), static_cast<int>(row0), s,
+                               smem_u32(box));
+          else
+            bulk_store_3d(&a->tmC, static_cast<int>(col), static_cast<int>(row0), s, smem_u32(box));
+        }
         if (++next == kBoxes) next = 0;
       }
     }
@@ -623,7 +642,7 @@ template <bool kAMn, bool kBMn>
 lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a, const void* B,
                       int64_t N, int64_t ld_b, int64_t K, int64_t seg_w, int n_split, void* C,
                       int64_t ldc, int64_t split_stride, uint32_t* err, cudaStream_t stream,
-                      int* n_split_out, bool nb_fastest, bool out_bf16 = false,
+                      int* n_split_out, bool nb_fastest, int out_mode = LP_GRAD_W_FLOAT32,
                       const GemmExtras& x = GemmExtras()) {
   static PerContextOnce attr;
   if (attr.run(dev.ctx_id, [] {
@@ -663,7 +682,9 @@ lp_status launch_gemm(const Device& dev, const void* A, int64_t M, int64_t ld_a,
   g.N = N;
   g.err = err;
   g.n_split = n_split;
+  const bool out_bf16 = out_mode == LP_GRAD_W_BFLOAT16;
   g.out_bf16 = out_bf16 ? 1 : 0;
+  g.out_add = out_mode == LP_GRAD_W_FLOAT32_ACCUMULATE ? 1 : 0;
   g.side = x.side;
   g.ticket = x.ticket;
   g.err_all = x.err_all;
@@ -758,7 +779,7 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
                                  const TauArgs& tau, const float* saved_lse,
                                  const float* saved_entropy, const float* g_logp,
                                  const float* g_ent, float* grad_h, void* grad_w,
-                                 bool grad_w_bf16, void* workspace, cudaStream_t stream) {
+                                 int grad_w_mode, void* workspace, cudaStream_t stream) {
   if (T > 0 && T < kSmallRows) {
     const SmallLayout S = small_layout(d, V, V_total);
     uint8_t* base = static_cast<uint8_t*>(workspace);
@@ -777,7 +798,7 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
     if (cudaGetLastError() != cudaSuccess) return LP_ERR_CUDA;
     const lp_status st =
         launch_linear_backward(dev, h16, d8, W, ld_w, y16, kSmallRows, d, V, V_total, q_first,
-                               n_q, tau, lse16, ent16, gl16, ge16, gh16, grad_w, grad_w_bf16,
+                               n_q, tau, lse16, ent16, gl16, ge16, gh16, grad_w, grad_w_mode,
                                workspace, stream);
     if (st != LP_OK) return st;
     lp_copy_rows_kernel<<<static_cast<unsigned>((T * d + 255) / 256), 256, 0, stream>>>(
@@ -896,7 +917,7 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
   x.withhold_first_load = fault_injection() == 2 ? 1 : 0;
   // column blocks fastest: a block of G is used by 16 consecutive units
   return launch_gemm<true, true>(dev, G, V, L.V8, H, d, ld_h, T, 0, 1, grad_w, d, 0, err + 3,
-                                 stream, nullptr, true, grad_w_bf16, x);
+                                 stream, nullptr, true, grad_w_mode, x);
 }
 
 lp_status launch_merge_grad_h(const Device& dev, const float* const* shard_grad_h, int n_shards,

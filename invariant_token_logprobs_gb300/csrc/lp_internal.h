@@ -136,7 +136,7 @@ lp_status launch_linear_backward(const Device& dev, const void* H, int64_t ld_h,
                                  const TauArgs& tau, const float* saved_lse,
                                  const float* saved_entropy, const float* g_logp,
                                  const float* g_ent, float* grad_h, void* grad_w,
-                                 bool grad_w_bf16, void* workspace, cudaStream_t stream);
+                                 int grad_w_mode, void* workspace, cudaStream_t stream);
 // grad_h [n] = the n_shards (1, 2, 4) partial dH in the quarter tree's order
 // (n a multiple of 4, every pointer 16-byte aligned)
 lp_status launch_merge_grad_h(const Device& dev, const float* const* shard_grad_h, int n_shards,

@@ -57,6 +57,7 @@ __all__ = [
     "merge_grad_h_partials",
     "GRAD_W_FLOAT32",
     "GRAD_W_BFLOAT16",
+    "GRAD_W_FLOAT32_ACCUMULATE",
     "linear_logprob_lse",
     "linear_logprob_backward",
     "lp_get_device_error",
@@ -407,21 +408,30 @@ def lp_linear_logprob_backward(H, W, targets, temperature, saved_lse, saved_entr
 
 GRAD_W_FLOAT32 = 0
 GRAD_W_BFLOAT16 = 1
+GRAD_W_FLOAT32_ACCUMULATE = 2
+
+
+def _grad_w_dtype_code(grad_W, accumulate: bool = False) -> int:
+    if accumulate:
+        if grad_W is None or grad_W.dtype != torch.float32:
+            raise TypeError("accumulating needs a float32 grad_W")
+        return GRAD_W_FLOAT32_ACCUMULATE
+    if grad_W is None or grad_W.dtype == torch.float32:
+        return GRAD_W_FLOAT32
+    if grad_W.dtype == torch.bfloat16:
+        return GRAD_W_BFLOAT16
+    raise TypeError("grad_W must be float32 or bfloat16")
 
 
 def lp_linear_logprob_backward_ex(H, W, targets, temperature, saved_lse, saved_entropy,
                                   grad_logp, grad_entropy, grad_H, grad_W, workspace,
-                                  stream=None) -> None:
-    """The backward with grad_W float32 or bfloat16 (taken from grad_W's dtype)."""
+                                  stream=None, accumulate: bool = False) -> None:
+    """The backward with grad_W float32 or bfloat16 (taken from grad_W's dtype);
+    accumulate=True adds the product into the float32 grad_W instead."""
     _check_bf16(H, W, targets)
     T, d = H.shape
     V = W.shape[0]
-    dtype = GRAD_W_FLOAT32
-    if grad_W is not None:
-        if grad_W.dtype == torch.bfloat16:
-            dtype = GRAD_W_BFLOAT16
-        elif grad_W.dtype != torch.float32:
-            raise TypeError("grad_W must be float32 or bfloat16")
+    dtype = _grad_w_dtype_code(grad_W, accumulate)
     _check("lp_linear_logprob_backward_ex", load().lp_linear_logprob_backward_ex(
         _ptr(H), _row_stride(H), _ptr(W), _row_stride(W), _ptr(targets), T, d, V,
         float(temperature), _ptr(saved_lse), _ptr(saved_entropy), _ptr(grad_logp),
@@ -429,12 +439,6 @@ def lp_linear_logprob_backward_ex(H, W, targets, temperature, saved_lse, saved_e
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
-def _grad_w_dtype_code(grad_W) -> int:
-    if grad_W is None or grad_W.dtype == torch.float32:
-        return GRAD_W_FLOAT32
-    if grad_W.dtype == torch.bfloat16:
-        return GRAD_W_BFLOAT16
-    raise TypeError("grad_W must be float32 or bfloat16")
 
 
 def lp_linear_logprob_partials_backward_workspace_size(T: int, d: int, vocab_total: int,
@@ -446,15 +450,16 @@ def lp_linear_logprob_partials_backward_workspace_size(T: int, d: int, vocab_tot
 def lp_linear_logprob_partials_backward(H, W_shard, targets, vocab_total, shard_index, n_shards,
                                         temperature, saved_lse, saved_entropy, grad_logp,
                                         grad_entropy, grad_H_partial, grad_W_shard, workspace,
-                                        stream=None) -> None:
-    """The shard's backward (grad_W_shard float32 or bfloat16, from its dtype, or None)."""
+                                        stream=None, accumulate: bool = False) -> None:
+    """The shard's backward (grad_W_shard float32 or bfloat16, from its dtype, or None;
+    accumulate=True adds into the float32 grad_W_shard)."""
     _check_bf16(H, W_shard, targets)
     T, d = H.shape
     _check("lp_linear_logprob_partials_backward", load().lp_linear_logprob_partials_backward(
         _ptr(H), _row_stride(H), _ptr(W_shard), _row_stride(W_shard), _ptr(targets), T, d,
         vocab_total, shard_index, n_shards, float(temperature), _ptr(saved_lse),
         _ptr(saved_entropy), _ptr(grad_logp), _ptr(grad_entropy), _ptr(grad_H_partial),
-        _ptr(grad_W_shard), _grad_w_dtype_code(grad_W_shard), _ptr(workspace),
+        _ptr(grad_W_shard), _grad_w_dtype_code(grad_W_shard, accumulate), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
@@ -508,13 +513,21 @@ def linear_logprob_lse(H, W, y, temperature: float = 1.0, workspace=None, stream
 
 def linear_logprob_backward(H, W, y, grad_logp=None, grad_entropy=None, temperature: float = 1.0,
                             with_grad_W: bool = True, saved_lse=None, saved_entropy=None,
-                            workspace=None, stream=None, grad_W_dtype=torch.float32):
-    """(grad_H [T, d] fp32, grad_W [V, d] fp32 / bf16 or None) of the fused path."""
+                            workspace=None, stream=None, grad_W_dtype=torch.float32,
+                            accumulate_into=None):
+    """(grad_H [T, d] fp32, grad_W [V, d] fp32 / bf16 or None) of the fused path;
+    with accumulate_into (a float32 [V, d] tensor, e.g. a main gradient) the
+    product is added into it and it is returned as grad_W."""
     T, d = H.shape
     V = W.shape[0]
     if workspace is None:
         workspace = _workspace(lp_linear_logprob_backward_workspace_size(T, d, V), H.device)
     gH = torch.empty((T, d), dtype=torch.float32, device=H.device)
+    if accumulate_into is not None:
+        lp_linear_logprob_backward_ex(H, W, y, temperature, saved_lse, saved_entropy, grad_logp,
+                                      grad_entropy, gH, accumulate_into, workspace, stream,
+                                      accumulate=True)
+        return gH, accumulate_into
     gW = torch.empty((V, d), dtype=grad_W_dtype, device=H.device) if with_grad_W else None
     if grad_W_dtype == torch.float32:
         lp_linear_logprob_backward(H, W, y, temperature, saved_lse, saved_entropy, grad_logp,

@@ -105,5 +105,9 @@ def run_cases(lp, synth) -> dict:
                 keep(f"bwd{T}.shard{n}.{i}", ph, pw)
                 parts.append(ph)
             keep(f"bwd{T}.shard{n}.merged", lp.merge_grad_h_partials(parts))
+        # grad_W added into a main gradient
+        main = torch.ones((V, d), device=DEV)
+        keep(f"bwd{T}.acc", *lp.linear_logprob_backward(f.H, f.W, f.y, gl, ge, saved_lse=lse,
+                                                        saved_entropy=ent, accumulate_into=main))
     torch.cuda.synchronize()
     return out

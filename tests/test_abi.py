@@ -145,6 +145,11 @@ def test_backward_argument_errors(lib):
     assert call(13, A + 4) == MISALIGNED              # grad_H 16-byte aligned
     assert call(16, ws - 1) == WS_SMALL
     assert lp.lp_linear_logprob_backward_workspace_size(-1, 8, 8) == 0
+    # the _ex form: grad_W written as float32 (0) or bf16 (1), or added into (2)
+    ex = lib.lp_linear_logprob_backward_ex
+    assert ex(*base[:15], 3, *base[15:]) == INVALID
+    assert ex(*base[:15], -1, *base[15:]) == INVALID
+    assert ex(*base[:5], 0, *base[6:15], 2, *base[15:]) == OK  # T == 0
 
 
 def _backward_ws(T, d, V, V_total):
@@ -192,7 +197,7 @@ def test_shard_backward_argument_errors(lib):
     assert call(lse=None) == INVALID                # a shard needs the merged statistics
     assert call(ent=None) == INVALID
     assert call(gl=None, ge=None) == INVALID        # no upstream gradient
-    assert call(dt=2) == INVALID                    # grad_W dtype
+    assert call(dt=3) == INVALID                    # grad_W dtype (0, 1, 2 are valid)
     assert call(tau=0.0) == INVALID
     assert call(gH=None) == INVALID
     assert call(gH=A + 8) == MISALIGNED
