@@ -476,20 +476,26 @@ def lp_merge_grad_h_partials(shard_grad_h: Sequence[torch.Tensor], grad_H, strea
 def linear_logprob_partials_backward(H, W_shard, y, vocab_total, shard_index, n_shards,
                                      saved_lse, saved_entropy, grad_logp=None, grad_entropy=None,
                                      temperature: float = 1.0, with_grad_W: bool = True,
-                                     grad_W_dtype=torch.float32, workspace=None, stream=None):
+                                     grad_W_dtype=torch.float32, workspace=None, stream=None,
+                                     accumulate_into=None):
     """(grad_H partial [T, d] fp32, grad_W_shard [rows of W_shard, d] or None) of one
-    vocabulary shard, from the merged rows' log Z and entropy."""
+    vocabulary shard, from the merged rows' log Z and entropy; with accumulate_into
+    (float32 [rows of W_shard, d]) the shard's grad_W is added into it."""
     T, d = H.shape
     if workspace is None:
         workspace = _workspace(
             lp_linear_logprob_partials_backward_workspace_size(T, d, vocab_total, n_shards),
             H.device)
     gH = torch.empty((T, d), dtype=torch.float32, device=H.device)
-    gW = (torch.empty((W_shard.shape[0], d), dtype=grad_W_dtype, device=H.device)
-          if with_grad_W else None)
+    if accumulate_into is not None:
+        gW = accumulate_into
+    else:
+        gW = (torch.empty((W_shard.shape[0], d), dtype=grad_W_dtype, device=H.device)
+              if with_grad_W else None)
     lp_linear_logprob_partials_backward(H, W_shard, y, vocab_total, shard_index, n_shards,
                                         temperature, saved_lse, saved_entropy, grad_logp,
-                                        grad_entropy, gH, gW, workspace, stream)
+                                        grad_entropy, gH, gW, workspace, stream,
+                                        accumulate=accumulate_into is not None)
     return gH, gW
 
 

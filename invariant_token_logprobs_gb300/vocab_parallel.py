@@ -157,18 +157,19 @@ def vocab_parallel_linear_logprob_backward(H: torch.Tensor, W_shard: torch.Tenso
                                            grad_logp=None, grad_entropy=None, group=None,
                                            temperature: float = 1.0, with_grad_W: bool = True,
                                            grad_W_dtype=torch.float32, workspace=None,
-                                           stream=None):
+                                           stream=None, accumulate_into=None):
     """(grad_H [T, d] fp32, grad_W_shard [end - begin, d] or None) from the merged
     rows' log Z and entropy (vocab_parallel_linear_logprob_lse): grad_H is the
     same on every rank and equal to the single-GPU result bit for bit, and
-    grad_W_shard is rows begin..end of the single-GPU grad_W."""
+    grad_W_shard is rows begin..end of the single-GPU grad_W (added into
+    accumulate_into, this rank's float32 main gradient rows, when given)."""
     rank, n, b, e = shard_of_rank(vocab_total, group)
     _check_w_shard(W_shard, rank, b, e)
     with _on(stream):
         part, gW = lp.linear_logprob_partials_backward(
             H, W_shard, y, vocab_total, rank, n, saved_lse, saved_entropy, grad_logp,
             grad_entropy, temperature=temperature, with_grad_W=with_grad_W,
-            grad_W_dtype=grad_W_dtype, workspace=workspace)
+            grad_W_dtype=grad_W_dtype, workspace=workspace, accumulate_into=accumulate_into)
         gathered = gather_partials(part, group)
         return lp.merge_grad_h_partials(gathered), gW
 

@@ -83,6 +83,15 @@ def test_shards_accumulate_their_rows():
                                                part, main[b:e], ws, accumulate=True)
     torch.cuda.synchronize()
     assert torch.equal(bits(main), bits(expect))
+    # the convenience form, two shards, on top
+    expect = expect + gW
+    for i in range(2):
+        b, e = lp.vocab_shard_range(V, i, 2)
+        _, rows = lp.linear_logprob_partials_backward(x.H, x.W[b:e], x.y, V, i, 2, lse, ent, gl,
+                                                      ge, accumulate_into=main[b:e])
+        assert rows.data_ptr() == main[b:e].data_ptr()
+    torch.cuda.synchronize()
+    assert torch.equal(bits(main), bits(expect))
 
 
 def test_accumulate_needs_float32():
