@@ -260,3 +260,41 @@ def test_shard_backward_graph_replay_bytes_equal_eager():
         torch.cuda.synchronize()
         assert torch.equal(ref_h.view(torch.int32), got_h.view(torch.int32)), seed
         assert torch.equal(ref_w.view(torch.int32), got_w.view(torch.int32)), seed
+
+
+def test_accumulating_backward_graph_replay_bytes_equal_eager():
+    """The backward adding grad_W into a main gradient, captured once: two
+    replays add what two eager calls add, byte for byte."""
+    T, d, V = 32, 128, 8192
+    x = synth.fused_inputs("fused_tiny", device=DEV, T=T, d=d, V=V, seed=7)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(8)
+    gl = torch.randn(T, generator=g, device=DEV)
+    ge = torch.randn(T, generator=g, device=DEV)
+    lse = torch.empty(T, device=DEV)
+    ent = torch.empty(T, device=DEV)
+    logp = torch.empty(T, device=DEV)
+    fws = torch.empty(lp.lp_linear_logprob_workspace_size(T, d, V), dtype=torch.uint8, device=DEV)
+    lp.lp_linear_logprob_lse(x.H, x.W, x.y, 1.0, logp, ent, lse, fws)
+    ws = torch.empty(lp.lp_linear_logprob_backward_workspace_size(T, d, V), dtype=torch.uint8,
+                     device=DEV)
+    gH = torch.empty((T, d), device=DEV)
+    main = torch.randn((V, d), generator=g, device=DEV)
+    start = main.clone()
+
+    def call():
+        lp.lp_linear_logprob_backward_ex(x.H, x.W, x.y, 1.0, lse, ent, gl, ge, gH, main, ws,
+                                         accumulate=True)
+
+    graph = _capture(call)  # a warm-up call inside _capture may run eagerly: start again
+    main.copy_(start)
+    torch.cuda.synchronize()
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    replayed = main.clone()
+    main.copy_(start)
+    call()
+    call()
+    torch.cuda.synchronize()
+    assert torch.equal(bits(replayed.reshape(-1)), bits(main.reshape(-1)))
