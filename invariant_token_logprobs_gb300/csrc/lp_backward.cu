@@ -17,18 +17,25 @@
 //   2. lp_grad_kernel: z tiles recomputed in tensor memory; the epilogue forms
 //      G in fp32 and stores it in bf16 as G [T, V];
 //   3. lp_gemm_kernel<K-major A, N-major B>: dH = G W, reading W [V, d] as an
-//      N-major operand, over 19 fixed vocabulary ranges (partial products in
-//      fp32);
+//      N-major operand, over fixed vocabulary ranges (partial products in
+//      fp32): 7 per quarter of the vocabulary when V % 64 == 0, else 19 of the
+//      whole vocabulary;
 //   4. lp_gemm_kernel<M-major A, N-major B>: dW = G^T H, reading G [T, V] as an
 //      M-major operand and H [T, d] as an N-major one.  A seventh warp per CTA
-//      adds the 19 ranges of dH in order meanwhile (lp_split_sum_kernel does
-//      it on its own when dW is not asked for), and the last CTA to finish
-//      fills dW with NaN if a wait of the call gave up.
+//      adds the ranges of dH meanwhile — each quarter's in order, then
+//      (Q0 + Q1) + (Q2 + Q3) — (lp_split_sum_kernel does it on its own when
+//      dW is not asked for), and the last CTA to finish fills dW with NaN if
+//      a wait of the call gave up.
 // Both products write their output through TMA bulk stores from a swizzled
-// staging area.  No operand is transposed in memory.  Every output
-// element is produced by one CTA pair with a fixed K order and split sums are
-// added in a fixed order: the results are deterministic, and a row of dH
-// depends only on that row's inputs (not on T or its offset).
+// staging area (dW may instead be added into a main gradient with the TMA
+// reduction).  No operand is transposed in memory.  Every output element is
+// produced by one CTA pair with a fixed K order and split sums are added in a
+// fixed order: the results are deterministic, and a row of dH depends only on
+// that row's inputs (not on T or its offset).  A call may cover a shard of
+// whole vocabulary quarters (W's rows of the shard, global targets, the merged
+// rows' statistics): its dW rows are those of the whole call, and its dH is
+// the quarter tree's subtree of its quarters, to be merged by
+// launch_merge_grad_h.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
