@@ -496,8 +496,9 @@ LP_API lp_status lp_linear_logprob_backward_ex(const void* H, int64_t ld_h, cons
  *   saved_lse, saved_entropy  [T] float32 of the merged rows (required).
  *   grad_logp, grad_entropy   as in lp_linear_logprob_backward.
  *   grad_H_partial [T, d] float32 output, dense rows, 16-byte aligned.
- *   grad_W_shard   [end - begin, d] output of grad_W_dtype, dense rows,
- *               16-byte aligned, or NULL to skip it.
+ *   grad_W_shard   [end - begin, d] output of grad_W_dtype (an lp_grad_w_dtype:
+ *               written as float32 or bfloat16, or added into a float32 main
+ *               gradient), dense rows, 16-byte aligned, or NULL to skip it.
  *   workspace   256-byte aligned, at least
  *               lp_linear_logprob_partials_backward_workspace_size(T, d,
  *               vocab_total, n_shards) bytes.
