@@ -74,6 +74,8 @@ def parse_args(argv=None):
     p.add_argument("--no-logits", action="store_true", help="skip the logits-path line item")
     p.add_argument("--no-backward", action="store_true", help="skip the backward line item")
     p.add_argument("--no-sweep", action="store_true", help="skip the batch-size sweep item")
+    p.add_argument("--no-tp", action="store_true",
+                   help="skip the per-rank vocabulary-parallel latency item")
     p.add_argument("--tp", type=int, default=0,
                    help="vocabulary-parallel ranks, 1, 2 or 4 (must equal the number of "
                         "processes); 0: the default replica mode")
@@ -546,6 +548,12 @@ def run_lp(args):
                                        world)
         torch.cuda.nvtx.range_pop()
 
+    tp_item = None
+    if not args.no_tp and world == 1:
+        torch.cuda.nvtx.range_push("lp.bench.vocab_parallel")
+        tp_item = bench_vocab_parallel(lp, torch, x, dev, stream)
+        torch.cuda.nvtx.range_pop()
+
     # last of the GPU items: its seconds of load would otherwise leave the
     # items after it running in a hotter, more power-capped state
     sweep_item = None
@@ -576,6 +584,7 @@ def run_lp(args):
         "backend": lp.lp_backend_id(),
         "logits_path": logits_item,
         "backward_path": backward_item,
+        "vocab_parallel": tp_item,
         "batch_sweep": sweep_item,
     }
     if rank == 0:
@@ -583,6 +592,71 @@ def run_lp(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def bench_vocab_parallel(lp, torch, x, dev, stream):
+    """Line item: what one rank of a 2- or 4-way vocabulary split runs at the
+    headline shape, timed on this GPU (the ranks' shards are the same size):
+    the forward (its shard's quarter states, then the merge of all ranks'
+    states) and the training backward (its shard's backward, then the merge of
+    all ranks' partial grad_H).  The all-gathers between them are not included
+    (one GPU): they move 32 T bytes per quarter and 4 T d bytes per rank."""
+    T, d = x.H.shape
+    V = x.W.shape[0]
+    g = torch.Generator(device=dev)
+    g.manual_seed(9)
+    gl = torch.randn(T, generator=g, device=dev)
+    ge = torch.randn(T, generator=g, device=dev)
+    logp, ent, lse = lp.linear_logprob_lse(x.H, x.W, x.y)
+    out = {"workload": "fused_qwen3_8b, one rank's share", "T": T, "d": d, "V": V,
+           "note": "per-rank kernels and merges on one GPU; all-gathers excluded"}
+
+    def timed(fn, n=10):
+        for _ in range(2):
+            fn()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n * 1e3
+
+    for n in (2, 4):
+        b, e = lp.vocab_shard_range(V, 0, n)
+        w0 = x.W[b:e]
+        fws = torch.empty(lp.lp_linear_logprob_partials_workspace_size(T, d, V, n),
+                          dtype=torch.uint8, device=dev)
+        part = torch.empty((T, 4 // n, lp.STATE_FLOATS), device=dev)
+        parts = [part] * n  # every rank's states have this shape; the merge reads them all
+        m_lp = torch.empty(T, device=dev)
+        m_ent = torch.empty(T, device=dev)
+        m_lse = torch.empty(T, device=dev)
+
+        def fwd():
+            lp.lp_linear_logprob_partials(x.H, w0, x.y, V, 0, n, part, fws)
+            lp.lp_merge_partials_lse(parts, T, m_lp, m_ent, m_lse)
+
+        bws = torch.empty(lp.lp_linear_logprob_partials_backward_workspace_size(T, d, V, n),
+                          dtype=torch.uint8, device=dev)
+        gh_part = torch.empty((T, d), device=dev)
+        gw_rows = torch.empty((e - b, d), device=dev)
+        gh_parts = [gh_part] * n
+        gH = torch.empty((T, d), device=dev)
+
+        def bwd():
+            lp.lp_linear_logprob_partials_backward(x.H, w0, x.y, V, 0, n, 1.0, lse, ent, gl, ge,
+                                                   gh_part, gw_rows, bws)
+            lp.lp_merge_grad_h_partials(gh_parts, gH)
+
+        f_us = timed(fwd)
+        b_us = timed(bwd)
+        if lp.lp_get_device_error(bws) != 0 or lp.lp_get_device_error(fws) != 0:
+            raise RuntimeError("device-side wait gave up in the vocabulary-parallel item")
+        out[f"tp{n}"] = {"forward_us_per_rank": f_us, "backward_us_per_rank": b_us}
+    return out
 
 
 def bench_backward(lp, torch, x, dev, stream, peaks, peaks_kind, max_over, world):
