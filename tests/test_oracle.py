@@ -1,8 +1,8 @@
 """Pins for the fp64 oracle: closed forms, worked examples, brute force,
 invariants and planted mistakes.  CPU only.
 
-The oracle must be pinned to something other than itself before it can judge
-the CUDA path.  Each ``pin_*`` below takes an implementation (the oracle, or a
+The oracle must be pinned to something other than itself before the CUDA
+path is checked against it.  Each ``pin_*`` below takes an implementation (the oracle, or a
 copy with a planted mistake) and raises AssertionError when it disagrees with
 mathematics fixed independently of the oracle's own formula:
 
