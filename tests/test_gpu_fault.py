@@ -81,3 +81,35 @@ def test_backward_withheld_load_poisons_grad_W(dtype):
     torch.cuda.synchronize()
     assert lp.lp_get_device_error(ws) == 0
     assert torch.equal(bits(gh), bits(ref_h)) and torch.equal(_bits16(gw), _bits16(ref_w))
+
+
+def test_backward_withheld_load_poisons_an_accumulated_grad_W():
+    """Accumulating into a main gradient when a wait of the grad_W product gives
+    up: the main gradient is NaN afterwards (documented), grad_H is exact, and
+    the next accumulating call adds exactly."""
+    lp.load()
+    x = synth.fused_inputs("fused_tiny", device=DEV)
+    T, d = x.H.shape
+    V = x.W.shape[0]
+    g = torch.Generator().manual_seed(6)
+    gl = torch.randn(T, generator=g).to(DEV)
+    ge = torch.randn(T, generator=g).to(DEV)
+    ref_h, ref_w = lp.linear_logprob_backward(x.H, x.W, x.y, gl, ge)
+    ws = torch.empty(lp.lp_linear_logprob_backward_workspace_size(T, d, V), dtype=torch.uint8,
+                     device=DEV)
+    main = torch.ones((V, d), device=DEV)
+    lp.lp_set_fault_injection(2)
+    try:
+        gh, _ = lp.linear_logprob_backward(x.H, x.W, x.y, gl, ge, workspace=ws,
+                                           accumulate_into=main)
+        torch.cuda.synchronize()
+    finally:
+        lp.lp_set_fault_injection(0)
+    assert lp.lp_get_device_error(ws) != 0
+    assert torch.isnan(main).all()
+    assert torch.equal(bits(gh), bits(ref_h))
+    main.fill_(1.0)
+    lp.linear_logprob_backward(x.H, x.W, x.y, gl, ge, workspace=ws, accumulate_into=main)
+    torch.cuda.synchronize()
+    assert lp.lp_get_device_error(ws) == 0
+    assert torch.equal(bits(main), bits(1.0 + ref_w))
