@@ -31,7 +31,8 @@ def max_err(gpu: torch.Tensor, ref: np.ndarray) -> float:
     g = gpu.double().cpu().numpy()
     both_nan = np.isnan(g) & np.isnan(ref)
     same_inf = np.isinf(g) & np.isinf(ref) & (np.sign(g) == np.sign(ref))
-    diff = np.where(both_nan | same_inf, 0.0, np.abs(g - ref))
+    with np.errstate(invalid="ignore"):  # inf - inf where both are the same infinity
+        diff = np.where(both_nan | same_inf, 0.0, np.abs(g - ref))
     diff = np.where(np.isnan(diff), np.inf, diff)
     return float(diff.max()) if diff.size else 0.0
 
