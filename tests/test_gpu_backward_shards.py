@@ -55,6 +55,7 @@ def _sharded(x, V, n, gl, ge, lse, ent, tau=1.0, dtype=torch.float32):
     (300, 512, 20480, 0.7, torch.float32),   # ragged row blocks, temperature
     (5, 64, 4096 + 64, 1.0, torch.bfloat16),  # the padded small batch, bf16 grad_W
     (129, 128, 64 * 1187, 1.0, torch.float32),  # quarters of 18992: not a multiple of 64
+    (1100, 256, 40960, 0.8, torch.float32),  # five row blocks (ragged), the wide gradient ring
 ])
 def test_shards_equal_single_gpu(T, d, V, tau, dtype):
     x = synth.fused_inputs("fused_tiny", device=DEV, T=T, d=d, V=V, seed=T + d)
